@@ -1,0 +1,186 @@
+"""fp64 CPU oracle for blockwise ring attention and shared-prefix fan-out.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product path (``ring_context_parallelism_gb300``) never imports it and shares
+no code with it.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, double precision, OpenMP
+over queries); this module compiles it with gcc on first use and marshals numpy
+arrays through ctypes.  Each function's docstring cites the passage it follows.
+
+Pins (all in ``tests/test_oracle_pins.py``): the ring-simulator worked example
+of "Agentic Multimodal Distributed Systems" section 8, closed forms, an
+arbitrary-precision brute force, torch's float64 softmax, the log-sum-exp
+gradient identity, and the invariances the pages state (KV order, shard count,
+partition + merge, GQA = repeated-KV MHA, fan-out = per-branch attention).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DTYPES = {"f32": 0, "bf16": 1, "f64": 2}
+
+
+def build(force: bool = False, mutant: int = 0, out: str | None = None) -> str:
+    """Compile attn_oracle.c into liboracle.so (gcc, -O2, OpenMP).
+
+    ``mutant`` > 0 builds a copy with one deliberately planted mistake (for the
+    test that checks the pins catch it) into ``out``."""
+    path = out or _LIB_PATH
+    if (not force and not mutant and os.path.exists(path)
+            and os.path.getmtime(path) >= os.path.getmtime(_SRC)):
+        return path
+    tmp = path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11", f"-DORACLE_MUTANT={int(mutant)}",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, path)
+    return path
+
+
+def use_library(path: str | None):
+    """Swap the loaded oracle library (None: back to the real oracle).  Test-only."""
+    global _lib
+    with _lock:
+        _lib = None if path is None else _bind(ctypes.CDLL(path))
+
+
+def _bind(lib):
+    vp, i, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.oracle_attention.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, i, vp, i64, vp, vp]
+    lib.oracle_attention.restype = i
+    lib.oracle_fanout.argtypes = [vp, vp, i, i, vp, vp, i, vp, vp, i, i, i, i, i, vp, i64, vp, vp]
+    lib.oracle_fanout.restype = i
+    lib.oracle_lse_merge.argtypes = [vp, vp, i, i, i, i, i, vp, vp]
+    lib.oracle_lse_merge.restype = i
+    lib.oracle_set_threads.argtypes = [i]
+    lib.oracle_max_threads.restype = i
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def _as_storage(x: np.ndarray, dtype: str) -> np.ndarray:
+    want = {"f32": np.float32, "bf16": np.uint16, "f64": np.float64}[dtype]
+    if x.dtype != want:
+        raise TypeError(f"oracle expects {want} storage for dtype {dtype}, got {x.dtype}")
+    return np.ascontiguousarray(x)
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def attention(q, k, v, *, dtype: str, causal: bool, kv_range=None, sel=None):
+    """Materialised softmax attention in fp64.
+
+    Follows "RingAttention and Context Parallelism: Mathematical Foundations",
+    section 1 (A = softmax(QK^T/sqrt(d_k) + M) V), section 5 (causal j <= i) and
+    section 7 (L = m + ln l, natural log).  GQA: q head h reads kv head
+    h // (Hq // Hkv).
+
+    q [B,S,Hq,D], k/v [B,S,Hkv,D] as numpy arrays in storage form (float32,
+    float64, or uint16 bit patterns for bf16).  ``kv_range=(lo, hi)`` restricts
+    the visible keys to positions [lo, hi) (the partial over one key shard).
+    ``sel``: optional int64 query ids (b*S + i)*Hq + h.
+    Returns (O, lse): [B,S,Hq,D] and [B,Hq,S] float64, or [n,D] and [n] with sel.
+    """
+    q, k, v = (_as_storage(t, dtype) for t in (q, k, v))
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    assert k.shape == (B, S, Hkv, D) and v.shape == k.shape
+    lo, hi = kv_range if kv_range is not None else (0, S)
+    if sel is not None:
+        sel = np.ascontiguousarray(sel, dtype=np.int64)
+        out = np.empty((sel.size, D), np.float64)
+        lse = np.empty((sel.size,), np.float64)
+    else:
+        out = np.empty((B, S, Hq, D), np.float64)
+        lse = np.empty((B, Hq, S), np.float64)
+    rc = _load().oracle_attention(_ptr(q), _ptr(k), _ptr(v), DTYPES[dtype], B, S, Hq, Hkv, D,
+                                  int(bool(causal)), int(lo), int(hi), _ptr(sel),
+                                  0 if sel is None else sel.size, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_attention rejected its arguments")
+    return out, lse
+
+
+def fanout(q_rows, offsets, k_prefix, v_prefix, k_suffix, v_suffix, *, dtype: str, sel=None):
+    """Shared-prefix fan-out attention in fp64.
+
+    Follows "AHBM Agentic Runtime Architecture" sections 1.1, 3.2 and 5.2: the
+    stacked rows of branch b (rows offsets[b]..offsets[b+1]) see the whole shared
+    prefix plus branch b's own private suffix, never another branch's suffix.
+
+    q_rows [R,Hq,D]; offsets int32 [nb+1]; k/v_prefix [Sp,Hkv,D];
+    k/v_suffix [nb,Ss,Hkv,D].  Returns (O [R,Hq,D], lse [Hq,R]) float64, or
+    ([n,D], [n]) when ``sel`` (ids r*Hq + h) is given.
+    """
+    q_rows, k_prefix, v_prefix, k_suffix, v_suffix = (
+        _as_storage(t, dtype) for t in (q_rows, k_prefix, v_prefix, k_suffix, v_suffix))
+    offsets = np.ascontiguousarray(offsets, dtype=np.int32)
+    R, Hq, D = q_rows.shape
+    Sp, Hkv, _ = k_prefix.shape
+    nb, Ss = k_suffix.shape[0], k_suffix.shape[1]
+    assert offsets.size == nb + 1
+    if sel is not None:
+        sel = np.ascontiguousarray(sel, dtype=np.int64)
+        out = np.empty((sel.size, D), np.float64)
+        lse = np.empty((sel.size,), np.float64)
+    else:
+        out = np.empty((R, Hq, D), np.float64)
+        lse = np.empty((Hq, R), np.float64)
+    rc = _load().oracle_fanout(_ptr(q_rows), _ptr(offsets), nb, R, _ptr(k_prefix), _ptr(v_prefix), Sp,
+                               _ptr(k_suffix), _ptr(v_suffix), Ss, Hq, Hkv, D, DTYPES[dtype],
+                               _ptr(sel), 0 if sel is None else sel.size, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_fanout rejected its arguments")
+    return out, lse
+
+
+def lse_merge(part_O, part_lse):
+    """Row-indexed log-sum-exp merge of partial states, fp64.
+
+    Follows "AHBM Agentic Runtime Architecture" sections 3.4-3.5 (merge the same
+    row index across sequence shards) with the combination implied by the
+    exactness identity of "RingAttention and Context Parallelism", section 2.
+
+    part_O [P,B,S,H,D] float64 (normalised partial outputs), part_lse [P,B,H,S].
+    Returns (O [B,S,H,D], lse [B,H,S]).
+    """
+    part_O = np.ascontiguousarray(part_O, dtype=np.float64)
+    part_lse = np.ascontiguousarray(part_lse, dtype=np.float64)
+    P, B, S, H, D = part_O.shape
+    assert part_lse.shape == (P, B, H, S)
+    out = np.empty((B, S, H, D), np.float64)
+    lse = np.empty((B, H, S), np.float64)
+    rc = _load().oracle_lse_merge(_ptr(part_O), _ptr(part_lse), P, B, S, H, D, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("oracle_lse_merge rejected its arguments")
+    return out, lse

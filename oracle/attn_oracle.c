@@ -1,0 +1,309 @@
+/*
+ * attn_oracle.c -- plain, slow, fp64 CPU oracle for blockwise ring attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file; only the tests, the package smoke check and the CPU-baseline leg
+ * of the benchmark do.  It shares no code with the CUDA kernels.
+ *
+ * What it computes is the plain definition of the result the blockwise method
+ * reaches exactly, written out with no blocking, no shards and no online
+ * recurrence:
+ *
+ *   - Scaled dot-product softmax attention, A = softmax(q K^T / sqrt(d_k) + M) V
+ *     with M the optional causal mask ("RingAttention and Context Parallelism:
+ *     Mathematical Foundations ...", section 1, the attention equation), and the
+ *     statement in section 2 that the blockwise recurrence equals softmax over
+ *     the concatenated sequence (the exactness identity after the online-softmax
+ *     equations).
+ *   - Causal masking on global positions: token i sees keys j <= i (same page,
+ *     section 5, first paragraph).
+ *   - The log-sum-exp statistic L = m + ln(l) kept for the backward pass (same
+ *     page, section 7, "RingAttention backward pass logic" figure), which is the
+ *     natural log of sum_j exp(s_j).
+ *   - Shared-prefix fan-out: a branch row sees the shared prefix keys plus its
+ *     own private suffix keys and never another branch's suffix ("AHBM Agentic
+ *     Runtime Architecture", sections 1.1, 3.2 and 5.2; "Supporting Agentic
+ *     Workloads", the context_i equation in the motivation subsection).
+ *   - The row-indexed merge of partial states over disjoint key sets ("AHBM
+ *     Agentic Runtime Architecture", sections 3.4-3.5), written as the
+ *     log-sum-exp combination that the exactness identity implies.
+ *
+ * Readings where the pages are silent:
+ *   - grouped-query heads: q head h reads kv head h / (Hq / Hkv);
+ *   - a query with no visible key has O = 0 and lse = -inf;
+ *   - layouts: q/k/v/out are [B, S, H, D] row-major, lse is [B, Hq, S].
+ *
+ * Every input element is widened to double exactly (fp32 or bf16 storage) and
+ * all arithmetic is double.  Parallelised over queries with OpenMP; each query
+ * materialises its full score row.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F64 = 2 };
+
+/* ORACLE_MUTANT plants one deliberate mistake, so that a test can check that
+ * the pins catch it.  The default build (no macro) is the oracle. */
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+/* Widen one stored element to double.  bf16 is the upper half of an IEEE
+ * binary32, so the widening is exact. */
+static double load_elem(const void* base, int dtype, int64_t idx) {
+    if (dtype == OR_F64) return ((const double*)base)[idx];
+    if (dtype == OR_F32) return (double)((const float*)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Softmax-weighted sum over an explicit list of key rows.
+ *   q_row      : D doubles
+ *   key_ptrs   : for each visible key, (tensor, element offset of its row)
+ * Writes D doubles to out and returns lse (or -inf with out = 0 when n == 0). */
+typedef struct {
+    const void* k;
+    const void* v;
+    int64_t off;
+} key_ref;
+
+static double softmax_row(const double* q_row, const key_ref* keys, int64_t n, int D,
+                          int dtype, double scale, double* s, double* out) {
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (n == 0) return -INFINITY;
+#if ORACLE_MUTANT == 6
+    if (n > 1) --n; /* mutant: drop the last visible key */
+#endif
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        double acc = 0.0;
+#if ORACLE_MUTANT == 5
+        for (int d = 0; d < D; ++d) acc += q_row[d] * load_elem(keys[j].v, dtype, keys[j].off + d);
+#else
+        for (int d = 0; d < D; ++d) acc += q_row[d] * load_elem(keys[j].k, dtype, keys[j].off + d);
+#endif
+        s[j] = acc * scale;
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        double p = exp(s[j] - m);
+        l += p;
+        for (int d = 0; d < D; ++d) out[d] += p * load_elem(keys[j].v, dtype, keys[j].off + d);
+    }
+    for (int d = 0; d < D; ++d) out[d] /= l;
+#if ORACLE_MUTANT == 3
+    return m + log2(l); /* mutant: wrong log base */
+#else
+    return m + log(l);
+#endif
+}
+
+/*
+ * Attention for the queries listed in `sel` (or every query when sel == NULL).
+ *   q [B,S,Hq,D], k/v [B,S,Hkv,D] in `dtype`.
+ *   Visible keys of query (b,i,h): j in [kv_begin, kv_end) and, if causal, j <= i.
+ *   sel ids encode (b,i,h) as (b*S + i)*Hq + h.
+ *   sel == NULL: out [B,S,Hq,D], lse [B,Hq,S].  Otherwise out [n_sel,D], lse [n_sel].
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_attention(const void* q, const void* k, const void* v, int dtype,
+                     int B, int S, int Hq, int Hkv, int D, int causal,
+                     int kv_begin, int kv_end, const int64_t* sel, int64_t n_sel,
+                     double* out, double* lse) {
+    if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv) return -1;
+    if (kv_begin < 0 || kv_end > S || kv_begin > kv_end) return -1;
+    const int64_t n_q = sel ? n_sel : (int64_t)B * S * Hq;
+    const int group = Hq / Hkv;
+#if ORACLE_MUTANT == 1
+    const double scale = 1.0 / (double)D; /* mutant: wrong softmax scale */
+#else
+    const double scale = 1.0 / sqrt((double)D);
+#endif
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* q_row = (double*)malloc(sizeof(double) * D);
+        double* s = (double*)malloc(sizeof(double) * (size_t)S);
+        key_ref* keys = (key_ref*)malloc(sizeof(key_ref) * (size_t)S);
+        double tmp_out[512];
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t t = 0; t < n_q; ++t) {
+            const int64_t id = sel ? sel[t] : t;
+            if (id < 0 || id >= (int64_t)B * S * Hq) { bad = 1; continue; }
+            const int h = (int)(id % Hq);
+            const int64_t bi = id / Hq;
+            const int i = (int)(bi % S);
+            const int b = (int)(bi / S);
+#if ORACLE_MUTANT == 4
+            const int hk = h % Hkv; /* mutant: interleaved instead of grouped GQA heads */
+#else
+            const int hk = h / group;
+#endif
+            for (int d = 0; d < D; ++d) q_row[d] = load_elem(q, dtype, id * D + d);
+            int64_t n = 0;
+            int hi = kv_end;
+#if ORACLE_MUTANT == 2
+            if (causal && i < hi) hi = i; /* mutant: causal mask drops the diagonal */
+            if (hi < kv_begin) hi = kv_begin;
+#else
+            if (causal && i + 1 < hi) hi = i + 1;
+#endif
+            for (int j = kv_begin; j < hi; ++j) {
+                keys[n].k = k;
+                keys[n].v = v;
+                keys[n].off = (((int64_t)b * S + j) * Hkv + hk) * D;
+                ++n;
+            }
+            double* o = D <= 512 ? tmp_out : NULL;
+            if (!o) { bad = 1; continue; }
+            const double L = softmax_row(q_row, keys, n, D, dtype, scale, s, o);
+            if (sel) {
+                memcpy(out + t * D, o, sizeof(double) * D);
+                lse[t] = L;
+            } else {
+                memcpy(out + id * D, o, sizeof(double) * D);
+                lse[((int64_t)b * Hq + h) * S + i] = L;
+            }
+        }
+        free(q_row);
+        free(s);
+        free(keys);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Shared-prefix fan-out attention.
+ *   q_rows [R,Hq,D]; branch b owns stacked rows [off[b], off[b+1]).
+ *   k/v_prefix [Sp,Hkv,D] shared by every branch; k/v_suffix [nb,Ss,Hkv,D].
+ *   Row r of branch b sees all Sp prefix keys and all Ss keys of suffix b.
+ *   sel ids encode (r,h) as r*Hq + h.  sel == NULL: out [R,Hq,D], lse [Hq,R];
+ *   otherwise out [n_sel,D], lse [n_sel].
+ */
+int oracle_fanout(const void* q_rows, const int32_t* off, int nb, int R,
+                  const void* k_prefix, const void* v_prefix, int Sp,
+                  const void* k_suffix, const void* v_suffix, int Ss,
+                  int Hq, int Hkv, int D, int dtype, const int64_t* sel, int64_t n_sel,
+                  double* out, double* lse) {
+    if (R < 0 || nb <= 0 || Sp < 0 || Ss < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || D > 512)
+        return -1;
+    if (off[0] != 0 || off[nb] != R) return -1;
+    for (int b = 0; b < nb; ++b)
+        if (off[b + 1] < off[b]) return -1;
+    const int64_t n_q = sel ? n_sel : (int64_t)R * Hq;
+    const int group = Hq / Hkv;
+    const double scale = 1.0 / sqrt((double)D);
+    const int64_t n_keys = (int64_t)Sp + Ss;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double q_row[512], o[512];
+        double* s = (double*)malloc(sizeof(double) * (size_t)(n_keys ? n_keys : 1));
+        key_ref* keys = (key_ref*)malloc(sizeof(key_ref) * (size_t)(n_keys ? n_keys : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < n_q; ++t) {
+            const int64_t id = sel ? sel[t] : t;
+            if (id < 0 || id >= (int64_t)R * Hq) { bad = 1; continue; }
+            const int h = (int)(id % Hq);
+            const int r = (int)(id / Hq);
+            int b = 0;
+            while (!(off[b] <= r && r < off[b + 1])) ++b;
+            const int hk = h / group;
+            for (int d = 0; d < D; ++d) q_row[d] = load_elem(q_rows, dtype, id * D + d);
+            int64_t n = 0;
+            for (int j = 0; j < Sp; ++j) {
+                keys[n].k = k_prefix;
+                keys[n].v = v_prefix;
+                keys[n].off = ((int64_t)j * Hkv + hk) * D;
+                ++n;
+            }
+            for (int j = 0; j < Ss; ++j) {
+                keys[n].k = k_suffix;
+                keys[n].v = v_suffix;
+                keys[n].off = (((int64_t)b * Ss + j) * Hkv + hk) * D;
+                ++n;
+            }
+            const double L = softmax_row(q_row, keys, n, D, dtype, scale, s, o);
+            if (sel) {
+                memcpy(out + t * D, o, sizeof(double) * D);
+                lse[t] = L;
+            } else {
+                memcpy(out + id * D, o, sizeof(double) * D);
+                lse[(int64_t)h * R + r] = L;
+            }
+        }
+        free(s);
+        free(keys);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Row-indexed merge of P partial states computed over disjoint key sets.
+ *   part_O [P,B,S,H,D] (normalised partial outputs), part_lse [P,B,H,S].
+ *   For each (b,s,h): M = max_p lse_p; w_p = exp(lse_p - M) (0 when lse_p = -inf);
+ *   O = sum_p w_p O_p / sum_p w_p; lse = M + ln(sum_p w_p).
+ *   All partials empty: O = 0, lse = -inf.
+ *   out [B,S,H,D], out_lse [B,H,S].
+ */
+int oracle_lse_merge(const double* part_O, const double* part_lse, int P, int B, int S, int H,
+                     int D, double* out, double* out_lse) {
+    if (P <= 0 || B <= 0 || S <= 0 || H <= 0 || D <= 0) return -1;
+    const int64_t rows = (int64_t)B * S * H;
+    const int64_t o_stride = rows * D;
+    const int64_t l_stride = rows;
+#pragma omp parallel for schedule(static)
+    for (int64_t id = 0; id < rows; ++id) {
+        const int h = (int)(id % H);
+        const int64_t bs = id / H;
+        const int s = (int)(bs % S);
+        const int b = (int)(bs / S);
+        const int64_t lidx = ((int64_t)b * H + h) * S + s;
+        double M = -INFINITY;
+        for (int p = 0; p < P; ++p)
+            if (part_lse[p * l_stride + lidx] > M) M = part_lse[p * l_stride + lidx];
+        double* o = out + id * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (M == -INFINITY) {
+            out_lse[lidx] = -INFINITY;
+            continue;
+        }
+        double wsum = 0.0;
+        for (int p = 0; p < P; ++p) {
+            const double L = part_lse[p * l_stride + lidx];
+            if (L == -INFINITY) continue;
+            const double w = exp(L - M);
+            wsum += w;
+            for (int d = 0; d < D; ++d) o[d] += w * part_O[p * o_stride + id * D + d];
+        }
+#if ORACLE_MUTANT != 7
+        for (int d = 0; d < D; ++d) o[d] /= wsum; /* mutant 7 forgets the normaliser */
+#endif
+        out_lse[lidx] = M + log(wsum);
+    }
+    return 0;
+}
