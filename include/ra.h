@@ -1,0 +1,171 @@
+/*
+ * ra.h -- C ABI of libra.so: blockwise exact attention walked in ring order,
+ * per-shard partials, the row-indexed log-sum-exp merge, and shared-prefix
+ * fan-out attention, on one NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers, owned and allocated by the
+ *    caller.  The library never allocates or frees memory and never
+ *    synchronises, except ra_device_status().  Inputs are read-only; outputs
+ *    are fully overwritten.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
+ *    the legacy default stream) of the current CUDA device.
+ *  - Layouts are dense row-major.  q/k/v/out are [B, S, H, D] (token-major,
+ *    head, then head dimension); lse is [B, Hq, S] fp32.
+ *  - Scores are q.k / sqrt(D) (the softmax scale of the attention definition
+ *    in "RingAttention and Context Parallelism: Mathematical Foundations",
+ *    section 1).  lse is the natural-log log-sum-exp of the scaled scores,
+ *    L = m + ln(l) (same page, section 7 figure).
+ *  - Grouped-query attention: q head h reads kv head h / (Hq / Hkv).
+ *  - Causal masking uses global positions: query i sees keys j <= i (same page,
+ *    section 5).
+ *  - Arguments are validated on the host before any launch.  A rejected call
+ *    returns a non-OK status and launches nothing; ra_last_error() then holds a
+ *    one-line message for the calling thread.  A failed launch returns
+ *    RA_ERR_CUDA.  Device-side waits are bounded: a wait that runs out records
+ *    RA_ERR_DEVICE_TIMEOUT in a device status word that ra_device_status()
+ *    reports (the kernel returns instead of hanging).
+ *  - Pointers must be 16-byte aligned (bulk tensor copies start on 16-byte
+ *    boundaries).
+ *  - dtype RA_BF16 runs the tensor-core path (tcgen05 MMA, TMEM accumulators,
+ *    TMA-staged tiles); RA_F32 runs an exact fp32 FMA path.  There is no CPU
+ *    fallback.
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RA_OK = 0,
+    RA_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment or divisibility */
+    RA_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+    RA_ERR_CUDA = 3,           /* a CUDA runtime/driver call or launch failed */
+    RA_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait ran out */
+    RA_ERR_WORKSPACE = 5       /* workspace missing or smaller than required */
+} ra_status;
+
+typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
+
+/*
+ * Blockwise exact attention with online softmax, KV walked in ring order.
+ *
+ * Defined by "RingAttention and Context Parallelism: Mathematical Foundations":
+ * section 2 (online softmax state (m, l, O), its five-step transition and the
+ * final A = O / l), section 3 (the sequence cut into n_shards contiguous shards
+ * of S/n_shards tokens; the query block of shard k visits KV shards
+ * k, k-1, ..., 0, N-1, ..., k+1, i.e. (k - t) mod N at step t) and section 5
+ * (causal: KV shards after the query's shard are skipped without loads).
+ *
+ *   q    [B, S, Hq, D]  dtype dt          k, v [B, S, Hkv, D] dtype dt
+ *   out  [B, S, Hq, D]  dtype dt          lse  [B, Hq, S] fp32 (may be NULL)
+ *   n_shards : shards of the ring; S % n_shards == 0.
+ *   block    : KV block walked within a shard; (S / n_shards) % block == 0.
+ *              The bf16 path consumes keys in 128-key tiles (a block of 64 is
+ *              walked as consecutive pairs, the same key order) and needs
+ *              (S / n_shards) % 128 == 0.
+ *   causal   : 0 or 1.
+ *   D        : 64 or 128.   Hq % Hkv == 0.
+ * Errors: RA_ERR_INVALID_ARG for any violated rule above, RA_ERR_UNSUPPORTED
+ * for a valid shape outside what the kernels implement, RA_ERR_CUDA if the
+ * launch fails.
+ */
+ra_status ra_blockwise_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                                int B, int S, int Hq, int Hkv, int D, int n_shards, int block,
+                                int causal, ra_dtype dt, void* stream);
+
+/*
+ * Per-shard partial states: the same ring walk, but the state is normalised and
+ * written out after every KV shard instead of being carried across shards --
+ * the per-shard partials that the "AHBM Agentic Runtime Architecture" page
+ * (section 3.3) has each sequence shard produce before the row-indexed merge.
+ *
+ *   partials_O   [n_shards, B, S, Hq, D] dtype dt : O_j / l_j for KV shard j
+ *   partials_lse [n_shards, B, Hq, S] fp32        : m_j + ln(l_j)
+ * A (query, KV shard) pair that the causal mask empties entirely is written as
+ * O = 0, lse = -inf without any compute.  Other arguments and errors as
+ * ra_blockwise_attn_fwd.  Merging the partials with ra_lse_merge gives
+ * ra_blockwise_attn_fwd's result up to rounding.
+ */
+ra_status ra_ring_partials_fwd(const void* q, const void* k, const void* v, void* partials_O,
+                               float* partials_lse, int B, int S, int Hq, int Hkv, int D,
+                               int n_shards, int block, int causal, ra_dtype dt, void* stream);
+
+/*
+ * Row-indexed log-sum-exp merge of P partial states computed over disjoint key
+ * sets ("AHBM Agentic Runtime Architecture", sections 3.4-3.5: the same row
+ * index is merged across sequence shards, never different rows).  Per
+ * (b, s, h):  M = max_p lse_p;  w_p = exp(lse_p - M);  O = sum_p w_p O_p / sum_p w_p;
+ * lse = M + ln(sum_p w_p).  A partial with lse_p = -inf has weight 0 and its
+ * O_p is not read; if every partial is empty the result is O = 0, lse = -inf.
+ *
+ *   partials_O   [P, B, S, H, D] dtype dt     partials_lse [P, B, H, S] fp32
+ *   out          [B, S, H, D]    dtype dt     out_lse      [B, H, S] fp32 (may be NULL)
+ *   D : 64 or 128.  P >= 1.
+ */
+ra_status ra_lse_merge(const void* partials_O, const float* partials_lse, void* out, float* out_lse,
+                       int P, int B, int S, int H, int D, ra_dtype dt, void* stream);
+
+/*
+ * Shared-prefix fan-out attention ("AHBM Agentic Runtime Architecture",
+ * sections 1.1-1.3, 3.2-3.4 and 5.2; "Supporting Agentic Workloads",
+ * stationary-KV policy).  The new query rows of n_branches branches are stacked
+ * into one tall Q; every row attends to the one shared prefix KV plus its own
+ * branch's private suffix KV (never another branch's).  The prefix is split into
+ * chunks processed in parallel; each prefix K/V tile is read from HBM once per
+ * KV head for all stacked rows; the prefix partials and the suffix partial are
+ * joined with the row-indexed log-sum-exp merge.  No causal mask.
+ *
+ *   q_rows         [R, Hq, D] dtype dt
+ *   branch_offsets int32 device array [n_branches + 1], CSR over the stacked
+ *                  rows: branch b owns rows [off[b], off[b+1]); off[0] = 0,
+ *                  off[n_branches] = R, non-decreasing (checked on device: a
+ *                  violation records RA_ERR_INVALID_ARG in the device status).
+ *   k_prefix, v_prefix [S_prefix, Hkv, D] dtype dt, shared by all branches.
+ *   k_suffix, v_suffix [n_branches, S_suffix, Hkv, D] dtype dt.
+ *   out            [R, Hq, D] dtype dt;   lse [Hq, R] fp32 (may be NULL).
+ *   workspace      device scratch of at least
+ *                  ra_prefix_fanout_workspace_size(...) bytes, 256-byte aligned,
+ *                  owned by the caller; contents on entry are ignored.
+ *   Only dt = RA_BF16 is implemented; D = 64 or 128; Hq % Hkv == 0 and
+ *   128 % (Hq / Hkv) == 0; S_prefix >= 0, S_suffix >= 0, R >= 0.
+ * Errors: RA_ERR_WORKSPACE if workspace is NULL or too small, otherwise as above.
+ */
+ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                                const void* k_prefix, const void* v_prefix, int S_prefix,
+                                const void* k_suffix, const void* v_suffix, int S_suffix, void* out,
+                                float* lse, int Hq, int Hkv, int D, ra_dtype dt, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace ra_prefix_fanout_attn needs for these sizes on the current
+ * device (0 if the sizes are invalid). */
+size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int S_suffix, int Hq,
+                                       int Hkv, int D, ra_dtype dt);
+
+/*
+ * Host-side view of the ring walk the kernels take (no GPU needed): for the
+ * 128-row query tile starting at q_row0, writes to shard_order[] the KV shards
+ * in the order they are visited ((k - t) mod n_shards, causal-empty shards
+ * skipped) and returns how many there are, or -1 on invalid arguments.
+ * shard_order must hold n_shards ints.
+ */
+int ra_ring_shard_order(int S, int n_shards, int causal, int q_row0, int* shard_order);
+
+/* Synchronises `stream`, then returns and clears the device status word:
+ * RA_OK, RA_ERR_DEVICE_TIMEOUT or RA_ERR_INVALID_ARG (device-side check), or
+ * RA_ERR_CUDA if the stream reports an error. */
+ra_status ra_device_status(void* stream);
+
+/* Thread-local one-line description of the last non-OK status ("" if none). */
+const char* ra_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H_ */

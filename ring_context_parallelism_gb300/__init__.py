@@ -1,0 +1,6 @@
+"""Blockwise exact attention walked in ring order, per-shard partials with a
+row-indexed log-sum-exp merge, and shared-prefix fan-out attention, for one
+NVIDIA GB300 (sm_103a).  The compute runs in libra.so (hand-written CUDA
+kernels behind a C ABI, include/ra.h); this package is a thin binding."""
+from .ra import (RAError, attn, device_status, fanout, fanout_workspace_size, load, lse_merge,  # noqa: F401
+                 ring_partials, ring_shard_order)

@@ -1,0 +1,185 @@
+// attn_simt.cu -- exact fp32 blockwise attention on the CUDA cores.
+//
+// The fp32 inputs are kept in fp32 end to end (no TF32 tensor-core rounding):
+// scores and P~V are FFMA, exponentials use expf.  Same walk and the same
+// online-softmax state transition as the tensor-core path ("RingAttention and
+// Context Parallelism: Mathematical Foundations", sections 2-3, 5): a CTA owns
+// 32 query rows of one head inside one shard and streams 32-key chunks of each
+// KV block in ring order, staging them in shared memory.  A query row is split
+// over D/32 threads (32 head dims each); a score is their partial dot products
+// combined with xor shuffles.  Thread `sub` of a row owns head dims
+// sub, sub + D/32, sub + 2*D/32, ... so that the threads of a row read
+// consecutive shared-memory words.
+#include <cmath>
+
+#include "ra_device.cuh"
+#include "ra_internal.h"
+#include "ra_walk.h"
+
+namespace ra {
+
+static __device__ unsigned g_simt_status[2];
+
+namespace {
+
+constexpr int kRows = 32;   // query rows per CTA
+constexpr int kChunk = 32;  // keys staged per step
+
+struct SimtParams {
+    const float *q, *k, *v;
+    int B, S, Hq, Hkv, n_shards, block, causal, partials, n_qtiles;
+    float scale;
+    OutDesc out;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kRows * (D / 32)) attn_simt_kernel(const SimtParams p) {
+    constexpr int TPR = D / 32;  // threads per row
+    __shared__ __align__(16) float ks[kChunk][D];
+    __shared__ __align__(16) float vs[kChunk][D];
+
+    const int tid = threadIdx.x;
+    const int r_local = tid / TPR;
+    const int sub = tid % TPR;  // which 32 dims
+    const int idx = blockIdx.x;
+    const int groups = p.B * p.Hq;
+    const int qt_rev = idx / groups;
+    const int rem = idx % groups;
+    const int b = rem / p.Hq;
+    const int h = rem % p.Hq;
+    const int qt = p.causal ? p.n_qtiles - 1 - qt_rev : qt_rev;
+    const int r0 = qt * kRows;
+    const int row = r0 + r_local;
+    const int hk = h / (p.Hq / p.Hkv);
+    const int L = p.S / p.n_shards;
+
+    float q[32], o[32];
+    const float* qp = p.q + ((static_cast<long long>(b) * p.S + row) * p.Hq + h) * D + sub;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        q[j] = qp[j * TPR];
+        o[j] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+
+    const OutDesc& out = p.out;
+    const long long o_base = static_cast<long long>(b) * out.o_b + static_cast<long long>(row) * out.o_row +
+                             static_cast<long long>(h) * out.o_h + sub;
+    const long long lse_base = static_cast<long long>(b) * out.lse_b + static_cast<long long>(h) * out.lse_h + row;
+
+    auto write = [&](int part) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float* dst = static_cast<float*>(out.o) + o_base + static_cast<long long>(part) * out.o_part;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dst[j * TPR] = o[j] * inv;
+        if (sub == 0 && out.lse)
+            out.lse[lse_base + static_cast<long long>(part) * out.lse_part] = l > 0.f ? m + logf(l) : -INFINITY;
+    };
+
+    const RingWalk w = make_ring_walk(p.S, p.n_shards, kRows, p.causal, r0, kRows);
+    for (int t = 0; t < w.n_visited; ++t) {
+        const int j = ring_shard_at(w, t);
+        const int key_lo = j * L;
+        int key_hi = key_lo + L;
+        if (p.causal && j == w.k) key_hi = min(key_hi, r0 + kRows);
+        for (int blk = key_lo; blk < key_hi; blk += p.block) {
+            const int blk_hi = min(blk + p.block, key_hi);
+            for (int c0 = blk; c0 < blk_hi; c0 += kChunk) {
+                const int n = min(kChunk, blk_hi - c0);
+                __syncthreads();
+                for (int e = tid; e < kChunk * (D / 4); e += blockDim.x) {
+                    const int kr = e / (D / 4);
+                    const int kc = (e % (D / 4)) * 4;
+                    float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
+                    if (kr < n) {
+                        const long long off = ((static_cast<long long>(b) * p.S + c0 + kr) * p.Hkv + hk) * D + kc;
+                        kv4 = *reinterpret_cast<const float4*>(p.k + off);
+                        vv4 = *reinterpret_cast<const float4*>(p.v + off);
+                    }
+                    *reinterpret_cast<float4*>(&ks[kr][kc]) = kv4;
+                    *reinterpret_cast<float4*>(&vs[kr][kc]) = vv4;
+                }
+                __syncthreads();
+                float s[kChunk];
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kChunk; ++c) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int d = 0; d < 32; ++d) acc = fmaf(q[d], ks[c][d * TPR + sub], acc);
+#pragma unroll
+                    for (int x = 1; x < TPR; x <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
+                    const bool vis = c < n && (!p.causal || c0 + c <= row);
+                    s[c] = vis ? acc * p.scale : -INFINITY;
+                    mx = fmaxf(mx, s[c]);
+                }
+                const float m_new = fmaxf(m, mx);
+                if (m_new == -INFINITY) continue;  // nothing visible yet for this row
+                const float alpha = (m == -INFINITY) ? 0.f : expf(m - m_new);
+                float rs = 0.f;
+#pragma unroll
+                for (int d = 0; d < 32; ++d) o[d] *= alpha;
+#pragma unroll
+                for (int c = 0; c < kChunk; ++c) {
+                    const float pc = expf(s[c] - m_new);
+                    rs += pc;
+#pragma unroll
+                    for (int d = 0; d < 32; ++d) o[d] = fmaf(pc, vs[c][d * TPR + sub], o[d]);
+                }
+                l = l * alpha + rs;
+                m = m_new;
+            }
+        }
+        if (p.partials) {
+            write(j);
+            m = -INFINITY;
+            l = 0.f;
+#pragma unroll
+            for (int d = 0; d < 32; ++d) o[d] = 0.f;
+        }
+    }
+    if (!p.partials) {
+        write(0);
+    } else {
+        for (int t = w.n_visited; t < p.n_shards; ++t) write(ring_shard_at(w, t));  // empty: O = 0, lse = -inf
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_ring_simt(const RingSimtArgs& a, cudaStream_t stream) {
+    SimtParams p;
+    p.q = a.q;
+    p.k = a.k;
+    p.v = a.v;
+    p.B = a.B;
+    p.S = a.S;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.n_shards = a.n_shards;
+    p.block = a.block;
+    p.causal = a.causal;
+    p.partials = a.partials;
+    p.n_qtiles = a.S / kRows;
+    p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(a.D)));
+    p.out = a.out;
+    const int grid = p.n_qtiles * a.B * a.Hq;
+    if (a.D == 128)
+        attn_simt_kernel<128><<<grid, kRows * 4, 0, stream>>>(p);
+    else
+        attn_simt_kernel<64><<<grid, kRows * 2, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+unsigned read_clear_status_simt(unsigned* where) {
+    unsigned h[2] = {0, 0};
+    cudaMemcpyFromSymbol(h, g_simt_status, sizeof h);
+    if (h[0]) {
+        const unsigned z[2] = {0, 0};
+        cudaMemcpyToSymbol(g_simt_status, z, sizeof z);
+    }
+    if (where) *where = h[1];
+    return h[0];
+}
+
+}  // namespace ra

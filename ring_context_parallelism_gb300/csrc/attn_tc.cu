@@ -1,0 +1,697 @@
+// attn_tc.cu -- blockwise exact attention on the sm_103a tensor cores.
+//
+// One CTA owns up to two 128-row query tiles that read the same K/V tiles (two
+// query heads of one GQA group in the ring prefill; two row tiles of the
+// stacked branch rows in the fan-out), and walks the KV tiles in ring order.
+// Per KV tile, the online-softmax state transition of "RingAttention and
+// Context Parallelism: Mathematical Foundations", section 2 figure, is run as:
+//
+//   S   = Q K^T                  tcgen05.mma (smem x smem -> TMEM, fp32)
+//   m'  = max(m, rowmax(S))      softmax warps, one thread per row (TMEM lane)
+//   P~  = exp(S - m')            ex2 with log2(e)/sqrt(d) folded in; bf16 into TMEM
+//   l   = e^{m-m'} l + rowsum(P~)
+//   O   = e^{m-m'} O + P~ V      tcgen05.mma (P~ from TMEM, V from smem)
+//   A   = O / l,  lse = m + ln l epilogue
+//
+// The running max is only moved when a tile's max exceeds it by more than
+// 2^8 (in log2 units); otherwise the stale max is kept, which changes no
+// result (O and l share it) and skips the O rescale.
+//
+// Roles (384 threads):  warp 0 lane 0  TMA producer (Q once, then K_i, V_i
+// into a 4-stage smem ring);  warp 1 lane 0  MMA issuer (also allocates TMEM);
+// warps 4-7  softmax + epilogue of tile 0;  warps 8-11  same for tile 1.
+// TMEM: tile t uses columns [256t, 256t+128) for S (P~ overwrites its first
+// half as packed bf16) and [256t+128, 256t+128+D) for O.
+//
+// Every wait is bounded (ra::mbar_wait); a wait that runs out records
+// RA_ERR_DEVICE_TIMEOUT in the status word and the CTA unwinds and returns.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "ra_device.cuh"
+#include "ra_internal.h"
+#include "ra_walk.h"
+
+namespace ra {
+
+static __device__ unsigned g_tc_status[2];
+
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kTileN = 128;
+constexpr int kThreads = 384;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr int kTmemCols = 512;
+
+struct TcParams {
+    int fanout;     // 0 ring prefill, 1 fan-out
+    int partials;   // ring: one partial per KV shard
+    int causal;
+    int T2;         // ring: two heads per CTA (GQA group size even)
+    // ring
+    int B, S, Hq, Hkv, n_shards, n_qtiles, n_head_groups;
+    // fan-out
+    int R, G, rows_per_tile, n_mpairs, S_prefix, chunk_tiles, n_chunks, S_suffix, n_branches,
+        suffix_mpairs, n_prefix_units;
+    const int* offsets;
+    float scale_log2;
+    OutDesc out;
+};
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 64;                   // 128-byte column groups per row
+    static constexpr int kTileBytes = kTileM * D * 2;        // one Q/K/V tile
+    static constexpr int kStages = D == 128 ? 4 : 6;
+    static constexpr int kQOff = 0;
+    static constexpr int kKVOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+    static constexpr int kNumBars = 1 + 2 * kStages + 7;
+    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
+};
+
+// Unit of work of one CTA, identical in every thread.
+struct Unit {
+    int valid;
+    int T;                 // tiles (1 or 2)
+    int qc1[2], qc2[2], qc3[2];  // Q tensor-map coordinates (dims 1..3) per tile
+    int kv_head, kv_z;     // K/V map coordinates (dims 1 and 3)
+    int suffix;            // fan-out: K/V from the suffix maps
+    // ring
+    int b, head[2], q_row0;
+    // fan-out
+    int row0[2], row_hi, kv_lo, kv_hi, part;
+};
+
+__device__ __forceinline__ Unit decode_unit(const TcParams& p) {
+    Unit u;
+    u.valid = 1;
+    u.suffix = 0;
+    const int idx = blockIdx.x;
+    if (!p.fanout) {
+        const int groups = p.B * p.n_head_groups;
+        const int qt_rev = idx / groups;
+        const int rem = idx % groups;
+        u.b = rem / p.n_head_groups;
+        const int hg = rem % p.n_head_groups;
+        const int qt = p.causal ? p.n_qtiles - 1 - qt_rev : qt_rev;  // heaviest tiles launch first
+        u.q_row0 = qt * kTileM;
+        u.T = p.T2 ? 2 : 1;
+        for (int t = 0; t < 2; ++t) {
+            u.head[t] = hg * u.T + (t < u.T ? t : 0);
+            u.qc1[t] = u.head[t];
+            u.qc2[t] = u.q_row0;
+            u.qc3[t] = u.b;
+        }
+        u.kv_head = u.head[0] / (p.Hq / p.Hkv);
+        u.kv_z = u.b;
+        return u;
+    }
+    u.b = 0;
+    int mp;
+    if (idx < p.n_prefix_units) {
+        mp = idx % p.n_mpairs;
+        const int rest = idx / p.n_mpairs;
+        const int chunk = rest % p.n_chunks;
+        u.kv_head = rest / p.n_chunks;
+        u.kv_z = 0;
+        u.kv_lo = chunk * p.chunk_tiles * kTileN;
+        u.kv_hi = min(p.S_prefix, u.kv_lo + p.chunk_tiles * kTileN);
+        u.part = chunk;
+        u.row0[0] = 2 * mp * p.rows_per_tile;
+        u.row_hi = p.R;
+    } else {
+        const int j = idx - p.n_prefix_units;
+        mp = j % p.suffix_mpairs;
+        const int rest = j / p.suffix_mpairs;
+        u.kv_head = rest % p.Hkv;
+        const int br = rest / p.Hkv;
+        const int lo = p.offsets[br];
+        const int hi = p.offsets[br + 1];
+        if (lo < 0 || hi < lo || hi > p.R || (br == 0 && lo != 0) || (br == p.n_branches - 1 && hi != p.R)) {
+            if (threadIdx.x == 0) {
+                atomicCAS(&g_tc_status[0], 0u, kDevInvalidArg);
+                atomicCAS(&g_tc_status[1], 0u, 0x0F000000u | static_cast<unsigned>(br));
+            }
+            u.valid = 0;
+            return u;
+        }
+        u.suffix = 1;
+        u.kv_z = br;
+        u.kv_lo = 0;
+        u.kv_hi = p.S_suffix;
+        u.part = p.n_chunks;
+        u.row0[0] = lo + 2 * mp * p.rows_per_tile;
+        u.row_hi = hi;
+    }
+    u.row0[1] = u.row0[0] + p.rows_per_tile;
+    if (u.row0[0] >= u.row_hi) u.valid = 0;
+    u.T = (u.row0[1] < u.row_hi) ? 2 : 1;
+    for (int t = 0; t < 2; ++t) {
+        u.qc1[t] = 0;
+        u.qc2[t] = u.kv_head;
+        u.qc3[t] = u.row0[t];
+    }
+    return u;
+}
+
+// KV tile i of the unit's walk: first key, and flags for shard boundaries.
+struct TileInfo {
+    int kb, shard_pos;
+    bool first, last;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const TcParams& p, const Unit& u, const RingWalk& w, int i) {
+    TileInfo ti;
+    if (!p.fanout) {
+        ti.kb = ring_tile(w, i, &ti.shard_pos, &ti.first, &ti.last);
+    } else {
+        ti.kb = u.kv_lo + i * kTileN;
+        ti.shard_pos = 0;
+        ti.first = (i == 0);
+        ti.last = false;
+    }
+    return ti;
+}
+
+template <int D>
+__device__ __forceinline__ void store_row(const OutDesc& out, long long o_base, int chunk, const float* vals,
+                                          float inv_l) {
+    if (out.o_f32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out.o) + o_base + chunk * 32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(vals[4 * j] * inv_l, vals[4 * j + 1] * inv_l, vals[4 * j + 2] * inv_l,
+                                 vals[4 * j + 3] * inv_l);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out.o) + o_base + chunk * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(pack_bf16x2(vals[8 * j] * inv_l, vals[8 * j + 1] * inv_l),
+                                pack_bf16x2(vals[8 * j + 2] * inv_l, vals[8 * j + 3] * inv_l),
+                                pack_bf16x2(vals[8 * j + 4] * inv_l, vals[8 * j + 5] * inv_l),
+                                pack_bf16x2(vals[8 * j + 6] * inv_l, vals[8 * j + 7] * inv_l));
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k2,
+                   const __grid_constant__ CUtensorMap tm_v2, const TcParams p) {
+    using C = Cfg<D>;
+    const Unit u = decode_unit(p);
+    if (!u.valid) return;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* q_smem = smem + C::kQOff;
+    uint8_t* kv_smem = smem + C::kKVOff;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint64_t* q_full = bars;
+    uint64_t* kv_full = bars + 1;
+    uint64_t* kv_empty = kv_full + C::kStages;
+    uint64_t* s_full = kv_empty + C::kStages;  // [2]
+    uint64_t* p_full = s_full + 2;             // [2]
+    uint64_t* o_done = p_full + 2;             // [2]
+    uint64_t* drain = o_done + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    RingWalk w{};
+    int total;
+    if (!p.fanout) {
+        w = make_ring_walk(p.S, p.n_shards, kTileN, p.causal, u.q_row0, kTileM);
+        total = w.total;
+    } else {
+        total = (u.kv_hi - u.kv_lo + kTileN - 1) / kTileN;
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 128);
+            mbar_init(&o_done[t], 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int T = u.T;
+    unsigned* status = g_tc_status;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const CUtensorMap* km = u.suffix ? &tm_k2 : &tm_k;
+            const CUtensorMap* vm = u.suffix ? &tm_v2 : &tm_v;
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(km);
+            tma_prefetch_desc(vm);
+            mbar_arrive_expect_tx(q_full, T * C::kTileBytes);
+            for (int t = 0; t < T; ++t)
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(&tm_q, q_full, q_smem + t * C::kTileBytes + c * 16384, c * 64, u.qc1[t], u.qc2[t],
+                                u.qc3[t]);
+            int issued = 0;
+            for (int i = 0; i < total; ++i) {
+                const TileInfo ti = tile_info(p, u, w, i);
+                bool ok = true;
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    const int it = 2 * i + kv;
+                    const int s = it % C::kStages;
+                    ok = mbar_wait(&kv_empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag, status,
+                                   0x01000000u | it);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&kv_full[s], C::kTileBytes);
+                    uint8_t* dst = kv_smem + s * C::kTileBytes;
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_4d(kv ? vm : km, &kv_full[s], dst + c * 16384, c * 64, u.kv_head, ti.kb, u.kv_z);
+                    ++issued;
+                }
+                if (!ok) break;
+            }
+            if (*abort_flag) {
+                // let copies already in flight land before the CTA exits
+                for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
+                    mbar_wait(&kv_full[it % C::kStages], (it / C::kStages) & 1, abort_flag, status, 0);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, false, true);
+            const uint32_t q_addr = smem_u32(q_smem);
+            const uint32_t kv_addr = smem_u32(kv_smem);
+            bool ok = mbar_wait(q_full, 0, abort_flag, status, 0x02000000u);
+            tc_fence_after();
+            for (int i = 0; ok && i <= total; ++i) {
+                bool fresh_prev = false;
+                if (i > 0) {
+                    const TileInfo tp = tile_info(p, u, w, i - 1);
+                    fresh_prev = (i - 1 == 0) || (p.partials && tp.first);
+                }
+                for (int t = 0; t < T && ok; ++t) {
+                    const uint32_t tS = tmem_base + t * 256;
+                    const uint32_t tO = tS + 128;
+                    if (i > 0) {
+                        const int itv = 2 * (i - 1) + 1;
+                        const int sv = itv % C::kStages;
+                        if (t == 0) {
+                            ok = mbar_wait(&kv_full[sv], (itv / C::kStages) & 1, abort_flag, status,
+                                           0x03000000u | itv);
+                            if (!ok) break;
+                        }
+                        ok = mbar_wait(&p_full[t], (i - 1) & 1, abort_flag, status, 0x04000000u | (i - 1));
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t v_base = kv_addr + sv * C::kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kTileN / 16; ++kk) {
+                            const uint64_t bdesc = smem_desc_sw128(v_base + kk * 2048, 16384, 1024);
+                            mma_ts(tO, tS + kk * 8, bdesc, idesc_pv, (fresh_prev && kk == 0) ? 0u : 1u);
+                        }
+                        mma_commit(&o_done[t]);
+                    }
+                    if (i < total) {
+                        const int itk = 2 * i;
+                        const int sk = itk % C::kStages;
+                        if (t == 0) {
+                            ok = mbar_wait(&kv_full[sk], (itk / C::kStages) & 1, abort_flag, status,
+                                           0x05000000u | itk);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        const uint32_t a_base = q_addr + t * C::kTileBytes;
+                        const uint32_t b_base = kv_addr + sk * C::kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            mma_ss(tS, smem_desc_sw128(a_base + off, 16, 1024), smem_desc_sw128(b_base + off, 16, 1024),
+                                   idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&s_full[t]);
+                    }
+                }
+                if (!ok) break;
+                if (i > 0) mma_commit(&kv_empty[(2 * (i - 1) + 1) % C::kStages]);
+                if (i < total) mma_commit(&kv_empty[(2 * i) % C::kStages]);
+            }
+            // all issued MMAs complete before TMEM is released
+            mma_commit(drain);
+            mbar_wait(drain, 0, abort_flag, status, 0);
+        }
+    } else if (warp >= 4 && (warp - 4) / 4 < T) {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int t = (warp - 4) >> 2;
+        const int quad = warp & 3;
+        const int lane_row = quad * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem_base + lane_off + t * 256;
+        const uint32_t tO = tS + 128;
+
+        // this thread's output row
+        int row, head;
+        bool row_ok;
+        if (!p.fanout) {
+            row = u.q_row0 + lane_row;
+            head = u.head[t];
+            row_ok = true;
+        } else {
+            row = u.row0[t] + lane_row / p.G;
+            head = u.kv_head * p.G + lane_row % p.G;
+            row_ok = row < u.row_hi;
+        }
+        const OutDesc& out = p.out;
+        const long long o_row_base = static_cast<long long>(u.b) * out.o_b + static_cast<long long>(row) * out.o_row +
+                                     static_cast<long long>(head) * out.o_h;
+        const long long lse_base = static_cast<long long>(u.b) * out.lse_b + static_cast<long long>(head) * out.lse_h + row;
+
+        float m_use = -INFINITY, l_sum = 0.f;
+        bool ok = true;
+
+        // Normalise the O accumulator (after PV of walk tile i_done) and write it as part `part`.
+        auto flush = [&](int i_done, int part) -> bool {
+            if (!mbar_wait(&o_done[t], i_done & 1, abort_flag, status, 0x06000000u | i_done)) return false;
+            tc_fence_after();
+            const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+            const long long ob = o_row_base + static_cast<long long>(part) * out.o_part;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tO + c * 32, r);
+                tmem_wait_ld();
+                if (row_ok) store_row<D>(out, ob, c, reinterpret_cast<const float*>(r), inv_l);
+            }
+            if (row_ok && out.lse) {
+                const float L = l_sum > 0.f ? (m_use + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+                out.lse[lse_base + static_cast<long long>(part) * out.lse_part] = L;
+            }
+            return true;
+        };
+
+        for (int i = 0; i < total; ++i) {
+            const TileInfo ti = tile_info(p, u, w, i);
+            if (p.partials && ti.first && i > 0) {
+                if (!(ok = flush(i - 1, ring_shard_at(w, ti.shard_pos - 1)))) break;
+                m_use = -INFINITY;
+                l_sum = 0.f;
+            }
+            if (!(ok = mbar_wait(&s_full[t], i & 1, abort_flag, status, 0x07000000u | i))) break;
+            tc_fence_after();
+            float x[kTileN];
+#pragma unroll
+            for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(tS + c * 32, reinterpret_cast<uint32_t*>(x) + c * 32);
+            tmem_wait_ld();
+            // visible columns of this tile: c <= lim
+            int lim = kTileN - 1;
+            if (!p.fanout) {
+                if (p.causal) lim = min(lim, row - ti.kb);
+            } else {
+                lim = min(lim, u.kv_hi - 1 - ti.kb);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTileN; ++c) {
+                x[c] = (c <= lim) ? x[c] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, x[c]);
+            }
+            const bool fresh = (i == 0) || (p.partials && ti.first);
+            float alpha = 1.f;
+            bool resc = false;
+            if (fresh) {
+                m_use = mx;
+                l_sum = 0.f;
+            } else if (mx > m_use + kRescaleLog2) {
+                alpha = (m_use == -INFINITY) ? 0.f : ex2_approx(m_use - mx);
+                m_use = mx;
+                resc = true;
+            }
+            const float ms = (m_use == -INFINITY) ? 0.f : m_use;
+            float rs = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < kTileN; c0 += 32) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float p0 = ex2_approx(x[c0 + 2 * j] - ms);
+                    const float p1 = ex2_approx(x[c0 + 2 * j + 1] - ms);
+                    rs += p0 + p1;
+                    pk[j] = pack_bf16x2(p0, p1);
+                }
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                    "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(tS + c0 / 2),
+                    "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7]),
+                    "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]), "r"(pk[14]),
+                    "r"(pk[15])
+                    : "memory");
+            }
+            l_sum = l_sum * alpha + rs;
+            if (__any_sync(0xffffffffu, resc)) {
+                // O of the previous tiles must be complete before it is rescaled
+                if (!(ok = mbar_wait(&o_done[t], (i - 1) & 1, abort_flag, status, 0x08000000u | i))) break;
+                tc_fence_after();
+                const float a = resc ? alpha : 1.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * a);
+                    tmem_st32(tO + c * 32, r);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&p_full[t]);
+        }
+        if (ok && total > 0) {
+            if (!p.fanout && p.partials) {
+                const TileInfo tl = tile_info(p, u, w, total - 1);
+                ok = flush(total - 1, ring_shard_at(w, tl.shard_pos));
+            } else {
+                ok = flush(total - 1, p.fanout ? u.part : 0);
+            }
+        }
+        if (ok && !p.fanout && p.partials) {
+            // KV shards the causal mask empties for this tile: O = 0, lse = -inf
+            for (int t2 = w.n_visited; t2 < p.n_shards; ++t2) {
+                const int j = ring_shard_at(w, t2);
+                const long long ob = o_row_base + static_cast<long long>(j) * out.o_part;
+                float zeros[32];
+#pragma unroll
+                for (int z = 0; z < 32; ++z) zeros[z] = 0.f;
+                for (int c = 0; c < D / 32; ++c) store_row<D>(out, ob, c, zeros, 0.f);
+                if (out.lse) out.lse[lse_base + static_cast<long long>(j) * out.lse_part] = -INFINITY;
+            }
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 4-D bf16 tensor map, dims innermost first, strides in bytes for dims 1..3,
+// box (64, b1, b2, b3), 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, const unsigned long long dims[4], const unsigned long long strides[3],
+              const unsigned box[4]) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
+    cuuint64_t gs[3] = {strides[0], strides[1], strides[2]};
+    cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gd, gs, bx, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch(const TcParams& p, int grid, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                   const CUtensorMap& k2, const CUtensorMap& v2, cudaStream_t stream) {
+    const int smem = Cfg<D>::kSmemBytes;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    if (grid <= 0) return cudaSuccess;
+    attn_tc_kernel<D><<<grid, kThreads, smem, stream>>>(q, k, v, k2, v2, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
+    TcParams p{};
+    p.fanout = 0;
+    p.partials = a.partials;
+    p.causal = a.causal;
+    p.B = a.B;
+    p.S = a.S;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.n_shards = a.n_shards;
+    p.n_qtiles = a.S / kTileM;
+    p.T2 = ((a.Hq / a.Hkv) % 2 == 0) ? 1 : 0;
+    p.n_head_groups = a.Hq / (p.T2 ? 2 : 1);
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
+    p.out = a.out;
+    const unsigned long long D = a.D, esz = 2;
+    CUtensorMap tq, tk, tv;
+    const unsigned long long qd[4] = {D, (unsigned long long)a.Hq, (unsigned long long)a.S, (unsigned long long)a.B};
+    const unsigned long long qs[3] = {D * esz, D * esz * a.Hq, D * esz * a.Hq * a.S};
+    const unsigned long long kd[4] = {D, (unsigned long long)a.Hkv, (unsigned long long)a.S, (unsigned long long)a.B};
+    const unsigned long long ks[3] = {D * esz, D * esz * a.Hkv, D * esz * a.Hkv * a.S};
+    const unsigned box[4] = {64, 1, 128, 1};
+    if (!make_map(&tq, a.q, qd, qs, box) || !make_map(&tk, a.k, kd, ks, box) || !make_map(&tv, a.v, kd, ks, box))
+        return cudaErrorInvalidValue;
+    const int grid = p.n_qtiles * a.B * p.n_head_groups;
+    return a.D == 128 ? launch<128>(p, grid, tq, tk, tv, tk, tv, stream)
+                      : launch<64>(p, grid, tq, tk, tv, tk, tv, stream);
+}
+
+void fanout_chunking(int R, int S_prefix, int Hq, int Hkv, int n_sm, int* n_chunks, int* chunk_tiles) {
+    const int G = Hq / Hkv;
+    const int rows_per_tile = kTileM / G;
+    const int n_mpairs = (R + 2 * rows_per_tile - 1) / (2 * rows_per_tile);
+    const int n_tiles = (S_prefix + kTileN - 1) / kTileN;
+    if (n_tiles == 0 || n_mpairs == 0) {
+        *n_chunks = 0;
+        *chunk_tiles = 1;
+        return;
+    }
+    // Choose the split that minimises (waves x tiles per chunk) on n_sm SMs,
+    // preferring fewer chunks (fewer partials) on ties.
+    long long best = -1;
+    int best_c = 1;
+    const int max_c = n_tiles < 64 ? n_tiles : 64;
+    for (int c = 1; c <= max_c; ++c) {
+        const int ct = (n_tiles + c - 1) / c;
+        const int cc = (n_tiles + ct - 1) / ct;
+        const long long units = static_cast<long long>(Hkv) * n_mpairs * cc;
+        const long long waves = (units + n_sm - 1) / n_sm;
+        const long long cost = waves * ct * 1000 + cc;  // tie-break: fewer chunks
+        if (best < 0 || cost < best) {
+            best = cost;
+            best_c = cc;
+        }
+    }
+    *chunk_tiles = (n_tiles + best_c - 1) / best_c;
+    *n_chunks = (n_tiles + *chunk_tiles - 1) / *chunk_tiles;
+}
+
+cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
+    TcParams p{};
+    p.fanout = 1;
+    p.partials = 0;
+    p.causal = 0;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.R = a.R;
+    p.G = a.Hq / a.Hkv;
+    p.rows_per_tile = kTileM / p.G;
+    p.n_mpairs = (a.R + 2 * p.rows_per_tile - 1) / (2 * p.rows_per_tile);
+    p.S_prefix = a.S_prefix;
+    p.chunk_tiles = a.chunk_tiles;
+    p.n_chunks = a.n_chunks;
+    p.S_suffix = a.S_suffix;
+    p.n_branches = a.n_branches;
+    p.suffix_mpairs = p.n_mpairs;  // upper bound: a branch holds at most R rows
+    p.offsets = a.offsets;
+    p.n_prefix_units = (a.S_prefix > 0) ? a.Hkv * p.n_mpairs * a.n_chunks : 0;
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
+    p.out = a.part;
+    const unsigned long long D = a.D, esz = 2;
+    CUtensorMap tq, tk, tv, tk2, tv2;
+    const unsigned long long qd[4] = {D, (unsigned long long)p.G, (unsigned long long)a.Hkv, (unsigned long long)a.R};
+    const unsigned long long qs[3] = {D * esz, D * esz * p.G, D * esz * a.Hq};
+    const unsigned qbox[4] = {64, (unsigned)p.G, 1, (unsigned)p.rows_per_tile};
+    const unsigned box[4] = {64, 1, 128, 1};
+    if (!make_map(&tq, a.q_rows, qd, qs, qbox)) return cudaErrorInvalidValue;
+    const unsigned long long kd[4] = {D, (unsigned long long)a.Hkv,
+                                      (unsigned long long)(a.S_prefix > 0 ? a.S_prefix : 1), 1};
+    const unsigned long long ks[3] = {D * esz, D * esz * a.Hkv, D * esz * a.Hkv * (a.S_prefix > 0 ? a.S_prefix : 1)};
+    const unsigned long long sd[4] = {D, (unsigned long long)a.Hkv, (unsigned long long)(a.S_suffix > 0 ? a.S_suffix : 1),
+                                      (unsigned long long)a.n_branches};
+    const unsigned long long ss[3] = {D * esz, D * esz * a.Hkv, D * esz * a.Hkv * (a.S_suffix > 0 ? a.S_suffix : 1)};
+    const void* kp = a.S_prefix > 0 ? a.k_prefix : a.k_suffix;
+    const void* vp = a.S_prefix > 0 ? a.v_prefix : a.v_suffix;
+    const void* ksf = a.S_suffix > 0 ? a.k_suffix : a.k_prefix;
+    const void* vsf = a.S_suffix > 0 ? a.v_suffix : a.v_prefix;
+    if (a.S_prefix > 0) {
+        if (!make_map(&tk, kp, kd, ks, box) || !make_map(&tv, vp, kd, ks, box)) return cudaErrorInvalidValue;
+    }
+    if (a.S_suffix > 0) {
+        if (!make_map(&tk2, ksf, sd, ss, box) || !make_map(&tv2, vsf, sd, ss, box)) return cudaErrorInvalidValue;
+    }
+    if (a.S_prefix == 0) {
+        tk = tk2;
+        tv = tv2;
+    }
+    if (a.S_suffix == 0) {
+        tk2 = tk;
+        tv2 = tv;
+    }
+    const int n_suffix_units = (a.S_suffix > 0) ? a.n_branches * a.Hkv * p.suffix_mpairs : 0;
+    const int grid = p.n_prefix_units + n_suffix_units;
+    return a.D == 128 ? launch<128>(p, grid, tq, tk, tv, tk2, tv2, stream)
+                      : launch<64>(p, grid, tq, tk, tv, tk2, tv2, stream);
+}
+
+unsigned read_clear_status_tc(unsigned* where) {
+    unsigned h[2] = {0, 0};
+    cudaMemcpyFromSymbol(h, g_tc_status, sizeof h);
+    if (h[0]) {
+        const unsigned z[2] = {0, 0};
+        cudaMemcpyToSymbol(g_tc_status, z, sizeof z);
+    }
+    if (where) *where = h[1];
+    return h[0];
+}
+
+}  // namespace ra

@@ -1,0 +1,161 @@
+// lse_merge.cu -- row-indexed log-sum-exp merge of partial attention states.
+//
+// "AHBM Agentic Runtime Architecture", sections 3.4-3.5: partial states of the
+// same query row computed over different sequence shards are merged row by
+// row (never across rows), by the same primitive at every level of the
+// reduction.  With normalised partials (O_p, lse_p) the merge is
+//   M = max_p lse_p,  w_p = exp(lse_p - M),
+//   O = sum_p w_p O_p / sum_p w_p,  lse = M + ln(sum_p w_p),
+// which is the exactness identity of "RingAttention and Context Parallelism",
+// section 2, applied to whole shards.  An empty partial (lse = -inf) gets
+// weight 0 and its O is not read.
+//
+// One warp per (b, s, h) row; lane l owns D/32 consecutive head dims, so a
+// warp reads each partial row as one contiguous 128- or 256/512-byte segment.
+// fp32 arithmetic.  Bandwidth-bound: each partial row is read once.
+#include <cmath>
+
+#include "ra_device.cuh"
+#include "ra_internal.h"
+
+namespace ra {
+
+static __device__ unsigned g_merge_status[2];
+
+namespace {
+
+constexpr int kWarps = 8;
+
+template <int E, bool F32>
+struct Vec;  // E consecutive elements of one lane
+template <>
+struct Vec<4, true> {
+    static __device__ __forceinline__ void load(const void* p, float* x) {
+        const float4 v = *reinterpret_cast<const float4*>(p);
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    }
+    static __device__ __forceinline__ void store(void* p, const float* x) {
+        *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+};
+template <>
+struct Vec<2, true> {
+    static __device__ __forceinline__ void load(const void* p, float* x) {
+        const float2 v = *reinterpret_cast<const float2*>(p);
+        x[0] = v.x; x[1] = v.y;
+    }
+    static __device__ __forceinline__ void store(void* p, const float* x) {
+        *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+    }
+};
+template <>
+struct Vec<4, false> {
+    static __device__ __forceinline__ void load(const void* p, float* x) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
+        x[0] = __low2float(a); x[1] = __high2float(a); x[2] = __low2float(b); x[3] = __high2float(b);
+    }
+    static __device__ __forceinline__ void store(void* p, const float* x) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+    }
+};
+template <>
+struct Vec<2, false> {
+    static __device__ __forceinline__ void load(const void* p, float* x) {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(p);
+        x[0] = __low2float(a); x[1] = __high2float(a);
+    }
+    static __device__ __forceinline__ void store(void* p, const float* x) {
+        *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(x[0], x[1]);
+    }
+};
+
+template <int D, bool PART_F32, bool OUT_F32>
+__global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const void* __restrict__ part_O,
+                                                                const float* __restrict__ part_lse,
+                                                                void* __restrict__ out, float* __restrict__ out_lse,
+                                                                int P, int S, int H, long long rows) {
+    constexpr int E = D / 32;
+    const long long rid = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    if (rid >= rows) return;
+    const int lane = threadIdx.x & 31;
+    // rid = (b*S + s)*H + h
+    const int h = static_cast<int>(rid % H);
+    const long long bs = rid / H;
+    const int s = static_cast<int>(bs % S);
+    const long long b = bs / S;
+    const long long lse_idx = (b * H + h) * S + s;
+    const long long o_stride = rows * D;  // elements between partials
+    const long long l_stride = rows;
+
+    // max over partials (lanes stride over p)
+    float M = -INFINITY;
+    for (int pp = lane; pp < P; pp += 32) M = fmaxf(M, part_lse[pp * l_stride + lse_idx]);
+#pragma unroll
+    for (int x = 16; x; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    if (M != -INFINITY) {
+        const size_t esz = PART_F32 ? 4 : 2;
+        const char* base = static_cast<const char*>(part_O) + (rid * D + lane * E) * esz;
+        for (int pp = 0; pp < P; ++pp) {
+            const float L = part_lse[pp * l_stride + lse_idx];
+            if (L == -INFINITY) continue;  // empty partial: weight 0, O not read
+            const float w = expf(L - M);
+            wsum += w;
+            float x[E];
+            Vec<E, PART_F32>::load(base + pp * o_stride * esz, x);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] *= inv;
+    char* dst = static_cast<char*>(out) + (rid * D + lane * E) * (OUT_F32 ? 4 : 2);
+    Vec<E, OUT_F32>::store(dst, acc);
+    if (out_lse && lane == 0) out_lse[lse_idx] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+}
+
+template <int D, bool PF, bool OF>
+cudaError_t run(const MergeArgs& a, long long rows, cudaStream_t stream) {
+    const long long blocks = (rows + kWarps - 1) / kWarps;
+    lse_merge_kernel<D, PF, OF><<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(
+        a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(a.B) * a.S * a.H;
+    if (rows == 0) return cudaSuccess;
+    const int key = (a.D == 128 ? 4 : 0) | (a.part_f32 ? 2 : 0) | (a.out_f32 ? 1 : 0);
+    switch (key) {
+        case 0: return run<64, false, false>(a, rows, stream);
+        case 1: return run<64, false, true>(a, rows, stream);
+        case 2: return run<64, true, false>(a, rows, stream);
+        case 3: return run<64, true, true>(a, rows, stream);
+        case 4: return run<128, false, false>(a, rows, stream);
+        case 5: return run<128, false, true>(a, rows, stream);
+        case 6: return run<128, true, false>(a, rows, stream);
+        default: return run<128, true, true>(a, rows, stream);
+    }
+}
+
+unsigned read_clear_status_merge(unsigned* where) {
+    unsigned h[2] = {0, 0};
+    cudaMemcpyFromSymbol(h, g_merge_status, sizeof h);
+    if (h[0]) {
+        const unsigned z[2] = {0, 0};
+        cudaMemcpyToSymbol(g_merge_status, z, sizeof z);
+    }
+    if (where) *where = h[1];
+    return h[0];
+}
+
+}  // namespace ra

@@ -1,0 +1,260 @@
+// ra_api.cu -- the C ABI declared in include/ra.h: host-side validation,
+// output layout descriptors, dispatch to the kernels, device status.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+
+#include "../../include/ra.h"
+#include "ra_internal.h"
+#include "ra_walk.h"
+
+namespace {
+
+thread_local char g_err[256] = "";
+
+ra_status fail(ra_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+ra_status ok() {
+    g_err[0] = '\0';
+    return RA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ra_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(RA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+// Checks shared by the fused and partial ring entry points.
+ra_status check_ring(const void* q, const void* k, const void* v, const void* out, int B, int S, int Hq, int Hkv,
+                     int D, int n_shards, int block, int causal, ra_dtype dt) {
+    if (!q || !k || !v || !out) return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    if (B < 1 || S < 1 || Hq < 1 || Hkv < 1) return fail(RA_ERR_INVALID_ARG, "B, S, Hq, Hkv must be >= 1");
+    if (Hq % Hkv) return fail(RA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+    if (D != 64 && D != 128) return fail(RA_ERR_INVALID_ARG, "D must be 64 or 128 (got %d)", D);
+    if (n_shards < 1 || S % n_shards) return fail(RA_ERR_INVALID_ARG, "S (%d) %% n_shards (%d) != 0", S, n_shards);
+    const int L = S / n_shards;
+    if (block < 1 || L % block) return fail(RA_ERR_INVALID_ARG, "shard length %d %% block %d != 0", L, block);
+    if (causal != 0 && causal != 1) return fail(RA_ERR_INVALID_ARG, "causal must be 0 or 1");
+    if (dt == RA_BF16) {
+        if (L % 128) return fail(RA_ERR_UNSUPPORTED, "bf16 path needs shard length %% 128 == 0 (got %d)", L);
+        if (block != 64 && block % 128)
+            return fail(RA_ERR_UNSUPPORTED, "bf16 path walks 128-key tiles: block must be 64 or a multiple of 128");
+    } else if (dt == RA_F32) {
+        if (L % 32) return fail(RA_ERR_UNSUPPORTED, "fp32 path needs shard length %% 32 == 0 (got %d)", L);
+    } else {
+        return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dt));
+    }
+    const long long elems = static_cast<long long>(B) * S * Hq * D;
+    if (elems > (1ll << 40)) return fail(RA_ERR_INVALID_ARG, "tensor too large");
+    return RA_OK;
+}
+
+ra_status ring_common(const void* q, const void* k, const void* v, void* out, float* lse, int B, int S, int Hq,
+                      int Hkv, int D, int n_shards, int block, int causal, ra_dtype dt, void* stream, int partials) {
+    ra_status st = check_ring(q, k, v, out, B, S, Hq, Hkv, D, n_shards, block, causal, dt);
+    if (st != RA_OK) return st;
+    if (lse && !aligned16(lse)) return fail(RA_ERR_INVALID_ARG, "lse must be 16-byte aligned");
+    ra::OutDesc od;
+    od.o = out;
+    od.lse = lse;
+    od.o_row = static_cast<long long>(Hq) * D;
+    od.o_h = D;
+    od.o_b = static_cast<long long>(S) * Hq * D;
+    od.o_part = static_cast<long long>(B) * S * Hq * D;
+    od.lse_h = S;
+    od.lse_b = static_cast<long long>(Hq) * S;
+    od.lse_part = static_cast<long long>(B) * Hq * S;
+    od.o_f32 = (dt == RA_F32);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (dt == RA_BF16) {
+        ra::RingTcArgs a{q, k, v, B, S, Hq, Hkv, D, n_shards, causal, partials, od};
+        e = ra::launch_ring_tc(a, s);
+    } else {
+        ra::RingSimtArgs a{static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+                           B, S, Hq, Hkv, D, n_shards, block, causal, partials, od};
+        e = ra::launch_ring_simt(a, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, partials ? "ring partials launch" : "ring attention launch");
+    return ok();
+}
+
+struct FanoutPlan {
+    int n_chunks, chunk_tiles, P;
+    size_t part_o_bytes, part_lse_bytes, total;
+};
+
+FanoutPlan plan_fanout(int R, int S_prefix, int S_suffix, int Hq, int Hkv, int D) {
+    FanoutPlan f{};
+    ra::fanout_chunking(R, S_prefix, Hq, Hkv, sm_count(), &f.n_chunks, &f.chunk_tiles);
+    if (S_prefix == 0) f.n_chunks = 0;
+    f.P = f.n_chunks + (S_suffix > 0 ? 1 : 0);
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    f.part_o_bytes = up(static_cast<size_t>(f.P) * R * Hq * D * sizeof(float));
+    f.part_lse_bytes = up(static_cast<size_t>(f.P) * Hq * R * sizeof(float));
+    f.total = f.part_o_bytes + f.part_lse_bytes;
+    return f;
+}
+
+ra_status check_fanout(const void* q_rows, const int* offsets, int n_branches, int R, const void* k_prefix,
+                       const void* v_prefix, int S_prefix, const void* k_suffix, const void* v_suffix, int S_suffix,
+                       const void* out, int Hq, int Hkv, int D, ra_dtype dt) {
+    if (dt != RA_BF16 && dt != RA_F32) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dt));
+    if (dt != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "fan-out is implemented for bf16 only");
+    if (R < 0 || n_branches < 1 || S_prefix < 0 || S_suffix < 0)
+        return fail(RA_ERR_INVALID_ARG, "R >= 0, n_branches >= 1, S_prefix >= 0, S_suffix >= 0 required");
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv) return fail(RA_ERR_INVALID_ARG, "Hq must be a positive multiple of Hkv");
+    if (128 % (Hq / Hkv)) return fail(RA_ERR_UNSUPPORTED, "128 %% (Hq / Hkv) != 0");
+    if (D != 64 && D != 128) return fail(RA_ERR_INVALID_ARG, "D must be 64 or 128 (got %d)", D);
+    if (S_prefix + S_suffix < 1) return fail(RA_ERR_INVALID_ARG, "no keys: S_prefix + S_suffix must be >= 1");
+    if (R > 0 && (!q_rows || !out || !offsets)) return fail(RA_ERR_INVALID_ARG, "null pointer");
+    if (S_prefix > 0 && (!k_prefix || !v_prefix)) return fail(RA_ERR_INVALID_ARG, "null prefix pointer");
+    if (S_suffix > 0 && (!k_suffix || !v_suffix)) return fail(RA_ERR_INVALID_ARG, "null suffix pointer");
+    const void* ptrs[6] = {q_rows, k_prefix, v_prefix, k_suffix, v_suffix, out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    if (offsets && (reinterpret_cast<uintptr_t>(offsets) & 3u)) return fail(RA_ERR_INVALID_ARG, "offsets misaligned");
+    return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ra_blockwise_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int S,
+                                int Hq, int Hkv, int D, int n_shards, int block, int causal, ra_dtype dt,
+                                void* stream) {
+    return ring_common(q, k, v, out, lse, B, S, Hq, Hkv, D, n_shards, block, causal, dt, stream, 0);
+}
+
+ra_status ra_ring_partials_fwd(const void* q, const void* k, const void* v, void* partials_O, float* partials_lse,
+                               int B, int S, int Hq, int Hkv, int D, int n_shards, int block, int causal,
+                               ra_dtype dt, void* stream) {
+    if (!partials_lse) return fail(RA_ERR_INVALID_ARG, "partials_lse must not be NULL");
+    return ring_common(q, k, v, partials_O, partials_lse, B, S, Hq, Hkv, D, n_shards, block, causal, dt, stream, 1);
+}
+
+ra_status ra_lse_merge(const void* partials_O, const float* partials_lse, void* out, float* out_lse, int P, int B,
+                       int S, int H, int D, ra_dtype dt, void* stream) {
+    if (!partials_O || !partials_lse || !out) return fail(RA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(partials_O) || !aligned16(out) || !aligned16(partials_lse) || (out_lse && !aligned16(out_lse)))
+        return fail(RA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (P < 1 || B < 1 || S < 1 || H < 1) return fail(RA_ERR_INVALID_ARG, "P, B, S, H must be >= 1");
+    if (D != 64 && D != 128) return fail(RA_ERR_INVALID_ARG, "D must be 64 or 128 (got %d)", D);
+    if (dt != RA_BF16 && dt != RA_F32) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dt));
+    if (static_cast<long long>(P) * B * S * H * D > (1ll << 42)) return fail(RA_ERR_INVALID_ARG, "too large");
+    ra::MergeArgs a{partials_O, partials_lse, out, out_lse, P, B, S, H, D, dt == RA_F32, dt == RA_F32};
+    cudaError_t e = ra::launch_lse_merge(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "lse merge launch");
+    return ok();
+}
+
+size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv, int D,
+                                       ra_dtype dt) {
+    if (R < 0 || n_branches < 1 || S_prefix < 0 || S_suffix < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
+        (D != 64 && D != 128) || dt != RA_BF16 || 128 % (Hq / Hkv) || S_prefix + S_suffix < 1)
+        return 0;
+    return plan_fanout(R, S_prefix, S_suffix, Hq, Hkv, D).total;
+}
+
+ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                                const void* k_prefix, const void* v_prefix, int S_prefix, const void* k_suffix,
+                                const void* v_suffix, int S_suffix, void* out, float* lse, int Hq, int Hkv, int D,
+                                ra_dtype dt, void* workspace, size_t workspace_bytes, void* stream) {
+    ra_status st = check_fanout(q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix, k_suffix,
+                                v_suffix, S_suffix, out, Hq, Hkv, D, dt);
+    if (st != RA_OK) return st;
+    if (lse && !aligned16(lse)) return fail(RA_ERR_INVALID_ARG, "lse must be 16-byte aligned");
+    if (R == 0) return ok();
+    const FanoutPlan f = plan_fanout(R, S_prefix, S_suffix, Hq, Hkv, D);
+    if (!workspace || workspace_bytes < f.total)
+        return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", f.total, workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    float* part_o = static_cast<float*>(workspace);
+    float* part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + f.part_o_bytes);
+
+    ra::FanoutTcArgs a{};
+    a.q_rows = q_rows;
+    a.offsets = branch_offsets;
+    a.n_branches = n_branches;
+    a.R = R;
+    a.k_prefix = k_prefix;
+    a.v_prefix = v_prefix;
+    a.S_prefix = S_prefix;
+    a.k_suffix = k_suffix;
+    a.v_suffix = v_suffix;
+    a.S_suffix = S_suffix;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.n_chunks = f.n_chunks;
+    a.chunk_tiles = f.chunk_tiles;
+    a.part.o = part_o;
+    a.part.lse = part_lse;
+    a.part.o_row = static_cast<long long>(Hq) * D;
+    a.part.o_h = D;
+    a.part.o_part = static_cast<long long>(R) * Hq * D;
+    a.part.lse_h = R;
+    a.part.lse_part = static_cast<long long>(Hq) * R;
+    a.part.o_f32 = 1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = ra::launch_fanout_tc(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fan-out attention launch");
+    ra::MergeArgs m{part_o, part_lse, out, lse, f.P, 1, R, Hq, D, 1, 0};
+    e = ra::launch_lse_merge(m, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fan-out merge launch");
+    return ok();
+}
+
+int ra_ring_shard_order(int S, int n_shards, int causal, int q_row0, int* shard_order) {
+    if (S < 1 || n_shards < 1 || S % n_shards || q_row0 < 0 || q_row0 >= S || !shard_order) return -1;
+    const ra::RingWalk w = ra::make_ring_walk(S, n_shards, 1, causal ? 1 : 0, q_row0, 1);
+    for (int t = 0; t < w.n_visited; ++t) shard_order[t] = ra::ring_shard_at(w, t);
+    return w.n_visited;
+}
+
+ra_status ra_device_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    unsigned where = 0, code = ra::read_clear_status_tc(&where);
+    const char* who = "tensor-core attention";
+    if (!code) {
+        code = ra::read_clear_status_simt(&where);
+        who = "fp32 attention";
+    }
+    if (!code) {
+        code = ra::read_clear_status_merge(&where);
+        who = "lse merge";
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "device status");
+    if (code == RA_ERR_DEVICE_TIMEOUT)
+        return fail(RA_ERR_DEVICE_TIMEOUT, "%s: bounded device wait ran out (site 0x%08x)", who, where);
+    if (code == RA_ERR_INVALID_ARG)
+        return fail(RA_ERR_INVALID_ARG, "%s: device-side argument check failed (0x%08x)", who, where);
+    if (code) return fail(static_cast<ra_status>(code), "%s: device status %u", who, code);
+    return ok();
+}
+
+const char* ra_last_error(void) { return g_err; }
+
+}  // extern "C"

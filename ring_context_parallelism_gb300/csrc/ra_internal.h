@@ -1,0 +1,74 @@
+// ra_internal.h -- launch interfaces between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace ra {
+
+// Where a kernel writes its per-row results.  Element offsets:
+//   O   : part*o_part + b*o_b + row*o_row + head*o_h + d
+//   lse : part*lse_part + b*lse_b + head*lse_h + row
+struct OutDesc {
+    void* o = nullptr;
+    float* lse = nullptr;
+    long long o_b = 0, o_row = 0, o_h = 0, o_part = 0;
+    long long lse_b = 0, lse_h = 0, lse_part = 0;
+    int o_f32 = 0;  // 1: fp32 O, 0: bf16 O
+};
+
+// Ring-order prefill on the tensor cores (bf16).  partials=1 flushes one
+// normalised partial per KV shard.
+struct RingTcArgs {
+    const void *q, *k, *v;
+    int B, S, Hq, Hkv, D, n_shards, causal, partials;
+    OutDesc out;
+};
+cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream);
+
+// Shared-prefix fan-out on the tensor cores (bf16): prefix chunks + per-branch
+// suffix, each writing an fp32 partial into the workspace.
+struct FanoutTcArgs {
+    const void* q_rows;
+    const int* offsets;
+    int n_branches, R;
+    const void *k_prefix, *v_prefix;
+    int S_prefix;
+    const void *k_suffix, *v_suffix;
+    int S_suffix;
+    int Hq, Hkv, D;
+    int n_chunks, chunk_tiles;  // prefix split
+    OutDesc part;               // fp32 partials [P][R][Hq][D], lse [P][Hq][R]
+};
+cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream);
+
+// Prefix chunking chosen for a fan-out call (shared by the workspace query).
+void fanout_chunking(int R, int S_prefix, int Hq, int Hkv, int n_sm, int* n_chunks, int* chunk_tiles);
+
+// Exact fp32 path (CUDA-core FMA).
+struct RingSimtArgs {
+    const float *q, *k, *v;
+    int B, S, Hq, Hkv, D, n_shards, block, causal, partials;
+    OutDesc out;
+};
+cudaError_t launch_ring_simt(const RingSimtArgs& a, cudaStream_t stream);
+
+// Row-indexed LSE merge.  part_f32 / out_f32 select fp32 or bf16 storage.
+struct MergeArgs {
+    const void* part_O;
+    const float* part_lse;
+    void* out;
+    float* out_lse;
+    int P, B, S, H, D;
+    int part_f32, out_f32;
+};
+cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t stream);
+
+// Status words of each translation unit: read (after the caller synchronised)
+// and clear.  Returns the first non-zero code, 0 if none.
+unsigned read_clear_status_tc(unsigned* where);
+unsigned read_clear_status_simt(unsigned* where);
+unsigned read_clear_status_merge(unsigned* where);
+
+}  // namespace ra

@@ -1,0 +1,186 @@
+"""Thin Python binding over libra.so (the C ABI of include/ra.h).
+
+Argument marshalling only: dtype / contiguity / device checks, output
+allocation through PyTorch, and the raw pointers plus the current CUDA stream
+passed to the library.  Every step of the attention runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback -- if libra.so is missing or no
+GPU is present the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libra.so")
+
+RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_DEVICE_TIMEOUT, RA_ERR_WORKSPACE = range(6)
+RA_F32, RA_BF16 = 0, 1
+STATUS_NAMES = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
+                4: "RA_ERR_DEVICE_TIMEOUT", 5: "RA_ERR_WORKSPACE"}
+
+# name -> (restype, argtypes), mirroring include/ra.h
+_vp, _i, _sz, _fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+SIGNATURES = {
+    "ra_blockwise_attn_fwd": (_i, [_vp, _vp, _vp, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
+    "ra_ring_partials_fwd": (_i, [_vp, _vp, _vp, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
+    "ra_lse_merge": (_i, [_vp, _fp, _vp, _fp, _i, _i, _i, _i, _i, _i, _vp]),
+    "ra_prefix_fanout_attn": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _fp, _i, _i, _i, _i,
+                                   _vp, _sz, _vp]),
+    "ra_prefix_fanout_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "ra_ring_shard_order": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
+    "ra_device_status": (_i, [_vp]),
+    "ra_last_error": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+class RAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def load(path: str = LIB_PATH):
+    """Load libra.so (built by build.py / __graft_entry__.build())."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (python -m ring_context_parallelism_gb300.build)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != RA_OK:
+        raise RAError(status, load().ra_last_error().decode())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return RA_BF16
+    if t.dtype == torch.float32:
+        return RA_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _cuda(*ts):
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("tensors must be on one device")
+    return dev
+
+
+def _stream(dev) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def attn(q, k, v, n_shards: int, block: int, causal: bool, out=None, lse=None, want_lse: bool = True):
+    """Blockwise ring-order attention.  q [B,S,Hq,D], k/v [B,S,Hkv,D] (bf16 or fp32).
+    Returns (out [B,S,Hq,D], lse [B,Hq,S] fp32 or None)."""
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, S, Hkv, D) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q/k/v shapes or dtypes disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, S, device=q.device, dtype=torch.float32)
+    dev = _cuda(q, k, v, out, lse)
+    _check(load().ra_blockwise_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, Hq, Hkv, D,
+                                        n_shards, block, int(bool(causal)), _dt(q), _stream(dev)))
+    return out, lse
+
+
+def ring_partials(q, k, v, n_shards: int, block: int, causal: bool, partials_O=None, partials_lse=None):
+    """Per-KV-shard partials: (partials_O [N,B,S,Hq,D], partials_lse [N,B,Hq,S] fp32)."""
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if partials_O is None:
+        partials_O = torch.empty((n_shards, B, S, Hq, D), device=q.device, dtype=q.dtype)
+    if partials_lse is None:
+        partials_lse = torch.empty((n_shards, B, Hq, S), device=q.device, dtype=torch.float32)
+    dev = _cuda(q, k, v, partials_O, partials_lse)
+    _check(load().ra_ring_partials_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(partials_O), _ptr(partials_lse), B, S, Hq,
+                                       Hkv, D, n_shards, block, int(bool(causal)), _dt(q), _stream(dev)))
+    return partials_O, partials_lse
+
+
+def lse_merge(partials_O, partials_lse, out=None, out_lse=None, want_lse: bool = True):
+    """Row-indexed LSE merge: partials_O [P,B,S,H,D], partials_lse [P,B,H,S] ->
+    (out [B,S,H,D], out_lse [B,H,S])."""
+    P, B, S, H, D = partials_O.shape
+    if partials_lse.shape != (P, B, H, S) or partials_lse.dtype != torch.float32:
+        raise ValueError("partials_lse must be fp32 [P,B,H,S]")
+    if out is None:
+        out = torch.empty((B, S, H, D), device=partials_O.device, dtype=partials_O.dtype)
+    if out_lse is None and want_lse:
+        out_lse = torch.empty((B, H, S), device=partials_O.device, dtype=torch.float32)
+    dev = _cuda(partials_O, partials_lse, out, out_lse)
+    _check(load().ra_lse_merge(_ptr(partials_O), _ptr(partials_lse), _ptr(out), _ptr(out_lse), P, B, S, H, D,
+                               _dt(partials_O), _stream(dev)))
+    return out, out_lse
+
+
+def fanout_workspace_size(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D, dtype=torch.bfloat16) -> int:
+    return int(load().ra_prefix_fanout_workspace_size(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D,
+                                                      RA_BF16 if dtype == torch.bfloat16 else RA_F32))
+
+
+def fanout(q_rows, branch_offsets, k_prefix, v_prefix, k_suffix, v_suffix, out=None, lse=None, workspace=None,
+           want_lse: bool = True):
+    """Shared-prefix fan-out attention.  q_rows [R,Hq,D]; branch_offsets int32 [nb+1] (device);
+    k/v_prefix [Sp,Hkv,D]; k/v_suffix [nb,Ss,Hkv,D].  Returns (out [R,Hq,D], lse [Hq,R])."""
+    R, Hq, D = q_rows.shape
+    Sp, Hkv, _ = k_prefix.shape
+    nb, Ss = k_suffix.shape[0], k_suffix.shape[1]
+    if branch_offsets.dtype != torch.int32 or branch_offsets.numel() != nb + 1:
+        raise ValueError("branch_offsets must be int32 [n_branches + 1]")
+    if out is None:
+        out = torch.empty_like(q_rows)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, R), device=q_rows.device, dtype=torch.float32)
+    need = fanout_workspace_size(R, nb, Sp, Ss, Hq, Hkv, D, q_rows.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q_rows.device, dtype=torch.uint8)
+    dev = _cuda(q_rows, branch_offsets, k_prefix, v_prefix, k_suffix, v_suffix, out, lse, workspace)
+    _check(load().ra_prefix_fanout_attn(_ptr(q_rows), _ptr(branch_offsets), nb, R, _ptr(k_prefix), _ptr(v_prefix),
+                                        Sp, _ptr(k_suffix), _ptr(v_suffix), Ss, _ptr(out), _ptr(lse), Hq, Hkv, D,
+                                        _dt(q_rows), _ptr(workspace), workspace.numel(), _stream(dev)))
+    return out, lse
+
+
+def ring_shard_order(S: int, n_shards: int, causal: bool, q_row0: int) -> list[int]:
+    """KV shards a query tile starting at q_row0 visits, in ring order (host-side, no GPU)."""
+    buf = (ctypes.c_int * max(n_shards, 1))()
+    n = load().ra_ring_shard_order(S, n_shards, int(bool(causal)), q_row0, buf)
+    if n < 0:
+        raise ValueError("invalid arguments")
+    return list(buf[:n])
+
+
+def device_status(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel recorded a device-side error."""
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    _check(load().ra_device_status(s))

@@ -1,0 +1,144 @@
+"""CPU-only checks of the C ABI: libra.so loads, exports every entry point that
+include/ra.h declares, rejects bad arguments on the host before any launch,
+and walks KV shards in the ring order the pages give."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ring_context_parallelism_gb300 as ra
+from ring_context_parallelism_gb300 import ra as rab
+from ring_context_parallelism_gb300.build import build
+from helpers import read_golden_arrows
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return ra.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ra.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ra_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("ra_blockwise_attn_fwd", "ra_lse_merge", "ra_prefix_fanout_attn", "ra_ring_partials_fwd",
+                 "ra_prefix_fanout_workspace_size", "ra_device_status", "ra_last_error", "ra_ring_shard_order"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in rab.SIGNATURES, f"binding lacks {name}"
+
+
+def _null_ring(lib, fn, **kw):
+    args = dict(q=16, k=16, v=16, out=16, lse=None, B=1, S=1024, Hq=4, Hkv=4, D=64, N=4, block=64, causal=0,
+                dt=rab.RA_F32)
+    args.update(kw)
+    return getattr(lib, fn)(args["q"], args["k"], args["v"], args["out"], args["lse"], args["B"], args["S"],
+                            args["Hq"], args["Hkv"], args["D"], args["N"], args["block"], args["causal"],
+                            args["dt"], None)
+
+
+@pytest.mark.parametrize("fn", ["ra_blockwise_attn_fwd", "ra_ring_partials_fwd"])
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), rab.RA_ERR_INVALID_ARG),
+    (dict(k=24), rab.RA_ERR_INVALID_ARG),           # misaligned
+    (dict(S=1000), rab.RA_ERR_INVALID_ARG),         # S % n_shards
+    (dict(block=48), rab.RA_ERR_INVALID_ARG),       # shard length % block
+    (dict(Hq=6, Hkv=4), rab.RA_ERR_INVALID_ARG),    # Hq % Hkv
+    (dict(D=96), rab.RA_ERR_INVALID_ARG),
+    (dict(causal=2), rab.RA_ERR_INVALID_ARG),
+    (dict(N=0), rab.RA_ERR_INVALID_ARG),
+    (dict(B=0), rab.RA_ERR_INVALID_ARG),
+    (dict(dt=7), rab.RA_ERR_INVALID_ARG),
+    (dict(dt=rab.RA_BF16, S=512, N=8), rab.RA_ERR_UNSUPPORTED),   # shard of 64 tokens < 128-key tile
+    (dict(dt=rab.RA_BF16, S=2048, N=4, block=192), rab.RA_ERR_INVALID_ARG),   # 512 % 192
+])
+def test_ring_argument_validation(lib, fn, kw, status):
+    kw = dict(kw, lse=16 if fn == "ra_ring_partials_fwd" else None)
+    rc = _null_ring(lib, fn, **kw)
+    assert rc == status, lib.ra_last_error()
+    assert lib.ra_last_error()
+
+
+def test_partials_need_lse(lib):
+    assert _null_ring(lib, "ra_ring_partials_fwd", lse=None) == rab.RA_ERR_INVALID_ARG
+
+
+def test_merge_argument_validation(lib):
+    f = lib.ra_lse_merge
+    assert f(None, 16, 16, None, 2, 1, 8, 2, 64, rab.RA_F32, None) == rab.RA_ERR_INVALID_ARG
+    assert f(16, 16, 16, None, 0, 1, 8, 2, 64, rab.RA_F32, None) == rab.RA_ERR_INVALID_ARG
+    assert f(16, 16, 16, None, 2, 1, 8, 2, 80, rab.RA_F32, None) == rab.RA_ERR_INVALID_ARG
+    assert f(16, 20, 16, None, 2, 1, 8, 2, 64, rab.RA_F32, None) == rab.RA_ERR_INVALID_ARG
+
+
+def test_fanout_argument_validation(lib):
+    f = lib.ra_prefix_fanout_attn
+    base = [16, 16, 4, 10, 16, 16, 256, 16, 16, 64, 16, None, 16, 2, 128, rab.RA_BF16, 256, 1 << 30, None]
+    def call(**kw):
+        a = list(base)
+        idx = dict(q=0, off=1, nb=2, R=3, kp=4, Sp=6, Ss=9, out=10, Hq=12, Hkv=13, D=14, dt=15, ws=16, wsb=17)
+        for k, v in kw.items():
+            a[idx[k]] = v
+        return f(*a)
+    assert call(dt=rab.RA_F32) == rab.RA_ERR_UNSUPPORTED
+    assert call(Hq=24, Hkv=8) == rab.RA_ERR_UNSUPPORTED
+    assert call(Hq=15, Hkv=2) == rab.RA_ERR_INVALID_ARG
+    assert call(nb=0) == rab.RA_ERR_INVALID_ARG
+    assert call(Sp=0, Ss=0) == rab.RA_ERR_INVALID_ARG
+    assert call(q=None) == rab.RA_ERR_INVALID_ARG
+    assert call(kp=None) == rab.RA_ERR_INVALID_ARG
+    assert call(D=32) == rab.RA_ERR_INVALID_ARG
+    assert call(ws=None) == rab.RA_ERR_WORKSPACE
+    assert call(wsb=64) == rab.RA_ERR_WORKSPACE
+    assert call(ws=272) == rab.RA_ERR_INVALID_ARG     # not 256-byte aligned
+    assert call(R=0) == rab.RA_OK                      # nothing to do, nothing launched
+
+
+def test_workspace_size_query(lib):
+    ws = ra.fanout_workspace_size(136, 16, 65536, 512, 64, 8, 128)
+    assert ws > 0 and ws % 256 == 0
+    assert ra.fanout_workspace_size(136, 16, 65536, 512, 64, 8, 96) == 0
+    assert ra.fanout_workspace_size(16, 16, 0, 512, 64, 8, 128) > 0
+
+
+def test_ring_order_matches_page_figure(lib):
+    rows = [r for r in read_golden_arrows("page_counts.txt") if r[0].startswith("ring_order")]
+    assert rows
+    for lhs, rhs in rows:
+        kv = dict(x.split("=") for x in lhs.split()[1:])
+        N, k = int(kv["N"]), int(kv["k"])
+        S = 128 * N
+        assert ra.ring_shard_order(S, N, False, k * 128) == [int(x) for x in rhs.split()]
+
+
+def test_causal_walk_skips_empty_shards(lib):
+    rows = [r for r in read_golden_arrows("page_counts.txt") if r[0].startswith("causal_pairs")]
+    assert rows
+    for lhs, rhs in rows:
+        N = int(lhs.split("=")[1])
+        S = 128 * N
+        orders = [ra.ring_shard_order(S, N, True, k * 128) for k in range(N)]
+        assert sum(len(o) for o in orders) == int(rhs)
+        for k, o in enumerate(orders):
+            assert o == list(range(k, -1, -1))      # own shard first, then k-1, ..., 0
+
+
+def test_ring_order_is_a_permutation(lib):
+    for N in (1, 2, 3, 5, 16):
+        S = N * 256
+        for row in range(0, S, 256):
+            o = ra.ring_shard_order(S, N, False, row)
+            assert sorted(o) == list(range(N)) and o[0] == row // 256
+            assert all((o[t] - o[t + 1]) % N == 1 for t in range(N - 1))
