@@ -1,0 +1,455 @@
+"""Benchmark of the blockwise ring-attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--all]
+
+One JSON line on rank 0.  The headline step is one ra_blockwise_attn_fwd call
+on the causal GQA prefill workload (B=1, S=32768, Hq=32, Hkv=8, D=128, bf16,
+8 ring shards, 128-key blocks); `value` is its causal-adjusted attention
+TFLOP/s (4*D FLOPs per unmasked query/key pair).  The same line carries the
+other rows of the path measured on their own workloads: shared-prefix fan-out
+decode (HBM GB/s), per-shard partials + LSE merge on the Llama-3-70B-shaped
+layer, and (with --all) the million-token stress case.
+
+Under torchrun (--gpus N > 1) every rank runs an independent replica of the
+same workload (the path needs no exchange between GPUs); the barrier and the
+max over ranks are timing only.  `--impl reference` times the fp64 CPU oracle
+on a bounded sample of the same workload (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s (causal-adjusted) & % bf16 peak; fan-out decode HBM GB/s"
+HEADLINE = "gqa_causal_prefill_32k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes (read + write) per launch of the headline kernel from an ncu
+# capture, valid only while the kernel source hashes to the recorded value.
+NCU_TRAFFIC = {}
+
+
+# ----------------------------------------------------------------------------------------------
+# work accounting (algorithmic FLOPs and bytes)
+# ----------------------------------------------------------------------------------------------
+
+def ring_flops(B, S, Hq, D, causal):
+    """4*D FLOPs (QK^T and PV) per unmasked (query, key) pair."""
+    pairs = S * (S + 1) // 2 if causal else S * S
+    return 4 * D * Hq * B * pairs
+
+
+def fanout_flops(R, Hq, D, S_prefix, S_suffix):
+    return 4 * D * Hq * R * (S_prefix + S_suffix)
+
+
+def fanout_bytes(R, n_branches, Hq, Hkv, D, S_prefix, S_suffix, esz=2):
+    """Prefix K+V once, every suffix K+V once, Q in, O out, lse out."""
+    kv = 2 * esz * Hkv * D * (S_prefix + n_branches * S_suffix)
+    return kv + 2 * esz * R * Hq * D + 4 * Hq * R
+
+
+def ring_bytes(B, S, Hq, Hkv, D, esz=2):
+    return esz * B * S * D * (2 * Hq + 2 * Hkv) + 4 * B * Hq * S
+
+
+def merge_bytes(P, B, S, H, D, esz=2):
+    return P * B * S * H * (D * esz + 4) + B * S * H * (D * esz + 4)
+
+
+def peaks():
+    p = dict(FALLBACK_PEAKS)
+    src = "fallback"
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            m = json.load(open(path))
+            for k in p:
+                if k in m:
+                    p[k] = float(m[k])
+            src = "measured"
+        except Exception:
+            pass
+    p["source"] = src
+    return p
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in ("attn_tc.cu", "ra_device.cuh", "ra_walk.h"):
+        h.update(open(os.path.join(ROOT, "ring_context_parallelism_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        busy = [s for s in sm if mx and s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------------------------
+# timing helpers
+# ----------------------------------------------------------------------------------------------
+
+def timed_steps(fn, steps, warmup, flush=None):
+    """W untimed calls, then K calls each bracketed by CUDA events on the current
+    stream (L2 flushed before each call, outside the events).  Returns per-step ms."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in ev:
+        if flush is not None:
+            flush()
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in ev]
+
+
+def make_flush(nbytes=512 << 20):
+    import torch
+
+    buf = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+
+    def flush():
+        buf.fill_(1.0)
+
+    return flush
+
+
+# ----------------------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------------------
+
+def run_ours(args, rank, world):
+    import torch
+
+    import ring_context_parallelism_gb300 as ra
+    from ring_context_parallelism_gb300.build import build
+    from ring_context_parallelism_gb300.inputs import WORKLOADS, attention_inputs, fanout_inputs
+
+    if rank == 0 or not os.path.exists(os.path.join(ROOT, "ring_context_parallelism_gb300", "libra.so")):
+        build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    ra.load()
+    pk = peaks()
+    flush = make_flush()
+    w = WORKLOADS[HEADLINE]
+    q, k, v = attention_inputs(w, "cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.S, device="cuda", dtype=torch.float32)
+    flops = ring_flops(w.B, w.S, w.Hq, w.D, w.causal)
+
+    def step():
+        ra.attn(q, k, v, w.n_shards, w.block, w.causal, out=out, lse=lse)
+
+    result = {}
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        # headline: K timed steps between barriers + syncs
+        for _ in range(args.warmup):
+            step()
+        ra.device_status()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        ms = timed_steps(step, args.steps, 0, flush)
+        ra.device_status()
+        total_ms = sum(ms)
+        if world > 1:
+            t = torch.tensor([total_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            total_ms = float(t.item())
+        ms_step = total_ms / args.steps
+        value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+        # e2e through the public API with host buffers
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            O, L = ra.attn(qd, kd, vd, w.n_shards, w.block, w.causal, out=out, lse=lse)
+            oh.copy_(O, non_blocking=True)
+            lh.copy_(L, non_blocking=True)
+
+        e2e_ms = timed_steps(e2e_step, max(3, min(args.steps, 10)), 2, flush)
+        ra.device_status()
+        e2e = {"value": flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+               "ms_per_step": statistics.mean(e2e_ms),
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (qh, kh, vh)),
+               "d2h_bytes_per_step": oh.numel() * oh.element_size() + lh.numel() * lh.element_size()}
+        del qh, kh, vh, oh, lh, qd, kd, vd
+
+        # fan-out decode (config 4) and its R=16 sub-case
+        for name in ("fanout_decode", "fanout_decode1"):
+            fw = WORKLOADS[name]
+            x = fanout_inputs(fw, "cuda")
+            R = x["R"]
+            fo = torch.empty_like(x["q_rows"])
+            fl = torch.empty(fw.Hq, R, device="cuda", dtype=torch.float32)
+            ws = torch.empty(ra.fanout_workspace_size(R, fw.n_branches, fw.S_prefix, fw.S_suffix, fw.Hq, fw.Hkv,
+                                                      fw.D), dtype=torch.uint8, device="cuda")
+
+            def fstep():
+                ra.fanout(x["q_rows"], x["offsets"], x["k_prefix"], x["v_prefix"], x["k_suffix"], x["v_suffix"],
+                          out=fo, lse=fl, workspace=ws)
+
+            fms = timed_steps(fstep, 20, 5, flush)
+            ra.device_status()
+            t = statistics.median(fms) * 1e-3
+            by = fanout_bytes(R, fw.n_branches, fw.Hq, fw.Hkv, fw.D, fw.S_prefix, fw.S_suffix)
+            fl_ = fanout_flops(R, fw.Hq, fw.D, fw.S_prefix, fw.S_suffix)
+            bound_t = max(by / (pk["hbm_gbs"] * 1e9), fl_ / (pk["bf16_tflops"] * 1e12))
+            result[name] = {"R": R, "rows_per_branch": x["rows"], "us": t * 1e6, "GB_per_s": by / t / 1e9,
+                            "frac_hbm": by / t / 1e9 / pk["hbm_gbs"], "TFLOP_per_s": fl_ / t / 1e12,
+                            "frac_binding_roofline": bound_t / t, "algorithmic_bytes": by, "flops": fl_,
+                            "workspace_bytes": ws.numel(), "launches_per_call": 2}
+            del x, fo, fl, ws
+
+        # per-shard partials + LSE merge on the Llama-3-70B-shaped layer
+        pw = WORKLOADS["llama70b_layer_128k_partials"]
+        del q, k, v, out, lse
+        torch.cuda.empty_cache()
+        pq, pkk, pv = attention_inputs(pw, "cuda")
+        pO = torch.empty((pw.n_shards, pw.B, pw.S, pw.Hq, pw.D), device="cuda", dtype=pq.dtype)
+        pL = torch.empty((pw.n_shards, pw.B, pw.Hq, pw.S), device="cuda", dtype=torch.float32)
+        mO = torch.empty_like(pq)
+        mL = torch.empty(pw.B, pw.Hq, pw.S, device="cuda", dtype=torch.float32)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        times = []
+        for it in range(3):
+            flush()
+            ev[0].record()
+            ra.ring_partials(pq, pkk, pv, pw.n_shards, pw.block, pw.causal, partials_O=pO, partials_lse=pL)
+            ev[1].record()
+            ra.lse_merge(pO, pL, out=mO, out_lse=mL)
+            ev[2].record()
+            torch.cuda.synchronize()
+            if it > 0:
+                times.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
+        ra.device_status()
+        pf = ring_flops(pw.B, pw.S, pw.Hq, pw.D, pw.causal)
+        tp = statistics.mean(t[0] for t in times) * 1e-3
+        tm = statistics.mean(t[1] for t in times) * 1e-3
+        mb = merge_bytes(pw.n_shards, pw.B, pw.S, pw.Hq, pw.D)
+        result["llama70b_layer_128k_partials"] = {
+            "partials_ms": tp * 1e3, "partials_TFLOP_per_s": pf / tp / 1e12,
+            "merge_ms": tm * 1e3, "merge_GB_per_s": mb / tm / 1e9, "merge_frac_hbm": mb / tm / 1e9 / pk["hbm_gbs"],
+            "pipeline_ms": (tp + tm) * 1e3, "pipeline_TFLOP_per_s": pf / (tp + tm) / 1e12, "flops": pf,
+            "partials_bytes": pO.numel() * 2 + pL.numel() * 4}
+        del pq, pkk, pv, pO, pL, mO, mL
+        torch.cuda.empty_cache()
+
+        if args.all:
+            sw = WORKLOADS["million_token_stress"]
+            sq, sk, sv = attention_inputs(sw, "cuda")
+            so = torch.empty_like(sq)
+            sl = torch.empty(sw.B, sw.Hq, sw.S, device="cuda", dtype=torch.float32)
+            sms = timed_steps(lambda: ra.attn(sq, sk, sv, sw.n_shards, sw.block, True, out=so, lse=sl), 1, 1)
+            ra.device_status()
+            sf = ring_flops(sw.B, sw.S, sw.Hq, sw.D, True)
+            result["million_token_stress"] = {"s": sms[0] / 1e3, "TFLOP_per_s": sf / (sms[0] * 1e-3) / 1e12,
+                                              "frac_bf16_peak": sf / (sms[0] * 1e-3) / 1e12 / pk["bf16_tflops"]}
+            del sq, sk, sv, so, sl
+
+    clocks = clk.summary()
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    kh = kernel_hash()
+    traffic = NCU_TRAFFIC.get(kh)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic: seeded N(0,1) bf16 inputs",
+        "config": {"workload": HEADLINE, "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "n_shards": w.n_shards, "block": w.block, "causal": w.causal, "flops_per_step": flops,
+                   "l2": "flushed before every step (512 MB write); inputs 402 MB > L2",
+                   "parallelism": f"replicas x{world}"},
+        "pct_bf16_peak": 100.0 * achieved / pk["bf16_tflops"],
+        "roofline": {"kernel": "attn_tc_kernel<128>", "bound": "tensor", "achieved": achieved,
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                     "peak_source": pk["source"] + " (burst)",
+                     "frac_of_sustained": achieved / pk["bf16_tflops_sustained"],
+                     "traffic": traffic, "algorithmic_bytes": ring_bytes(w.B, w.S, w.Hq, w.Hkv, w.D),
+                     "kernel_hash": kh},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    line.update(result)
+    return line
+
+
+# ----------------------------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# ----------------------------------------------------------------------------------------------
+
+def oracle_sample_rate(target_s=10.0, max_queries=1 << 16, seed=0):
+    """Times the fp64 oracle on seeded query samples of the headline workload
+    until about target_s seconds of CPU work; returns (TFLOP/s, seconds,
+    queries, cores)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from ring_context_parallelism_gb300.inputs import WORKLOADS, attention_inputs
+
+    w = WORKLOADS[HEADLINE]
+    # the headline workload's shapes and seed, drawn on the host
+    q, k, v = attention_inputs(w, "cpu")
+    qs = q.view(torch.int16).numpy().view(np.uint16)
+    ks = k.view(torch.int16).numpy().view(np.uint16)
+    vs = v.view(torch.int16).numpy().view(np.uint16)
+    cores = oracle.max_threads()
+    n = 256
+    done_q, done_flops, spent = 0, 0, 0.0
+    rng = np.random.default_rng(seed)
+    while spent < target_s and done_q < max_queries:
+        ids = np.sort(rng.choice(w.B * w.S * w.Hq, size=n, replace=False)).astype(np.int64)
+        rows = (ids // w.Hq) % w.S
+        t0 = time.perf_counter()
+        oracle.attention(qs, ks, vs, dtype="bf16", causal=w.causal, sel=ids)
+        dt = time.perf_counter() - t0
+        spent += dt
+        done_q += n
+        done_flops += int(4 * w.D * (rows + 1).sum())
+        if dt < target_s / 8:
+            n *= 2
+    return done_flops / spent / 1e12, spent, done_q, cores
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle, timed per step on a bounded
+    sample of the headline workload's queries."""
+    per_step = []
+    cores = None
+    queries = 0
+    for i in range(args.warmup + args.steps):
+        rate, spent, nq, cores = oracle_sample_rate(target_s=2.0, max_queries=4096, seed=i)
+        if i >= args.warmup:
+            per_step.append((rate, spent, nq))
+            queries += nq
+    value = statistics.mean(r for r, _, _ in per_step)
+    ms = statistics.mean(s for _, s, _ in per_step) * 1e3
+    sample = (f"{queries} seeded (row, head) queries of {HEADLINE} over {args.steps} steps "
+              f"(about 2 s of CPU work per step); FLOPs counted as 4*D per visible key")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic: seeded N(0,1) bf16 inputs",
+            "config": {"workload": HEADLINE}, "gpu_launches": 0,
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--all", action="store_true", help="also time the million-token stress workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    import torch
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = run_ours(args, rank, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, spent, nq, cores = oracle_sample_rate()
+        line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{nq} seeded (row, head) queries of {HEADLINE}, {spent:.1f} s of "
+                                          f"CPU work; FLOPs counted as 4*D per visible key"}
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
