@@ -148,6 +148,41 @@ size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int 
                                        int Hkv, int D, ra_dtype dt);
 
 /*
+ * Size of the device scratch array behind ra_prefix_fanout_attn_noalloc:
+ * 32 MiB, held on every GPU that loads libra.so until the process exits.
+ */
+#define RA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * ra_prefix_fanout_attn without a workspace argument, for callers that cannot
+ * allocate device memory themselves -- for example a plugin inside a host
+ * framework that owns every allocation and hands it only fixed input/output
+ * buffers, or a latency-critical decode loop where a cudaMalloc (which can
+ * synchronise the device) is not allowed.  The pages have no counterpart: this
+ * is a packaging variant of the fan-out entry point above, not a step of the
+ * method.
+ *
+ * Same arguments, layouts, semantics and errors as ra_prefix_fanout_attn, minus
+ * the workspace.  The partials live instead in one file-scope device array of
+ * RA_NOALLOC_SCRATCH_BYTES inside the library; the prefix is split into as
+ * many chunks as fit in it.  A call whose partials cannot fit even with one
+ * prefix chunk (roughly R * Hq * D * 8 bytes > RA_NOALLOC_SCRATCH_BYTES) is
+ * rejected with RA_ERR_WORKSPACE before anything is launched.  Nothing is
+ * allocated or freed: no cudaMalloc, no cudaFree, no allocating library call.
+ *
+ * The first call on a device (with that device current) looks up the array's
+ * device address with cudaGetSymbolAddress; make that first call before any
+ * stream capture.  Every call, on every stream, shares the one array, and it
+ * keeps the previous call's contents (nothing in it needs to start at zero):
+ * calls that can overlap on the GPU race on it, so serialise them, e.g. on
+ * one stream.
+ */
+ra_status ra_prefix_fanout_attn_noalloc(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                                        const void* k_prefix, const void* v_prefix, int S_prefix,
+                                        const void* k_suffix, const void* v_suffix, int S_suffix, void* out,
+                                        float* lse, int Hq, int Hkv, int D, ra_dtype dt, void* stream);
+
+/*
  * Host-side view of the ring walk the kernels take (no GPU needed): for the
  * 128-row query tile starting at q_row0, writes to shard_order[] the KV shards
  * in the order they are visited ((k - t) mod n_shards, causal-empty shards

@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 
 #include "../../include/ra.h"
 #include "ra_internal.h"
@@ -137,6 +138,57 @@ ra_status check_fanout(const void* q_rows, const int* offsets, int n_branches, i
 
 }  // namespace
 
+// Scratch of ra_prefix_fanout_attn_noalloc: the fan-out partials of callers
+// that cannot allocate a workspace.  Shared by every such call on a device.
+static __device__ __align__(256) unsigned char g_fanout_scratch[RA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_fanout_scratch on the current device, looked up once per
+// device (host code only sees a stand-in for the array's name).
+ra_status scratch_address(void** addr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(RA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fanout_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fan-out scratch)");
+        g_scratch_addr[dev] = p;
+    }
+    *addr = g_scratch_addr[dev];
+    return RA_OK;
+}
+
+// The usual plan if its partials fit in the scratch array, else the largest
+// chunk count that does; total == 0 if none fits.
+FanoutPlan plan_fanout_bounded(int R, int S_prefix, int S_suffix, int Hq, int Hkv, int D, size_t cap) {
+    FanoutPlan f = plan_fanout(R, S_prefix, S_suffix, Hq, Hkv, D);
+    if (f.total <= cap) return f;
+    const int n_tiles = (S_prefix + 127) / 128;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    for (int c = f.n_chunks - 1; c >= 1; --c) {
+        FanoutPlan g{};
+        g.chunk_tiles = (n_tiles + c - 1) / c;
+        g.n_chunks = (n_tiles + g.chunk_tiles - 1) / g.chunk_tiles;
+        g.P = g.n_chunks + (S_suffix > 0 ? 1 : 0);
+        g.part_o_bytes = up(static_cast<size_t>(g.P) * R * Hq * D * sizeof(float));
+        g.part_lse_bytes = up(static_cast<size_t>(g.P) * Hq * R * sizeof(float));
+        g.total = g.part_o_bytes + g.part_lse_bytes;
+        if (g.total <= cap) return g;
+    }
+    FanoutPlan none{};
+    return none;
+}
+
+}  // namespace
+
 extern "C" {
 
 ra_status ra_blockwise_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int S,
@@ -191,6 +243,60 @@ ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, i
         return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     float* part_o = static_cast<float*>(workspace);
     float* part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + f.part_o_bytes);
+
+    ra::FanoutTcArgs a{};
+    a.q_rows = q_rows;
+    a.offsets = branch_offsets;
+    a.n_branches = n_branches;
+    a.R = R;
+    a.k_prefix = k_prefix;
+    a.v_prefix = v_prefix;
+    a.S_prefix = S_prefix;
+    a.k_suffix = k_suffix;
+    a.v_suffix = v_suffix;
+    a.S_suffix = S_suffix;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.n_chunks = f.n_chunks;
+    a.chunk_tiles = f.chunk_tiles;
+    a.part.o = part_o;
+    a.part.lse = part_lse;
+    a.part.o_row = static_cast<long long>(Hq) * D;
+    a.part.o_h = D;
+    a.part.o_part = static_cast<long long>(R) * Hq * D;
+    a.part.lse_h = R;
+    a.part.lse_part = static_cast<long long>(Hq) * R;
+    a.part.o_f32 = 1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = ra::launch_fanout_tc(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fan-out attention launch");
+    ra::MergeArgs m{part_o, part_lse, out, lse, f.P, 1, R, Hq, D, 1, 0};
+    e = ra::launch_lse_merge(m, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fan-out merge launch");
+    return ok();
+}
+
+ra_status ra_prefix_fanout_attn_noalloc(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                                        const void* k_prefix, const void* v_prefix, int S_prefix,
+                                        const void* k_suffix, const void* v_suffix, int S_suffix, void* out,
+                                        float* lse, int Hq, int Hkv, int D, ra_dtype dt, void* stream) {
+    ra_status st = check_fanout(q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix, k_suffix,
+                                v_suffix, S_suffix, out, Hq, Hkv, D, dt);
+    if (st != RA_OK) return st;
+    if (lse && !aligned16(lse)) return fail(RA_ERR_INVALID_ARG, "lse must be 16-byte aligned");
+    if (R == 0) return ok();
+    const size_t cap = RA_NOALLOC_SCRATCH_BYTES;
+    const FanoutPlan f = plan_fanout_bounded(R, S_prefix, S_suffix, Hq, Hkv, D, cap);
+    if (f.total == 0)
+        return fail(RA_ERR_WORKSPACE,
+                    "fan-out partials for R=%d, Hq=%d, D=%d do not fit the %zu-byte static scratch; "
+                    "use ra_prefix_fanout_attn with a workspace", R, Hq, D, cap);
+    void* scratch = nullptr;
+    st = scratch_address(&scratch);
+    if (st != RA_OK) return st;
+    float* part_o = static_cast<float*>(scratch);
+    float* part_lse = reinterpret_cast<float*>(static_cast<char*>(scratch) + f.part_o_bytes);
 
     ra::FanoutTcArgs a{};
     a.q_rows = q_rows;

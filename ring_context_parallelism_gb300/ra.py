@@ -30,6 +30,8 @@ SIGNATURES = {
     "ra_prefix_fanout_attn": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _fp, _i, _i, _i, _i,
                                    _vp, _sz, _vp]),
     "ra_prefix_fanout_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "ra_prefix_fanout_attn_noalloc": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _fp, _i, _i, _i, _i,
+                                           _vp]),
     "ra_ring_shard_order": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
     "ra_device_status": (_i, [_vp]),
     "ra_last_error": (ctypes.c_char_p, []),
@@ -168,6 +170,28 @@ def fanout(q_rows, branch_offsets, k_prefix, v_prefix, k_suffix, v_suffix, out=N
     _check(load().ra_prefix_fanout_attn(_ptr(q_rows), _ptr(branch_offsets), nb, R, _ptr(k_prefix), _ptr(v_prefix),
                                         Sp, _ptr(k_suffix), _ptr(v_suffix), Ss, _ptr(out), _ptr(lse), Hq, Hkv, D,
                                         _dt(q_rows), _ptr(workspace), workspace.numel(), _stream(dev)))
+    return out, lse
+
+
+def fanout_noalloc(q_rows, branch_offsets, k_prefix, v_prefix, k_suffix, v_suffix, out=None, lse=None,
+                   want_lse: bool = True):
+    """Shared-prefix fan-out through ra_prefix_fanout_attn_noalloc: for callers
+    that cannot allocate device scratch, the partials go to the library's
+    static device array instead of a workspace.  Same arguments and results as
+    fanout() minus the workspace; calls sharing a device must not overlap."""
+    R, Hq, D = q_rows.shape
+    Sp, Hkv, _ = k_prefix.shape
+    nb, Ss = k_suffix.shape[0], k_suffix.shape[1]
+    if branch_offsets.dtype != torch.int32 or branch_offsets.numel() != nb + 1:
+        raise ValueError("branch_offsets must be int32 [n_branches + 1]")
+    if out is None:
+        out = torch.empty_like(q_rows)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, R), device=q_rows.device, dtype=torch.float32)
+    dev = _cuda(q_rows, branch_offsets, k_prefix, v_prefix, k_suffix, v_suffix, out, lse)
+    _check(load().ra_prefix_fanout_attn_noalloc(_ptr(q_rows), _ptr(branch_offsets), nb, R, _ptr(k_prefix),
+                                                _ptr(v_prefix), Sp, _ptr(k_suffix), _ptr(v_suffix), Ss, _ptr(out),
+                                                _ptr(lse), Hq, Hkv, D, _dt(q_rows), _stream(dev)))
     return out, lse
 
 
