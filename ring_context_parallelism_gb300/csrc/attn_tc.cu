@@ -259,8 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int T = u.T;
     unsigned* status = g_tc_status;
 
+    // Register split, set inside each role: 128 x 40 (producer / MMA
+    // warpgroup) + 2 x 128 x 232 (softmax warpgroups) = 64512, the 384 x 168
+    // registers of the launch.
+
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
         if (lane == 0) {
             const CUtensorMap* km = u.suffix ? &tm_k2 : &tm_k;
             const CUtensorMap* vm = u.suffix ? &tm_v2 : &tm_v;
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, false, true);
@@ -361,9 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(drain);
             mbar_wait(drain, 0, abort_flag, status, 0);
         }
-    } else if (warp >= 4 && (warp - 4) / 4 < T) {
+    } else if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
+    } else {
         // ------------------------------------------------------------ softmax + epilogue
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
         const int t = (warp - 4) >> 2;
+        if (t < T) {
         const int quad = warp & 3;
         const int lane_row = quad * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -419,23 +429,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!(ok = mbar_wait(&s_full[t], i & 1, abort_flag, status, 0x07000000u | i))) break;
             tc_fence_after();
-            float x[kTileN];
+            uint32_t sr[kTileN];
 #pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(tS + c * 32, reinterpret_cast<uint32_t*>(x) + c * 32);
+            for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
             tmem_wait_ld();
-            // visible columns of this tile: c <= lim
+            // visible columns of this tile: c <= lim (only diagonal and tail tiles mask)
             int lim = kTileN - 1;
             if (!p.fanout) {
                 if (p.causal) lim = min(lim, row - ti.kb);
             } else {
                 lim = min(lim, u.kv_hi - 1 - ti.kb);
             }
-            float mx = -INFINITY;
+            if (lim < kTileN - 1) {
 #pragma unroll
-            for (int c = 0; c < kTileN; ++c) {
-                x[c] = (c <= lim) ? x[c] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, x[c]);
+                for (int c = 0; c < kTileN; ++c)
+                    if (c > lim) sr[c] = 0xff800000u;  // -inf
             }
+            float mraw = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTileN; c += 2) mraw = fmax3(mraw, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            const float mx = mraw * p.scale_log2;  // scores in log2 units
             const bool fresh = (i == 0) || (p.partials && ti.first);
             float alpha = 1.f;
             bool resc = false;
@@ -447,16 +460,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_use = mx;
                 resc = true;
             }
-            const float ms = (m_use == -INFINITY) ? 0.f : m_use;
-            float rs = 0.f;
+            const float neg_ms = (m_use == -INFINITY) ? 0.f : -m_use;
+            const float sc = p.scale_log2;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
             for (int c0 = 0; c0 < kTileN; c0 += 32) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float p0 = ex2_approx(x[c0 + 2 * j] - ms);
-                    const float p1 = ex2_approx(x[c0 + 2 * j + 1] - ms);
-                    rs += p0 + p1;
+                    float y0, y1;
+                    ffma2(y0, y1, __uint_as_float(sr[c0 + 2 * j]), __uint_as_float(sr[c0 + 2 * j + 1]), sc, sc,
+                          neg_ms, neg_ms);
+                    const float p0 = ex2_approx(y0);
+                    const float p1 = ex2_approx(y1);
+                    if (j & 1)
+                        fadd2(a2, a3, p0, p1);
+                    else
+                        fadd2(a0, a1, p0, p1);
                     pk[j] = pack_bf16x2(p0, p1);
                 }
                 asm volatile(
@@ -467,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     "r"(pk[15])
                     : "memory");
             }
+            const float rs = (a0 + a1) + (a2 + a3);
             l_sum = l_sum * alpha + rs;
             if (__any_sync(0xffffffffu, resc)) {
                 // O of the previous tiles must be complete before it is rescaled
@@ -506,6 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < D / 32; ++c) store_row<D>(out, ob, c, zeros, 0.f);
                 if (out.lse) out.lse[lse_base + static_cast<long long>(j) * out.lse_part] = -INFINITY;
             }
+        }
         }
         tc_fence_before();
     }

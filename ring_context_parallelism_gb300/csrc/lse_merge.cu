@@ -11,7 +11,7 @@
 // weight 0 and its O is not read.
 //
 // One warp per (b, s, h) row; lane l owns D/32 consecutive head dims, so a
-// warp reads each partial row as one contiguous 128- or 256/512-byte segment.
+// warp reads each partial row as one contiguous 128- to 512-byte segment.
 // fp32 arithmetic.  Bandwidth-bound: each partial row is read once.
 #include <cmath>
 
@@ -89,9 +89,15 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const void* __re
     const long long o_stride = rows * D;  // elements between partials
     const long long l_stride = rows;
 
-    // max over partials (lanes stride over p)
+    // Lane j holds lse of partial g*32 + j; the weights are broadcast with
+    // shuffles and the partials' rows are loaded 8 at a time so that several
+    // loads are in flight per lane.
     float M = -INFINITY;
-    for (int pp = lane; pp < P; pp += 32) M = fmaxf(M, part_lse[pp * l_stride + lse_idx]);
+    for (int g = 0; g < P; g += 32) {
+        const int pp = g + lane;
+        const float L = pp < P ? part_lse[pp * l_stride + lse_idx] : -INFINITY;
+        M = fmaxf(M, L);
+    }
 #pragma unroll
     for (int x = 16; x; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
 
@@ -102,15 +108,34 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const void* __re
     if (M != -INFINITY) {
         const size_t esz = PART_F32 ? 4 : 2;
         const char* base = static_cast<const char*>(part_O) + (rid * D + lane * E) * esz;
-        for (int pp = 0; pp < P; ++pp) {
-            const float L = part_lse[pp * l_stride + lse_idx];
-            if (L == -INFINITY) continue;  // empty partial: weight 0, O not read
-            const float w = expf(L - M);
-            wsum += w;
-            float x[E];
-            Vec<E, PART_F32>::load(base + pp * o_stride * esz, x);
+        for (int g = 0; g < P; g += 32) {
+            const int pp = g + lane;
+            const float L = pp < P ? part_lse[pp * l_stride + lse_idx] : -INFINITY;
+            const float myw = (L == -INFINITY) ? 0.f : expf(L - M);   // empty partial: weight 0
+            float ws = myw;
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+            for (int x = 16; x; x >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, x);
+            wsum += ws;
+            const int n = min(32, P - g);
+            for (int j0 = 0; j0 < n; j0 += 8) {
+                float w[8];
+                float x[8][E];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    w[j] = __shfl_sync(0xffffffffu, myw, (j0 + j) & 31);
+                    if (j0 + j >= n) w[j] = 0.f;
+                    if (w[j] != 0.f) {
+                        Vec<E, PART_F32>::load(base + static_cast<long long>(g + j0 + j) * o_stride * esz, x[j]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < E; ++e) x[j][e] = 0.f;   // O of an empty partial is not read
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[e] = fmaf(w[j], x[j][e], acc[e]);
+            }
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
