@@ -64,8 +64,13 @@ def ring_bytes(B, S, Hq, Hkv, D, esz=2):
     return esz * B * S * D * (2 * Hq + 2 * Hkv) + 4 * B * Hq * S
 
 
-def merge_bytes(P, B, S, H, D, esz=2):
-    return P * B * S * H * (D * esz + 4) + B * S * H * (D * esz + 4)
+def merge_bytes(P, B, S, H, D, esz=2, causal=False):
+    """Non-empty partial rows read once (with a causal mask, the query rows of
+    shard k have k + 1 non-empty shard partials), every partial lse read, the
+    merged O and lse written."""
+    L = S // P
+    nonempty_rows = B * H * (L * P * (P + 1) // 2 if causal else S * P)
+    return nonempty_rows * D * esz + P * B * S * H * 4 + B * S * H * (D * esz + 4)
 
 
 def peaks():
@@ -301,7 +306,7 @@ def run_ours(args, rank, world):
         pf = ring_flops(pw.B, pw.S, pw.Hq, pw.D, pw.causal)
         tp = statistics.mean(t[0] for t in times) * 1e-3
         tm = statistics.mean(t[1] for t in times) * 1e-3
-        mb = merge_bytes(pw.n_shards, pw.B, pw.S, pw.Hq, pw.D)
+        mb = merge_bytes(pw.n_shards, pw.B, pw.S, pw.Hq, pw.D, causal=pw.causal)
         result["llama70b_layer_128k_partials"] = {
             "partials_ms": tp * 1e3, "partials_TFLOP_per_s": pf / tp / 1e12,
             "merge_ms": tm * 1e3, "merge_GB_per_s": mb / tm / 1e9, "merge_frac_hbm": mb / tm / 1e9 / pk["hbm_gbs"],

@@ -18,7 +18,7 @@
 // result (O and l share it) and skips the O rescale.
 //
 // Roles (384 threads):  warp 0 lane 0  TMA producer (Q once, then K_i, V_i
-// into a 4-stage smem ring);  warp 1 lane 0  MMA issuer (also allocates TMEM);
+// into a 4-stage smem ring, 8 for D = 64);  warp 1 lane 0  MMA issuer (also allocates TMEM);
 // warps 4-7  softmax + epilogue of tile 0;  warps 8-11  same for tile 1.
 // TMEM: tile t uses columns [256t, 256t+128) for S (P~ overwrites its first
 // half as packed bf16) and [256t+128, 256t+128+D) for O.
@@ -56,6 +56,8 @@ struct TcParams {
     // fan-out
     int R, G, rows_per_tile, n_mpairs, S_prefix, chunk_tiles, n_chunks, S_suffix, n_branches,
         suffix_mpairs, n_prefix_units;
+    int split_prefix;   // prefix units hold one row tile: split their KV tiles over both tile slots
+    int suffix_slot0;   // first partial slot of the suffix (2 slots per suffix unit)
     const int* offsets;
     float scale_log2;
     OutDesc out;
@@ -65,12 +67,16 @@ template <int D>
 struct Cfg {
     static constexpr int kChunks = D / 64;                   // 128-byte column groups per row
     static constexpr int kTileBytes = kTileM * D * 2;        // one Q/K/V tile
-    static constexpr int kStages = D == 128 ? 4 : 6;
+#ifndef RA_TC_STAGES_D128
+#define RA_TC_STAGES_D128 4
+#endif
+    static constexpr int kStages = D == 128 ? RA_TC_STAGES_D128 : 8;  // up to the 227 KB of shared memory
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
     static constexpr int kNumBars = 1 + 2 * kStages + 7;
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
+    static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 };
 
 // Unit of work of one CTA, identical in every thread.
@@ -83,13 +89,19 @@ struct Unit {
     // ring
     int b, head[2], q_row0;
     // fan-out
-    int row0[2], row_hi, kv_lo, kv_hi, part;
+    int row0[2], row_hi, kv_lo, kv_hi;
+    int split;             // both tiles share Q tile 0 and take alternate KV tiles
+    int n_q;               // Q tiles to load
+    int slot[2];           // output partial slot per tile
+    int empty_slot;        // fan-out suffix without split: slot that gets lse = -inf for these rows (-1: none)
 };
 
 __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
     Unit u;
     u.valid = 1;
     u.suffix = 0;
+    u.split = 0;
+    u.empty_slot = -1;
     const int idx = blockIdx.x;
     if (!p.fanout) {
         const int groups = p.B * p.n_head_groups;
@@ -108,21 +120,33 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         }
         u.kv_head = u.head[0] / (p.Hq / p.Hkv);
         u.kv_z = u.b;
+        u.n_q = u.T;
+        u.slot[0] = u.slot[1] = 0;
         return u;
     }
     u.b = 0;
     int mp;
     if (idx < p.n_prefix_units) {
+        // KV head varies fastest after the row pair: the CTAs of one chunk's
+        // heads run together and stream the same token rows, which share DRAM
+        // pages ([S, Hkv, D] layout).
         mp = idx % p.n_mpairs;
         const int rest = idx / p.n_mpairs;
+#ifndef RA_FANOUT_CHUNK_FASTEST
+        u.kv_head = rest % p.Hkv;
+        const int chunk = rest / p.Hkv;
+#else
         const int chunk = rest % p.n_chunks;
         u.kv_head = rest / p.n_chunks;
+#endif
         u.kv_z = 0;
         u.kv_lo = chunk * p.chunk_tiles * kTileN;
         u.kv_hi = min(p.S_prefix, u.kv_lo + p.chunk_tiles * kTileN);
-        u.part = chunk;
         u.row0[0] = 2 * mp * p.rows_per_tile;
         u.row_hi = p.R;
+        u.split = p.split_prefix;
+        u.slot[0] = p.split_prefix ? 2 * chunk : chunk;
+        u.slot[1] = p.split_prefix ? 2 * chunk + 1 : chunk;
     } else {
         const int j = idx - p.n_prefix_units;
         mp = j % p.suffix_mpairs;
@@ -143,13 +167,17 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         u.kv_z = br;
         u.kv_lo = 0;
         u.kv_hi = p.S_suffix;
-        u.part = p.n_chunks;
         u.row0[0] = lo + 2 * mp * p.rows_per_tile;
         u.row_hi = hi;
+        u.split = (hi - lo <= p.rows_per_tile) ? 1 : 0;
+        u.slot[0] = p.suffix_slot0;
+        u.slot[1] = p.suffix_slot0 + (u.split ? 1 : 0);
+        if (!u.split) u.empty_slot = p.suffix_slot0 + 1;
     }
-    u.row0[1] = u.row0[0] + p.rows_per_tile;
+    u.row0[1] = u.split ? u.row0[0] : u.row0[0] + p.rows_per_tile;
     if (u.row0[0] >= u.row_hi) u.valid = 0;
-    u.T = (u.row0[1] < u.row_hi) ? 2 : 1;
+    u.T = (u.split || u.row0[1] < u.row_hi) ? 2 : 1;
+    u.n_q = u.split ? 1 : u.T;
     for (int t = 0; t < 2; ++t) {
         u.qc1[t] = 0;
         u.qc2[t] = u.kv_head;
@@ -272,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(km);
             tma_prefetch_desc(vm);
-            mbar_arrive_expect_tx(q_full, T * C::kTileBytes);
-            for (int t = 0; t < T; ++t)
+            mbar_arrive_expect_tx(q_full, u.n_q * C::kTileBytes);
+            for (int t = 0; t < u.n_q; ++t)
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_4d(&tm_q, q_full, q_smem + t * C::kTileBytes + c * 16384, c * 64, u.qc1[t], u.qc2[t],
                                 u.qc3[t]);
@@ -298,7 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*abort_flag) {
                 // let copies already in flight land before the CTA exits
                 for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
-                    mbar_wait(&kv_full[it % C::kStages], (it / C::kStages) & 1, abort_flag, status, 0);
+                    mbar_wait_landing(&kv_full[it % C::kStages], (it / C::kStages) & 1);
+                mbar_wait_landing(q_full, 0);
             }
         }
     } else if (warp == 1) {
@@ -311,7 +340,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t kv_addr = smem_u32(kv_smem);
             bool ok = mbar_wait(q_full, 0, abort_flag, status, 0x02000000u);
             tc_fence_after();
-            for (int i = 0; ok && i <= total; ++i) {
+            if (u.split) {
+                // Both tile slots use Q tile 0; KV tile i goes to slot i % 2.
+                // Issue order QK(i), PV(i-1) keeps one slot's softmax running
+                // while the other slot's MMAs execute.
+                for (int i = 0; ok && i <= total; ++i) {
+                    if (i < total) {
+                        const int t = i & 1;
+                        const uint32_t tS = tmem_base + t * 256;
+                        const int itk = 2 * i;
+                        const int sk = itk % C::kStages;
+                        ok = mbar_wait(&kv_full[sk], (itk / C::kStages) & 1, abort_flag, status, 0x05000000u | itk);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t b_base = kv_addr + sk * C::kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            mma_ss(tS, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(b_base + off, 16, 1024),
+                                   idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&s_full[t]);
+                        mma_commit(&kv_empty[sk]);
+                    }
+                    if (i > 0) {
+                        const int i2 = i - 1;
+                        const int t2 = i2 & 1;
+                        const int j2 = i2 >> 1;
+                        const uint32_t tS2 = tmem_base + t2 * 256;
+                        const uint32_t tO2 = tS2 + 128;
+                        const int itv = 2 * i2 + 1;
+                        const int sv = itv % C::kStages;
+                        ok = mbar_wait(&kv_full[sv], (itv / C::kStages) & 1, abort_flag, status, 0x03000000u | itv);
+                        if (!ok) break;
+                        ok = mbar_wait(&p_full[t2], j2 & 1, abort_flag, status, 0x04000000u | i2);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t v_base = kv_addr + sv * C::kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kTileN / 16; ++kk) {
+                            const uint64_t bdesc = smem_desc_sw128(v_base + kk * 2048, 16384, 1024);
+                            mma_ts(tO2, tS2 + kk * 8, bdesc, idesc_pv, (j2 == 0 && kk == 0) ? 0u : 1u);
+                        }
+                        mma_commit(&o_done[t2]);
+                        mma_commit(&kv_empty[sv]);
+                    }
+                }
+            }
+            for (int i = 0; ok && !u.split && i <= total; ++i) {
                 bool fresh_prev = false;
                 if (i > 0) {
                     const TileInfo tp = tile_info(p, u, w, i - 1);
@@ -400,9 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_use = -INFINITY, l_sum = 0.f;
         bool ok = true;
 
-        // Normalise the O accumulator (after PV of walk tile i_done) and write it as part `part`.
-        auto flush = [&](int i_done, int part) -> bool {
-            if (!mbar_wait(&o_done[t], i_done & 1, abort_flag, status, 0x06000000u | i_done)) return false;
+        // Normalise the O accumulator (after this slot's PV number j_done) and write it as part `part`.
+        auto flush = [&](int j_done, int part) -> bool {
+            if (!mbar_wait(&o_done[t], j_done & 1, abort_flag, status, 0x06000000u | j_done)) return false;
             tc_fence_after();
             const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
             const long long ob = o_row_base + static_cast<long long>(part) * out.o_part;
@@ -420,14 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
 
-        for (int i = 0; i < total; ++i) {
+        // Walk tiles of this slot: all of them, or every other one in split mode.
+        const int i_step = u.split ? 2 : 1;
+        int jj = 0;  // this slot's tile count so far (barrier phase index)
+        for (int i = u.split ? t : 0; i < total; i += i_step, ++jj) {
             const TileInfo ti = tile_info(p, u, w, i);
-            if (p.partials && ti.first && i > 0) {
-                if (!(ok = flush(i - 1, ring_shard_at(w, ti.shard_pos - 1)))) break;
+            if (p.partials && ti.first && jj > 0) {
+                if (!(ok = flush(jj - 1, ring_shard_at(w, ti.shard_pos - 1)))) break;
                 m_use = -INFINITY;
                 l_sum = 0.f;
             }
-            if (!(ok = mbar_wait(&s_full[t], i & 1, abort_flag, status, 0x07000000u | i))) break;
+            if (!(ok = mbar_wait(&s_full[t], jj & 1, abort_flag, status, 0x07000000u | i))) break;
             tc_fence_after();
             uint32_t sr[kTileN];
 #pragma unroll
@@ -449,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < kTileN; c += 2) mraw = fmax3(mraw, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
             const float mx = mraw * p.scale_log2;  // scores in log2 units
-            const bool fresh = (i == 0) || (p.partials && ti.first);
+            const bool fresh = (jj == 0) || (p.partials && ti.first);
             float alpha = 1.f;
             bool resc = false;
             if (fresh) {
@@ -491,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_sum = l_sum * alpha + rs;
             if (__any_sync(0xffffffffu, resc)) {
                 // O of the previous tiles must be complete before it is rescaled
-                if (!(ok = mbar_wait(&o_done[t], (i - 1) & 1, abort_flag, status, 0x08000000u | i))) break;
+                if (!(ok = mbar_wait(&o_done[t], (jj - 1) & 1, abort_flag, status, 0x08000000u | i))) break;
                 tc_fence_after();
                 const float a = resc ? alpha : 1.f;
 #pragma unroll
@@ -508,13 +587,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&p_full[t]);
         }
-        if (ok && total > 0) {
+        if (ok) {
             if (!p.fanout && p.partials) {
                 const TileInfo tl = tile_info(p, u, w, total - 1);
-                ok = flush(total - 1, ring_shard_at(w, tl.shard_pos));
-            } else {
-                ok = flush(total - 1, p.fanout ? u.part : 0);
+                ok = flush(jj - 1, ring_shard_at(w, tl.shard_pos));
+            } else if (jj > 0) {
+                ok = flush(jj - 1, p.fanout ? u.slot[t] : 0);
+            } else if (row_ok && out.lse) {
+                // a split slot that received no KV tile: an empty partial (its O is never read)
+                out.lse[lse_base + static_cast<long long>(u.slot[t]) * out.lse_part] = -INFINITY;
             }
+            if (ok && u.empty_slot >= 0 && row_ok && out.lse)
+                out.lse[lse_base + static_cast<long long>(u.empty_slot) * out.lse_part] = -INFINITY;
         }
         if (ok && !p.fanout && p.partials) {
             // KV shards the causal mask empties for this tile: O = 0, lse = -inf
@@ -617,6 +701,15 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
                       : launch<64>(p, grid, tq, tk, tv, tk, tv, stream);
 }
 
+int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_suffix, int* split_prefix, int* suffix_slot0) {
+    const int rows_per_tile = kTileM / (Hq / Hkv);
+    const int split = (R <= rows_per_tile) ? 1 : 0;
+    const int prefix_slots = n_chunks * (split ? 2 : 1);
+    if (split_prefix) *split_prefix = split;
+    if (suffix_slot0) *suffix_slot0 = prefix_slots;
+    return prefix_slots + (S_suffix > 0 ? 2 : 0);
+}
+
 void fanout_chunking(int R, int S_prefix, int Hq, int Hkv, int n_sm, int* n_chunks, int* chunk_tiles) {
     const int G = Hq / Hkv;
     const int rows_per_tile = kTileM / G;
@@ -666,6 +759,7 @@ cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
     p.suffix_mpairs = p.n_mpairs;  // upper bound: a branch holds at most R rows
     p.offsets = a.offsets;
     p.n_prefix_units = (a.S_prefix > 0) ? a.Hkv * p.n_mpairs * a.n_chunks : 0;
+    fanout_slots(a.R, a.Hq, a.Hkv, a.S_prefix > 0 ? a.n_chunks : 0, a.S_suffix, &p.split_prefix, &p.suffix_slot0);
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
     p.out = a.part;
     const unsigned long long D = a.D, esz = 2;

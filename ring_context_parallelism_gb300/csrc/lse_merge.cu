@@ -10,9 +10,12 @@
 // section 2, applied to whole shards.  An empty partial (lse = -inf) gets
 // weight 0 and its O is not read.
 //
-// One warp per (b, s, h) row; lane l owns D/32 consecutive head dims, so a
-// warp reads each partial row as one contiguous 128- to 512-byte segment.
-// fp32 arithmetic.  Bandwidth-bound: each partial row is read once.
+// Lane l owns D/32 consecutive head dims, so a warp reads each partial row as
+// one contiguous 128- to 512-byte segment.  fp32 arithmetic.  Bandwidth-bound:
+// each non-empty partial row is read once.  Three kernels, chosen by shape: a
+// tiled one for many rows and up to 256 partials (coalesced lse reads, weights
+// in shared memory), a block-per-row one for few rows with many partials, and
+// a warp-per-row one otherwise.
 #include <cmath>
 
 #include "ra_device.cuh"
@@ -146,8 +149,220 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const void* __re
     if (out_lse && lane == 0) out_lse[lse_idx] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
 }
 
+// Tiled variant (P <= kMaxTiledP): a block owns 32 consecutive positions s of
+// one (b, h).  Phase 1: lane l of every warp reads lse of position s0 + l for
+// a subset of the partials -- consecutive lanes, consecutive addresses -- and
+// the block forms the max, the weights and their sum in shared memory.
+// Phase 2: each warp merges four of the 32 rows, streaming each non-empty
+// partial row (D contiguous elements) with eight loads in flight.
+constexpr int kMaxTiledP = 256;
+
+template <int D, bool PART_F32, bool OUT_F32>
+__global__ void __launch_bounds__(kWarps * 32) lse_merge_tiled_kernel(const void* __restrict__ part_O,
+                                                                      const float* __restrict__ part_lse,
+                                                                      void* __restrict__ out,
+                                                                      float* __restrict__ out_lse, int P, int S,
+                                                                      int H, long long rows) {
+    constexpr int E = D / 32;
+    extern __shared__ float wts[];             // [P][32] weights
+    __shared__ float red[kWarps][32];
+    __shared__ float Ms[32], inv_sum[32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_stiles = (S + 31) / 32;
+    const long long bh = blockIdx.x / n_stiles;  // b*H + h
+    const int s0 = (blockIdx.x % n_stiles) * 32;
+    const int h = static_cast<int>(bh % H);
+    const long long b = bh / H;
+    const long long l_stride = rows;
+    const long long lse_row = bh * S + s0;       // + lane
+    const bool in_range = s0 + lane < S;
+
+    float mloc = -INFINITY;
+    for (int pp = warp; pp < P; pp += kWarps) {
+        const float L = in_range ? part_lse[pp * l_stride + lse_row + lane] : -INFINITY;
+        wts[pp * 32 + lane] = L;
+        mloc = fmaxf(mloc, L);
+    }
+    red[warp][lane] = mloc;
+    __syncthreads();
+    if (warp == 0) {
+        float M = red[0][lane];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red[w][lane]);
+        Ms[lane] = M;
+    }
+    __syncthreads();
+    const float M = Ms[lane];
+    float ssum = 0.f;
+    for (int pp = warp; pp < P; pp += kWarps) {
+        const float L = wts[pp * 32 + lane];
+        const float wgt = (L == -INFINITY) ? 0.f : expf(L - M);   // empty partial: weight 0
+        wts[pp * 32 + lane] = wgt;
+        ssum += wgt;
+    }
+    red[warp][lane] = ssum;
+    __syncthreads();
+    if (warp == 0) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) t += red[w][lane];
+        inv_sum[lane] = t > 0.f ? 1.f / t : 0.f;
+        if (out_lse && in_range) out_lse[lse_row + lane] = t > 0.f ? M + logf(t) : -INFINITY;
+    }
+    __syncthreads();
+
+    const size_t esz = PART_F32 ? 4 : 2;
+    const long long o_stride = rows * D;
+    for (int r = warp; r < 32; r += kWarps) {
+        const int s = s0 + r;
+        if (s >= S) break;
+        const long long rid = (b * S + s) * H + h;
+        const char* base = static_cast<const char*>(part_O) + (rid * D + lane * E) * esz;
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+        for (int p0 = 0; p0 < P; p0 += 8) {
+            float w[8];
+            float x[8][E];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                w[j] = (p0 + j < P) ? wts[(p0 + j) * 32 + r] : 0.f;
+                if (w[j] != 0.f) {
+                    Vec<E, PART_F32>::load(base + static_cast<long long>(p0 + j) * o_stride * esz, x[j]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) x[j][e] = 0.f;   // O of an empty partial is not read
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = fmaf(w[j], x[j][e], acc[e]);
+        }
+        const float inv = inv_sum[r];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] *= inv;
+        Vec<E, OUT_F32>::store(static_cast<char*>(out) + (rid * D + lane * E) * (OUT_F32 ? 4 : 2), acc);
+    }
+}
+
+// Split-partials variant, for few rows with many partials (the fan-out join):
+// one block per row; warp w accumulates partials w, w + 8, ... and the eight
+// warps' sums are combined in shared memory, so all of a row's partial loads
+// are in flight at once.
+template <int D, bool PART_F32, bool OUT_F32>
+__global__ void __launch_bounds__(kWarps * 32) lse_merge_splitp_kernel(const void* __restrict__ part_O,
+                                                                       const float* __restrict__ part_lse,
+                                                                       void* __restrict__ out,
+                                                                       float* __restrict__ out_lse, int P, int S,
+                                                                       int H, long long rows) {
+    constexpr int E = D / 32;
+    __shared__ float part[kWarps][D];
+    const long long rid = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = static_cast<int>(rid % H);
+    const long long bs = rid / H;
+    const int s = static_cast<int>(bs % S);
+    const long long b = bs / S;
+    const long long lse_idx = (b * H + h) * S + s;
+    const long long l_stride = rows;
+    const long long o_stride = rows * D;
+
+    float M = -INFINITY;
+    for (int g = 0; g < P; g += 32) {
+        const int pp = g + lane;
+        M = fmaxf(M, pp < P ? part_lse[pp * l_stride + lse_idx] : -INFINITY);
+    }
+#pragma unroll
+    for (int x = 16; x; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    const size_t esz = PART_F32 ? 4 : 2;
+    const char* base = static_cast<const char*>(part_O) + (rid * D + lane * E) * esz;
+    if (M != -INFINITY) {
+        for (int g = 0; g < P; g += 32) {
+            const int pp = g + lane;
+            const float L = pp < P ? part_lse[pp * l_stride + lse_idx] : -INFINITY;
+            const float myw = (L == -INFINITY) ? 0.f : expf(L - M);   // empty partial: weight 0
+            float ws = myw;
+#pragma unroll
+            for (int x = 16; x; x >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, x);
+            wsum += ws;
+            // this warp's partials in the group: g + warp, g + warp + 8, g + warp + 16, g + warp + 24
+            float w[4];
+            float x[4][E];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int q = warp + j * kWarps;
+                w[j] = __shfl_sync(0xffffffffu, myw, q);
+                if (w[j] != 0.f) {
+                    Vec<E, PART_F32>::load(base + static_cast<long long>(g + q) * o_stride * esz, x[j]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) x[j][e] = 0.f;   // O of an empty partial is not read
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = fmaf(w[j], x[j][e], acc[e]);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) part[warp][lane * E + e] = acc[e];
+    __syncthreads();
+    if (warp == 0) {
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        float o[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            float t = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < kWarps; ++w2) t += part[w2][lane * E + e];
+            o[e] = t * inv;
+        }
+        Vec<E, OUT_F32>::store(static_cast<char*>(out) + (rid * D + lane * E) * (OUT_F32 ? 4 : 2), o);
+        if (out_lse && lane == 0) out_lse[lse_idx] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+    }
+}
+
+int sm_count_cached() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            n = v;
+        else
+            n = 148;
+    }
+    return n;
+}
+
 template <int D, bool PF, bool OF>
 cudaError_t run(const MergeArgs& a, long long rows, cudaStream_t stream) {
+    const long long tiled_blocks = static_cast<long long>(a.B) * a.H * ((a.S + 31) / 32);
+    const long long n_sm = sm_count_cached();
+    if (a.P <= kMaxTiledP && tiled_blocks >= 4 * n_sm) {
+        const long long blocks = tiled_blocks;
+        const size_t smem = static_cast<size_t>(a.P) * 32 * sizeof(float);
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(lse_merge_tiled_kernel<D, PF, OF>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+        }
+        lse_merge_tiled_kernel<D, PF, OF><<<static_cast<unsigned>(blocks), kWarps * 32, smem, stream>>>(
+            a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows);
+        return cudaGetLastError();
+    }
+    if (a.P >= 8 && rows <= 64 * n_sm * kWarps) {
+        lse_merge_splitp_kernel<D, PF, OF><<<static_cast<unsigned>(rows), kWarps * 32, 0, stream>>>(
+            a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows);
+        return cudaGetLastError();
+    }
     const long long blocks = (rows + kWarps - 1) / kWarps;
     lse_merge_kernel<D, PF, OF><<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(
         a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows);

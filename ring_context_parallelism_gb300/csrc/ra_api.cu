@@ -107,7 +107,7 @@ FanoutPlan plan_fanout(int R, int S_prefix, int S_suffix, int Hq, int Hkv, int D
     FanoutPlan f{};
     ra::fanout_chunking(R, S_prefix, Hq, Hkv, sm_count(), &f.n_chunks, &f.chunk_tiles);
     if (S_prefix == 0) f.n_chunks = 0;
-    f.P = f.n_chunks + (S_suffix > 0 ? 1 : 0);
+    f.P = ra::fanout_slots(R, Hq, Hkv, f.n_chunks, S_suffix, nullptr, nullptr);
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     f.part_o_bytes = up(static_cast<size_t>(f.P) * R * Hq * D * sizeof(float));
     f.part_lse_bytes = up(static_cast<size_t>(f.P) * Hq * R * sizeof(float));
@@ -177,7 +177,7 @@ FanoutPlan plan_fanout_bounded(int R, int S_prefix, int S_suffix, int Hq, int Hk
         FanoutPlan g{};
         g.chunk_tiles = (n_tiles + c - 1) / c;
         g.n_chunks = (n_tiles + g.chunk_tiles - 1) / g.chunk_tiles;
-        g.P = g.n_chunks + (S_suffix > 0 ? 1 : 0);
+        g.P = ra::fanout_slots(R, Hq, Hkv, g.n_chunks, S_suffix, nullptr, nullptr);
         g.part_o_bytes = up(static_cast<size_t>(g.P) * R * Hq * D * sizeof(float));
         g.part_lse_bytes = up(static_cast<size_t>(g.P) * Hq * R * sizeof(float));
         g.total = g.part_o_bytes + g.part_lse_bytes;

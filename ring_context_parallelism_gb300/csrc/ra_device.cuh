@@ -82,6 +82,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Bounded wait that ignores the abort flag and records nothing: used on the
+// way out of an aborted CTA to let asynchronous copies already issued land.
+__device__ __forceinline__ void mbar_wait_landing(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(a, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return;
+}
+
 // ---------------------------------------------------------------------------
 // TMA (bulk tensor copies, global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------

@@ -43,6 +43,11 @@ struct FanoutTcArgs {
 };
 cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream);
 
+// Partial slots of a fan-out call: prefix chunks take two slots each when the
+// stacked rows fit one row tile (the two softmax slots split the chunk's KV
+// tiles), else one; the suffix takes two.  Returns the slot count P.
+int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_suffix, int* split_prefix, int* suffix_slot0);
+
 // Prefix chunking chosen for a fan-out call (shared by the workspace query).
 void fanout_chunking(int R, int S_prefix, int Hq, int Hkv, int n_sm, int* n_chunks, int* chunk_tiles);
 

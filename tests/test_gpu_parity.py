@@ -186,6 +186,34 @@ def test_lse_merge_kernel(dt, D):
     assert torch.all(mO[0, 0, 0] == 0) and mL[0, 0, 0].item() == -float("inf")
 
 
+@pytest.mark.parametrize("P,B,S,H,D", [(40, 1, 16, 64, 128), (9, 1, 3, 4, 64), (33, 2, 7, 3, 128)])
+def test_lse_merge_few_rows_many_partials(P, B, S, H, D):
+    """The fan-out join shape: few rows, many partials (block-per-row merge)."""
+    g = torch.Generator().manual_seed(P + S)
+    pO = torch.randn(P, B, S, H, D, generator=g)
+    pL = torch.randn(P, B, H, S, generator=g) * 3
+    pL[1::4] = -float("inf")
+    mO, mL = ra.lse_merge(pO.cuda(), pL.cuda())
+    ra.device_status()
+    rO, rL = oracle.lse_merge(pO.double().numpy(), pL.double().numpy())
+    _close(mO.cpu().double().numpy(), rO, 1e-5, "merged O")
+    _close(mL.cpu().double().numpy(), rL, 1e-5, "merged lse")
+
+
+def test_lse_merge_many_partials():
+    """More partials than the tiled merge kernel holds in shared memory."""
+    P, B, S, H, D = 300, 1, 5, 2, 64
+    g = torch.Generator().manual_seed(17)
+    pO = torch.randn(P, B, S, H, D, generator=g)
+    pL = torch.randn(P, B, H, S, generator=g)
+    pL[::3] = -float("inf")
+    mO, mL = ra.lse_merge(pO.cuda(), pL.cuda())
+    ra.device_status()
+    rO, rL = oracle.lse_merge(pO.double().numpy(), pL.double().numpy())
+    _close(mO.cpu().double().numpy(), rO, 1e-5, "merged O")
+    _close(mL.cpu().double().numpy(), rL, 1e-5, "merged lse")
+
+
 # ------------------------------------------------------------------------------------------
 # shared-prefix fan-out
 # ------------------------------------------------------------------------------------------
