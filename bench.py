@@ -415,6 +415,47 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+PROFILE_CASES = ("prefill_16k", "fanout_decode", "fanout_decode1", "merge_16k")
+
+
+def run_profile_case(case):
+    """Three calls of one kernel family on a case sized for an ncu capture
+    (inputs larger than L2, a few GB on the device at most)."""
+    import torch
+
+    import ring_context_parallelism_gb300 as ra
+    from ring_context_parallelism_gb300.build import build
+    from ring_context_parallelism_gb300.inputs import WORKLOADS, attention_inputs, fanout_inputs, small
+
+    build()
+    ra.load()
+    if case == "prefill_16k":
+        w = small(WORKLOADS[HEADLINE], S=16384)
+        q, k, v = attention_inputs(w, "cuda")
+        o = torch.empty_like(q)
+        l = torch.empty(w.B, w.Hq, w.S, device="cuda")
+        for _ in range(3):
+            ra.attn(q, k, v, w.n_shards, w.block, True, out=o, lse=l)
+    elif case in ("fanout_decode", "fanout_decode1"):
+        w = WORKLOADS[case]
+        x = fanout_inputs(w, "cuda")
+        ws = torch.empty(ra.fanout_workspace_size(x["R"], w.n_branches, w.S_prefix, w.S_suffix, w.Hq, w.Hkv, w.D),
+                         dtype=torch.uint8, device="cuda")
+        for _ in range(3):
+            ra.fanout(x["q_rows"], x["offsets"], x["k_prefix"], x["v_prefix"], x["k_suffix"], x["v_suffix"],
+                      workspace=ws)
+    elif case == "merge_16k":
+        # per-shard partials of a 16384-token, 64-head causal layer (16 shards), then 3 merges
+        w = small(WORKLOADS["llama70b_layer_128k_partials"], S=16384)
+        q, k, v = attention_inputs(w, "cuda")
+        pO, pL = ra.ring_partials(q, k, v, w.n_shards, w.block, True)
+        for _ in range(3):
+            ra.lse_merge(pO, pL)
+    torch.cuda.synchronize()
+    ra.device_status()
+    print(json.dumps({"profile_case": case, "ok": True}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,7 +464,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--all", action="store_true", help="also time the million-token stress workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
+                    help="run three calls of one kernel family on a small case (for ncu captures) and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
