@@ -73,6 +73,23 @@ def merge_bytes(P, B, S, H, D, esz=2, causal=False):
     return nonempty_rows * D * esz + P * B * S * H * 4 + B * S * H * (D * esz + 4)
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's value (timing only: replicas exchange no data)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step: float, steps: int, total_ms: float, world: int) -> float:
+    """Whole-job rate: the units all ranks processed over the slowest rank's time (x 1e-12, per s)."""
+    return world * units_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
 def peaks():
     p = dict(FALLBACK_PEAKS)
     src = "fallback"
@@ -225,13 +242,9 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         ms = timed_steps(step, args.steps, 0, flush)
         ra.device_status()
-        total_ms = sum(ms)
-        if world > 1:
-            t = torch.tensor([total_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            total_ms = float(t.item())
+        total_ms = max_over_ranks(sum(ms), world, "cuda")
         ms_step = total_ms / args.steps
-        value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+        value = job_throughput(flops, args.steps, total_ms, world)
 
         # e2e through the public API with host buffers
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
