@@ -186,23 +186,35 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
     return u;
 }
 
-// KV tile i of the unit's walk: first key, and flags for shard boundaries.
-struct TileInfo {
-    int kb, shard_pos;
-    bool first, last;
-};
+// Walk of the unit's KV tiles: ring order (prefill) or one linear range (fan-out).
+__device__ __forceinline__ void walk_start(RingIter& it, const TcParams& p, const Unit& u, const RingWalk& w,
+                                           int total) {
+    if (!p.fanout)
+        it.start(w);
+    else
+        it.start_linear(u.kv_lo, total, kTileN);
+}
 
-__device__ __forceinline__ TileInfo tile_info(const TcParams& p, const Unit& u, const RingWalk& w, int i) {
-    TileInfo ti;
-    if (!p.fanout) {
-        ti.kb = ring_tile(w, i, &ti.shard_pos, &ti.first, &ti.last);
-    } else {
-        ti.kb = u.kv_lo + i * kTileN;
-        ti.shard_pos = 0;
-        ti.first = (i == 0);
-        ti.last = false;
+// S = Q K^T for one 128x128 tile: D/16 MMAs, both operands K-major in smem.
+// q_lo / k_lo: low descriptor words of the tiles (LBO field 16 B).
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_lo, uint32_t k_lo) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, false, false);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * (32 >> 4);
+        mma_ss(tS, sw128_desc(q_lo + off), sw128_desc(k_lo + off), idesc, kk > 0 ? 1u : 0u);
     }
-    return ti;
+}
+
+// O (+)= P~ V: 8 MMAs of 16 keys, P~ from TMEM (packed bf16 over S), V MN-major
+// in smem (v_lo: low descriptor word with LBO = 16 KB between 64-column groups).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo, bool accumulate_first) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kTileM, D, false, true);
+#pragma unroll
+    for (int kk = 0; kk < kTileN / 16; ++kk)
+        mma_ts(tO, tP + kk * 8, sw128_desc(v_lo + kk * (2048 >> 4)), idesc, (kk > 0 || accumulate_first) ? 1u : 0u);
 }
 
 template <int D>
@@ -306,8 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_4d(&tm_q, q_full, q_smem + t * C::kTileBytes + c * 16384, c * 64, u.qc1[t], u.qc2[t],
                                 u.qc3[t]);
             int issued = 0;
-            for (int i = 0; i < total; ++i) {
-                const TileInfo ti = tile_info(p, u, w, i);
+            RingIter wi;
+            walk_start(wi, p, u, w, total);
+            for (int i = 0; i < total; ++i, wi.next()) {
                 bool ok = true;
                 for (int kv = 0; kv < 2 && ok; ++kv) {
                     const int it = 2 * i + kv;
@@ -318,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&kv_full[s], C::kTileBytes);
                     uint8_t* dst = kv_smem + s * C::kTileBytes;
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_4d(kv ? vm : km, &kv_full[s], dst + c * 16384, c * 64, u.kv_head, ti.kb, u.kv_z);
+                        tma_load_4d(kv ? vm : km, &kv_full[s], dst + c * 16384, c * 64, u.kv_head, wi.kb, u.kv_z);
                     ++issued;
                 }
                 if (!ok) break;
@@ -334,10 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, false, true);
             const uint32_t q_addr = smem_u32(q_smem);
             const uint32_t kv_addr = smem_u32(kv_smem);
+            // low descriptor words: Q tiles and KV stages (K with LBO 16 B, V with LBO 16 KB)
+            const uint32_t q_lo0 = sw128_desc_lo(q_addr, 16);
+            const uint32_t k_lo0 = sw128_desc_lo(kv_addr, 16);
+            const uint32_t v_lo0 = sw128_desc_lo(kv_addr, 16384);
+            constexpr uint32_t kStageLo = C::kTileBytes >> 4;
             bool ok = mbar_wait(q_full, 0, abort_flag, status, 0x02000000u);
             tc_fence_after();
             if (u.split) {
@@ -347,19 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; ok && i <= total; ++i) {
                     if (i < total) {
                         const int t = i & 1;
-                        const uint32_t tS = tmem_base + t * 256;
                         const int itk = 2 * i;
                         const int sk = itk % C::kStages;
                         ok = mbar_wait(&kv_full[sk], (itk / C::kStages) & 1, abort_flag, status, 0x05000000u | itk);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t b_base = kv_addr + sk * C::kTileBytes;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_ss(tS, smem_desc_sw128(q_addr + off, 16, 1024), smem_desc_sw128(b_base + off, 16, 1024),
-                                   idesc_qk, kk > 0 ? 1u : 0u);
-                        }
+                        issue_qk<D>(tmem_base + t * 256, q_lo0, k_lo0 + sk * kStageLo);
                         mma_commit(&s_full[t]);
                         mma_commit(&kv_empty[sk]);
                     }
@@ -368,7 +377,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int t2 = i2 & 1;
                         const int j2 = i2 >> 1;
                         const uint32_t tS2 = tmem_base + t2 * 256;
-                        const uint32_t tO2 = tS2 + 128;
                         const int itv = 2 * i2 + 1;
                         const int sv = itv % C::kStages;
                         ok = mbar_wait(&kv_full[sv], (itv / C::kStages) & 1, abort_flag, status, 0x03000000u | itv);
@@ -376,26 +384,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = mbar_wait(&p_full[t2], j2 & 1, abort_flag, status, 0x04000000u | i2);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t v_base = kv_addr + sv * C::kTileBytes;
-#pragma unroll
-                        for (int kk = 0; kk < kTileN / 16; ++kk) {
-                            const uint64_t bdesc = smem_desc_sw128(v_base + kk * 2048, 16384, 1024);
-                            mma_ts(tO2, tS2 + kk * 8, bdesc, idesc_pv, (j2 == 0 && kk == 0) ? 0u : 1u);
-                        }
+                        issue_pv<D>(tS2 + 128, tS2, v_lo0 + sv * kStageLo, j2 > 0);
                         mma_commit(&o_done[t2]);
                         mma_commit(&kv_empty[sv]);
                     }
                 }
             }
+            // Paired tiles: iteration i issues PV_t(i-1) and QK_t(i) for t = 0, 1.
+            RingIter wp;  // at iteration i >= 1: tile i-1 (shard openings restart O in partials mode)
+            walk_start(wp, p, u, w, total);
             for (int i = 0; ok && !u.split && i <= total; ++i) {
-                bool fresh_prev = false;
-                if (i > 0) {
-                    const TileInfo tp = tile_info(p, u, w, i - 1);
-                    fresh_prev = (i - 1 == 0) || (p.partials && tp.first);
-                }
+                const bool fresh_prev = p.partials ? wp.first() : (i == 1);
                 for (int t = 0; t < T && ok; ++t) {
                     const uint32_t tS = tmem_base + t * 256;
-                    const uint32_t tO = tS + 128;
                     if (i > 0) {
                         const int itv = 2 * (i - 1) + 1;
                         const int sv = itv % C::kStages;
@@ -407,12 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = mbar_wait(&p_full[t], (i - 1) & 1, abort_flag, status, 0x04000000u | (i - 1));
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t v_base = kv_addr + sv * C::kTileBytes;
-#pragma unroll
-                        for (int kk = 0; kk < kTileN / 16; ++kk) {
-                            const uint64_t bdesc = smem_desc_sw128(v_base + kk * 2048, 16384, 1024);
-                            mma_ts(tO, tS + kk * 8, bdesc, idesc_pv, (fresh_prev && kk == 0) ? 0u : 1u);
-                        }
+                        issue_pv<D>(tS + 128, tS, v_lo0 + sv * kStageLo, !fresh_prev);
                         mma_commit(&o_done[t]);
                     }
                     if (i < total) {
@@ -424,20 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!ok) break;
                             tc_fence_after();
                         }
-                        const uint32_t a_base = q_addr + t * C::kTileBytes;
-                        const uint32_t b_base = kv_addr + sk * C::kTileBytes;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            mma_ss(tS, smem_desc_sw128(a_base + off, 16, 1024), smem_desc_sw128(b_base + off, 16, 1024),
-                                   idesc_qk, kk > 0 ? 1u : 0u);
-                        }
+                        issue_qk<D>(tS, q_lo0 + t * kStageLo, k_lo0 + sk * kStageLo);
                         mma_commit(&s_full[t]);
                     }
                 }
                 if (!ok) break;
                 if (i > 0) mma_commit(&kv_empty[(2 * (i - 1) + 1) % C::kStages]);
                 if (i < total) mma_commit(&kv_empty[(2 * i) % C::kStages]);
+                if (i > 0) wp.next();
             }
             // all issued MMAs complete before TMEM is released
             mma_commit(drain);
@@ -499,13 +489,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Walk tiles of this slot: all of them, or every other one in split mode.
         const int i_step = u.split ? 2 : 1;
         int jj = 0;  // this slot's tile count so far (barrier phase index)
+        RingIter wi;
+        walk_start(wi, p, u, w, total);
+        if (u.split && t == 1) wi.next();
+        int last_shard = wi.j;
         for (int i = u.split ? t : 0; i < total; i += i_step, ++jj) {
-            const TileInfo ti = tile_info(p, u, w, i);
-            if (p.partials && ti.first && jj > 0) {
-                if (!(ok = flush(jj - 1, ring_shard_at(w, ti.shard_pos - 1)))) break;
+            if (jj > 0) {
+                wi.next();
+                if (u.split) wi.next();
+            }
+            if (p.partials && wi.first() && jj > 0) {
+                // the previous KV shard of the ring is complete: flush it
+                if (!(ok = flush(jj - 1, last_shard))) break;
                 m_use = -INFINITY;
                 l_sum = 0.f;
             }
+            last_shard = wi.j;
+            const int tile_kb = wi.kb;
+            const bool tile_first = wi.first();
             if (!(ok = mbar_wait(&s_full[t], jj & 1, abort_flag, status, 0x07000000u | i))) break;
             tc_fence_after();
             uint32_t sr[kTileN];
@@ -515,9 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // visible columns of this tile: c <= lim (only diagonal and tail tiles mask)
             int lim = kTileN - 1;
             if (!p.fanout) {
-                if (p.causal) lim = min(lim, row - ti.kb);
+                if (p.causal) lim = min(lim, row - tile_kb);
             } else {
-                lim = min(lim, u.kv_hi - 1 - ti.kb);
+                lim = min(lim, u.kv_hi - 1 - tile_kb);
             }
             if (lim < kTileN - 1) {
 #pragma unroll
@@ -528,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < kTileN; c += 2) mraw = fmax3(mraw, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
             const float mx = mraw * p.scale_log2;  // scores in log2 units
-            const bool fresh = (jj == 0) || (p.partials && ti.first);
+            const bool fresh = (jj == 0) || (p.partials && tile_first);
             float alpha = 1.f;
             bool resc = false;
             if (fresh) {
@@ -589,8 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             if (!p.fanout && p.partials) {
-                const TileInfo tl = tile_info(p, u, w, total - 1);
-                ok = flush(jj - 1, ring_shard_at(w, tl.shard_pos));
+                ok = flush(jj - 1, last_shard);
             } else if (jj > 0) {
                 ok = flush(jj - 1, p.fanout ? u.slot[t] : 0);
             } else if (row_ok && out.lse) {

@@ -202,6 +202,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// The same descriptor split in two 32-bit words, for issue loops: the high
+// word (SBO = 1024 B, version, 128-byte swizzle) is constant, the low word is
+// the start address >> 4 with the LBO field; stepping along a tile adds an
+// immediate to the low word.
+constexpr uint32_t kSw128DescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t lo) {
+    return (static_cast<uint64_t>(kSw128DescHi) << 32) | lo;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulation.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
     return (1u << 4)                                  // D: f32

@@ -71,4 +71,52 @@ RA_HD int ring_tile(const RingWalk& w, int i, int* shard_pos, bool* first, bool*
     return ring_shard_at(w, t) * w.shard_len + in * w.tile;
 }
 
+// Incremental form of the same walk, for kernel loops: advancing costs adds
+// and compares only (no division per tile).
+struct RingIter {
+    int n_shards, L, tile, tiles_per_shard;
+    int t;      // ring step of the current shard
+    int j;      // current shard
+    int in;     // tile index within the current shard's visited tiles
+    int count;  // visited tiles of the current shard
+    int kb;     // first key of the current tile
+
+    RA_HD void start(const RingWalk& w) {
+        n_shards = w.n_shards;
+        L = w.shard_len;
+        tile = w.tile;
+        tiles_per_shard = w.tiles_per_shard;
+        t = 0;
+        j = w.k;
+        in = 0;
+        count = w.first_tiles;
+        kb = j * L;
+    }
+    // A single linear range of `count` tiles starting at key kv_lo.
+    RA_HD void start_linear(int kv_lo, int n_tiles, int tile_keys) {
+        n_shards = 1;
+        L = 0;
+        tile = tile_keys;
+        tiles_per_shard = n_tiles;
+        t = 0;
+        j = 0;
+        in = 0;
+        count = n_tiles;
+        kb = kv_lo;
+    }
+    RA_HD bool first() const { return in == 0; }
+    RA_HD bool last() const { return in == count - 1; }
+    RA_HD void next() {
+        ++in;
+        kb += tile;
+        if (in == count && n_shards > 1) {
+            ++t;
+            j = (j == 0) ? n_shards - 1 : j - 1;
+            in = 0;
+            count = tiles_per_shard;
+            kb = j * L;
+        }
+    }
+};
+
 }  // namespace ra
