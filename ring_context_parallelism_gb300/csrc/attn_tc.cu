@@ -57,7 +57,7 @@ struct TcParams {
     int R, G, rows_per_tile, n_mpairs, S_prefix, chunk_tiles, n_chunks, S_suffix, n_branches,
         suffix_mpairs, n_prefix_units;
     int split_prefix;   // prefix units hold one row tile: split their KV tiles over both tile slots
-    int suffix_slot0;   // first partial slot of the suffix (2 slots per suffix unit)
+    int suffix_slot0;   // partial slot of the suffix
     const int* offsets;
     float scale_log2;
     OutDesc out;
@@ -93,7 +93,6 @@ struct Unit {
     int split;             // both tiles share Q tile 0 and take alternate KV tiles
     int n_q;               // Q tiles to load
     int slot[2];           // output partial slot per tile
-    int empty_slot;        // fan-out suffix without split: slot that gets lse = -inf for these rows (-1: none)
 };
 
 __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
@@ -101,7 +100,6 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
     u.valid = 1;
     u.suffix = 0;
     u.split = 0;
-    u.empty_slot = -1;
     const int idx = blockIdx.x;
     if (!p.fanout) {
         const int groups = p.B * p.n_head_groups;
@@ -145,8 +143,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         u.row0[0] = 2 * mp * p.rows_per_tile;
         u.row_hi = p.R;
         u.split = p.split_prefix;
-        u.slot[0] = p.split_prefix ? 2 * chunk : chunk;
-        u.slot[1] = p.split_prefix ? 2 * chunk + 1 : chunk;
+        u.slot[0] = u.slot[1] = chunk;
     } else {
         const int j = idx - p.n_prefix_units;
         mp = j % p.suffix_mpairs;
@@ -170,9 +167,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         u.row0[0] = lo + 2 * mp * p.rows_per_tile;
         u.row_hi = hi;
         u.split = (hi - lo <= p.rows_per_tile) ? 1 : 0;
-        u.slot[0] = p.suffix_slot0;
-        u.slot[1] = p.suffix_slot0 + (u.split ? 1 : 0);
-        if (!u.split) u.empty_slot = p.suffix_slot0 + 1;
+        u.slot[0] = u.slot[1] = p.suffix_slot0;
     }
     u.row0[1] = u.split ? u.row0[0] : u.row0[0] + p.rows_per_tile;
     if (u.row0[0] >= u.row_hi) u.valid = 0;
@@ -588,17 +583,73 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&p_full[t]);
         }
-        if (ok) {
+        if (u.split) {
+            // The two slots hold online-softmax states of disjoint KV tiles of the
+            // same rows.  Slot 1 hands (m, l, O) to slot 0 through shared memory
+            // (the KV stages are idle once every MMA has completed), and slot 0
+            // writes their log-sum-exp combination as the unit's one partial.
+            // Slot 1 always arrives on the named barrier, so slot 0 never blocks.
+            float* xo = reinterpret_cast<float*>(kv_smem);  // [D][128], column-major: conflict-free
+            float* xm = xo + D * 128;
+            float* xl = xm + 128;
+            if (t == 1) {
+                bool have = ok && jj > 0 && mbar_wait(drain, 0, abort_flag, status, 0x09000000u);
+                have = __all_sync(0xffffffffu, have);
+                if (have) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) xo[(c * 32 + j) * 128 + lane_row] = __uint_as_float(r[j]);
+                    }
+                }
+                xm[lane_row] = have ? m_use : -INFINITY;
+                xl[lane_row] = have ? l_sum : 0.f;
+                asm volatile("bar.arrive 1, 256;" ::: "memory");
+            } else {
+                bool have0 = ok && mbar_wait(&o_done[0], (jj - 1) & 1, abort_flag, status, 0x0A000000u | jj);
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                have0 = __all_sync(0xffffffffu, have0);
+                if (have0) {
+                    tc_fence_after();
+                    const float m1 = xm[lane_row], l1 = xl[lane_row];
+                    const float m = fmaxf(m_use, m1);
+                    const float a0 = (m_use == -INFINITY) ? 0.f : ex2_approx(m_use - m);
+                    const float a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - m);
+                    const float L = a0 * l_sum + a1 * l1;
+                    const float inv = L > 0.f ? 1.f / L : 0.f;
+                    const long long ob = o_row_base + static_cast<long long>(u.slot[0]) * out.o_part;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float o1 = (a1 != 0.f) ? xo[(c * 32 + j) * 128 + lane_row] : 0.f;
+                            v[j] = a0 * __uint_as_float(r[j]) + a1 * o1;
+                        }
+                        if (row_ok) store_row<D>(out, ob, c, v, inv);
+                    }
+                    if (row_ok && out.lse)
+                        out.lse[lse_base + static_cast<long long>(u.slot[0]) * out.lse_part] =
+                            L > 0.f ? (m + log2f(L)) * 0.69314718055994531f : -INFINITY;
+                }
+                ok = have0;
+            }
+        } else if (ok) {
             if (!p.fanout && p.partials) {
                 ok = flush(jj - 1, last_shard);
             } else if (jj > 0) {
                 ok = flush(jj - 1, p.fanout ? u.slot[t] : 0);
             } else if (row_ok && out.lse) {
-                // a split slot that received no KV tile: an empty partial (its O is never read)
+                // a unit with no KV tile: an empty partial (its O is never read)
                 out.lse[lse_base + static_cast<long long>(u.slot[t]) * out.lse_part] = -INFINITY;
             }
-            if (ok && u.empty_slot >= 0 && row_ok && out.lse)
-                out.lse[lse_base + static_cast<long long>(u.empty_slot) * out.lse_part] = -INFINITY;
         }
         if (ok && !p.fanout && p.partials) {
             // KV shards the causal mask empties for this tile: O = 0, lse = -inf
@@ -703,11 +754,9 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
 
 int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_suffix, int* split_prefix, int* suffix_slot0) {
     const int rows_per_tile = kTileM / (Hq / Hkv);
-    const int split = (R <= rows_per_tile) ? 1 : 0;
-    const int prefix_slots = n_chunks * (split ? 2 : 1);
-    if (split_prefix) *split_prefix = split;
-    if (suffix_slot0) *suffix_slot0 = prefix_slots;
-    return prefix_slots + (S_suffix > 0 ? 2 : 0);
+    if (split_prefix) *split_prefix = (R <= rows_per_tile) ? 1 : 0;
+    if (suffix_slot0) *suffix_slot0 = n_chunks;
+    return n_chunks + (S_suffix > 0 ? 1 : 0);
 }
 
 void fanout_chunking(int R, int S_prefix, int Hq, int Hkv, int n_sm, int* n_chunks, int* chunk_tiles) {

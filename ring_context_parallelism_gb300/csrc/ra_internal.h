@@ -43,9 +43,10 @@ struct FanoutTcArgs {
 };
 cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream);
 
-// Partial slots of a fan-out call: prefix chunks take two slots each when the
-// stacked rows fit one row tile (the two softmax slots split the chunk's KV
-// tiles), else one; the suffix takes two.  Returns the slot count P.
+// Partial slots of a fan-out call: one per prefix chunk and one for the
+// suffix.  *split_prefix: the stacked rows fit one row tile, so each prefix
+// unit splits its KV tiles over its two softmax slots and combines them
+// before writing.  Returns the slot count P.
 int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_suffix, int* split_prefix, int* suffix_slot0);
 
 // Prefix chunking chosen for a fan-out call (shared by the workspace query).
