@@ -45,6 +45,7 @@ constexpr int kTileN = 128;
 constexpr int kThreads = 384;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kTmemCols = 512;
+constexpr int kMaxChunks = 64;
 
 struct TcParams {
     int fanout;     // 0 ring prefill, 1 fan-out
@@ -54,10 +55,12 @@ struct TcParams {
     // ring
     int B, S, Hq, Hkv, n_shards, n_qtiles, n_head_groups;
     // fan-out
-    int R, G, rows_per_tile, n_mpairs, S_prefix, chunk_tiles, n_chunks, S_suffix, n_branches,
+    int R, G, rows_per_tile, n_mpairs, S_prefix, n_chunks, S_suffix, n_branches,
         suffix_mpairs, n_prefix_units;
     int split_prefix;   // prefix units hold one row tile: split their KV tiles over both tile slots
-    int suffix_slot0;   // partial slot of the suffix
+    int suffix_slot0;   // partial slot of the suffix (suffix units; only without a prefix)
+    int fold;           // suffixes folded into prefix units: branch b into chunk b % n_chunks
+    int chunk_start[kMaxChunks + 1];  // prefix tile where chunk c starts
     const int* offsets;
     float scale_log2;
     OutDesc out;
@@ -67,14 +70,13 @@ template <int D>
 struct Cfg {
     static constexpr int kChunks = D / 64;                   // 128-byte column groups per row
     static constexpr int kTileBytes = kTileM * D * 2;        // one Q/K/V tile
-#ifndef RA_TC_STAGES_D128
-#define RA_TC_STAGES_D128 4
-#endif
-    static constexpr int kStages = D == 128 ? RA_TC_STAGES_D128 : 8;  // up to the 227 KB of shared memory
+    // Q tiles and K / V stages share kDataTiles tile slots: two Q tiles leave
+    // room for 3 K + 2 V stages (D = 128), a split unit's single Q tile for 3 + 3.
+    static constexpr int kDataTiles = D == 128 ? 7 : 10;
+    static constexpr int kMaxKV = D == 128 ? 3 : 4;          // per ring
     static constexpr int kQOff = 0;
-    static constexpr int kKVOff = 2 * kTileBytes;
-    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
-    static constexpr int kNumBars = 1 + 2 * kStages + 7;
+    static constexpr int kBarOff = kDataTiles * kTileBytes;
+    static constexpr int kNumBars = 1 + 4 * kMaxKV + 7;
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 };
@@ -93,15 +95,19 @@ struct Unit {
     int split;             // both tiles share Q tile 0 and take alternate KV tiles
     int n_q;               // Q tiles to load
     int slot[2];           // output partial slot per tile
+    int total;             // fan-out: KV tiles of the walk (prefix range + folded suffixes)
+    int fold_b0;           // fan-out prefix unit: first branch whose suffix is folded in (-1: none)
+    int unit_row_lo, unit_row_hi;  // stacked rows the unit's tiles cover
 };
 
+template <bool FAN>
 __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
     Unit u;
     u.valid = 1;
     u.suffix = 0;
     u.split = 0;
     const int idx = blockIdx.x;
-    if (!p.fanout) {
+    if (!FAN) {
         const int groups = p.B * p.n_head_groups;
         const int qt_rev = idx / groups;
         const int rem = idx % groups;
@@ -138,12 +144,34 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         u.kv_head = rest / p.n_chunks;
 #endif
         u.kv_z = 0;
-        u.kv_lo = chunk * p.chunk_tiles * kTileN;
-        u.kv_hi = min(p.S_prefix, u.kv_lo + p.chunk_tiles * kTileN);
+        u.kv_lo = p.chunk_start[chunk] * kTileN;
+        u.kv_hi = min(p.S_prefix, p.chunk_start[chunk + 1] * kTileN);
         u.row0[0] = 2 * mp * p.rows_per_tile;
         u.row_hi = p.R;
         u.split = p.split_prefix;
         u.slot[0] = u.slot[1] = chunk;
+        u.total = (u.kv_hi - u.kv_lo + kTileN - 1) / kTileN;
+        u.unit_row_lo = u.row0[0];
+        u.unit_row_hi = min(p.R, u.row0[0] + (u.split ? 1 : 2) * p.rows_per_tile);
+        u.fold_b0 = -1;
+        if (p.fold) {
+            // suffixes of branches chunk, chunk + n_chunks, ... whose rows meet this unit's rows
+            const int s_tiles = (p.S_suffix + kTileN - 1) / kTileN;
+            for (int b = chunk; b < p.n_branches; b += p.n_chunks) {
+                const int lo = p.offsets[b], hi = p.offsets[b + 1];
+                if (lo < 0 || hi < lo || hi > p.R) {
+                    if (threadIdx.x == 0) {
+                        atomicCAS(&g_tc_status[0], 0u, kDevInvalidArg);
+                        atomicCAS(&g_tc_status[1], 0u, 0x0F000000u | static_cast<unsigned>(b));
+                    }
+                    continue;
+                }
+                if (hi > lo && lo < u.unit_row_hi && hi > u.unit_row_lo) {
+                    if (u.fold_b0 < 0) u.fold_b0 = b;
+                    u.total += s_tiles;
+                }
+            }
+        }
     } else {
         const int j = idx - p.n_prefix_units;
         mp = j % p.suffix_mpairs;
@@ -168,6 +196,10 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         u.row_hi = hi;
         u.split = (hi - lo <= p.rows_per_tile) ? 1 : 0;
         u.slot[0] = u.slot[1] = p.suffix_slot0;
+        u.total = (p.S_suffix + kTileN - 1) / kTileN;
+        u.fold_b0 = -1;
+        u.unit_row_lo = lo;
+        u.unit_row_hi = hi;
     }
     u.row0[1] = u.split ? u.row0[0] : u.row0[0] + p.rows_per_tile;
     if (u.row0[0] >= u.row_hi) u.valid = 0;
@@ -181,14 +213,83 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
     return u;
 }
 
-// Walk of the unit's KV tiles: ring order (prefill) or one linear range (fan-out).
-__device__ __forceinline__ void walk_start(RingIter& it, const TcParams& p, const Unit& u, const RingWalk& w,
-                                           int total) {
-    if (!p.fanout)
-        it.start(w);
-    else
-        it.start_linear(u.kv_lo, total, kTileN);
-}
+// Position in a unit's walk of KV tiles.  Ring prefill: the ring order of
+// ra_walk.h.  Fan-out: the unit's prefix range, then the suffix of every
+// branch folded into it (only that branch's rows see those keys); a suffix
+// unit walks one branch's suffix.
+template <bool FAN>
+struct TileWalk {
+    static constexpr bool fan = FAN;
+    RingIter ring;
+    int seg;              // fan-out: 0 prefix, 1 suffix
+    int b;                // fan-out suffix segment: branch
+    int kb, key_end;      // first key of the tile, end of the segment's keys
+    int tin, tcount;      // tile within the segment, tiles in it
+    int row_lo, row_hi;   // stacked rows that see the segment
+    int stride;           // next folded branch: b + stride (0: none)
+
+    __device__ __forceinline__ bool seek_branch(const TcParams& p, const Unit& u, int from) {
+        for (int bb = from; stride > 0 && bb < p.n_branches; bb += stride) {
+            const int lo = p.offsets[bb], hi = p.offsets[bb + 1];
+            if (lo < 0 || hi < lo || hi > p.R) continue;
+            if (hi > lo && lo < u.unit_row_hi && hi > u.unit_row_lo) {
+                seg = 1;
+                b = bb;
+                kb = 0;
+                key_end = p.S_suffix;
+                tin = 0;
+                tcount = (p.S_suffix + kTileN - 1) / kTileN;
+                row_lo = lo;
+                row_hi = hi;
+                return true;
+            }
+        }
+        return false;
+    }
+    __device__ __forceinline__ void start(const TcParams& p, const Unit& u, const RingWalk& w) {
+        if (!fan) {
+            ring.start(w);
+            return;
+        }
+        if (u.suffix) {  // a suffix unit: one branch's suffix, rows = the unit's branch
+            seg = 1;
+            b = u.kv_z;
+            kb = 0;
+            key_end = p.S_suffix;
+            tin = 0;
+            tcount = (p.S_suffix + kTileN - 1) / kTileN;
+            row_lo = u.unit_row_lo;
+            row_hi = u.unit_row_hi;
+            stride = 0;
+            return;
+        }
+        seg = 0;
+        b = 0;
+        kb = u.kv_lo;
+        key_end = u.kv_hi;
+        tin = 0;
+        tcount = (u.kv_hi - u.kv_lo + kTileN - 1) / kTileN;
+        row_lo = 0;
+        row_hi = p.R;
+        stride = p.fold ? p.n_chunks : 0;
+    }
+    __device__ __forceinline__ void next(const TcParams& p, const Unit& u) {
+        if (!fan) {
+            ring.next();
+            return;
+        }
+        ++tin;
+        kb += kTileN;
+        if (tin == tcount) {
+            if (seg == 0) {
+                if (u.fold_b0 >= 0) seek_branch(p, u, u.fold_b0);
+            } else {
+                seek_branch(p, u, b + stride);
+            }
+        }
+    }
+    __device__ __forceinline__ int key() const { return fan ? kb : ring.kb; }
+};
 
 // S = Q K^T for one 128x128 tile: D/16 MMAs, both operands K-major in smem.
 // q_lo / k_lo: low descriptor words of the tiles (LBO field 16 B).
@@ -232,24 +333,60 @@ __device__ __forceinline__ void store_row(const OutDesc& out, long long o_base, 
     }
 }
 
-template <int D>
+// Stage and phase of a ring of n slots, advanced without division.
+struct StageCtr {
+    int s = 0, ph = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++s == n) {
+            s = 0;
+            ph ^= 1;
+        }
+    }
+};
+
+// Register split per warpgroup (sum = the launch's 384 x 168 = 64512): ring
+// mode 128 x 40 + 2 x 128 x 232; fan-out mode, whose producer also walks the
+// folded suffixes, 128 x 56 + 2 x 128 x 224.
+template <bool FAN>
+__device__ __forceinline__ void reg_dec() {
+    if (FAN)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    else
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
+}
+template <bool FAN>
+__device__ __forceinline__ void reg_inc() {
+    if (FAN)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+    else
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
+}
+
+template <int D, bool FAN>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k2,
                    const __grid_constant__ CUtensorMap tm_v2, const TcParams p) {
     using C = Cfg<D>;
-    const Unit u = decode_unit(p);
+    const Unit u = decode_unit<FAN>(p);
     if (!u.valid) return;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* q_smem = smem + C::kQOff;
-    uint8_t* kv_smem = smem + C::kKVOff;
+    // K and V rings after the Q tiles the unit loads
+    const int nK = C::kMaxKV;
+    const int nV = (u.n_q == 1) ? C::kMaxKV : C::kDataTiles - 2 - C::kMaxKV;
+    uint8_t* kv_smem = smem + C::kQOff + u.n_q * C::kTileBytes;
+    uint8_t* k_smem = kv_smem;
+    uint8_t* v_smem = kv_smem + nK * C::kTileBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* q_full = bars;
-    uint64_t* kv_full = bars + 1;
-    uint64_t* kv_empty = kv_full + C::kStages;
-    uint64_t* s_full = kv_empty + C::kStages;  // [2]
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = k_full + C::kMaxKV;
+    uint64_t* v_full = k_empty + C::kMaxKV;
+    uint64_t* v_empty = v_full + C::kMaxKV;
+    uint64_t* s_full = v_empty + C::kMaxKV;    // [2]
     uint64_t* p_full = s_full + 2;             // [2]
     uint64_t* o_done = p_full + 2;             // [2]
     uint64_t* drain = o_done + 2;
@@ -261,18 +398,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     RingWalk w{};
     int total;
-    if (!p.fanout) {
+    if (!FAN) {
         w = make_ring_walk(p.S, p.n_shards, kTileN, p.causal, u.q_row0, kTileM);
         total = w.total;
     } else {
-        total = (u.kv_hi - u.kv_lo + kTileN - 1) / kTileN;
+        total = u.total;
     }
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+        for (int s = 0; s < C::kMaxKV; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s_full[t], 1);
@@ -294,61 +433,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int T = u.T;
     unsigned* status = g_tc_status;
 
-    // Register split, set inside each role: 128 x 40 (producer / MMA
-    // warpgroup) + 2 x 128 x 232 (softmax warpgroups) = 64512, the 384 x 168
-    // registers of the launch.
+    // Register split, set inside each role (reg_dec / reg_inc).
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
+        reg_dec<FAN>();
         if (lane == 0) {
-            const CUtensorMap* km = u.suffix ? &tm_k2 : &tm_k;
-            const CUtensorMap* vm = u.suffix ? &tm_v2 : &tm_v;
             tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(km);
-            tma_prefetch_desc(vm);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            if (FAN) {
+                tma_prefetch_desc(&tm_k2);
+                tma_prefetch_desc(&tm_v2);
+            }
             mbar_arrive_expect_tx(q_full, u.n_q * C::kTileBytes);
             for (int t = 0; t < u.n_q; ++t)
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_4d(&tm_q, q_full, q_smem + t * C::kTileBytes + c * 16384, c * 64, u.qc1[t], u.qc2[t],
                                 u.qc3[t]);
             int issued = 0;
-            RingIter wi;
-            walk_start(wi, p, u, w, total);
-            for (int i = 0; i < total; ++i, wi.next()) {
-                bool ok = true;
-                for (int kv = 0; kv < 2 && ok; ++kv) {
-                    const int it = 2 * i + kv;
-                    const int s = it % C::kStages;
-                    ok = mbar_wait(&kv_empty[s], ((it / C::kStages) & 1) ^ 1, abort_flag, status,
-                                   0x01000000u | it);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(&kv_full[s], C::kTileBytes);
-                    uint8_t* dst = kv_smem + s * C::kTileBytes;
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_4d(kv ? vm : km, &kv_full[s], dst + c * 16384, c * 64, u.kv_head, wi.kb, u.kv_z);
-                    ++issued;
-                }
+            StageCtr ck, cv;
+            TileWalk<FAN> wi;
+            wi.start(p, u, w);
+            bool ok = true;
+            for (int i = 0; ok && i < total; ++i, wi.next(p, u)) {
+                const bool from_suffix = FAN && wi.seg == 1;
+                const CUtensorMap* kmap = from_suffix ? &tm_k2 : &tm_k;
+                const CUtensorMap* vmap = from_suffix ? &tm_v2 : &tm_v;
+                const int z = FAN ? (from_suffix ? wi.b : 0) : u.kv_z;
+                // K ring, then V ring: K tiles run ahead of the V tiles PV is still reading
+                ok = mbar_wait(&k_empty[ck.s], ck.ph ^ 1, abort_flag, status, 0x01000000u | (2 * i));
                 if (!ok) break;
+                mbar_arrive_expect_tx(&k_full[ck.s], C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(kmap, &k_full[ck.s], k_smem + ck.s * C::kTileBytes + c * 16384, c * 64, u.kv_head,
+                                wi.key(), z);
+                ck.next(nK);
+                ++issued;
+                ok = mbar_wait(&v_empty[cv.s], cv.ph ^ 1, abort_flag, status, 0x01000000u | (2 * i + 1));
+                if (!ok) break;
+                mbar_arrive_expect_tx(&v_full[cv.s], C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(vmap, &v_full[cv.s], v_smem + cv.s * C::kTileBytes + c * 16384, c * 64, u.kv_head,
+                                wi.key(), z);
+                cv.next(nV);
+                ++issued;
             }
             if (*abort_flag) {
-                // let copies already in flight land before the CTA exits
-                for (int it = issued - 1; it >= 0 && it >= issued - C::kStages; --it)
-                    mbar_wait_landing(&kv_full[it % C::kStages], (it / C::kStages) & 1);
+                // let copies already in flight land before the CTA exits: the
+                // last nK K loads and nV V loads issued
+                StageCtr lk, lv;
+                const int nk_issued = (issued + 1) / 2, nv_issued = issued / 2;
+                for (int n = 0; n < nk_issued; ++n) {
+                    if (n >= nk_issued - nK) mbar_wait_landing(&k_full[lk.s], lk.ph);
+                    lk.next(nK);
+                }
+                for (int n = 0; n < nv_issued; ++n) {
+                    if (n >= nv_issued - nV) mbar_wait_landing(&v_full[lv.s], lv.ph);
+                    lv.next(nV);
+                }
                 mbar_wait_landing(q_full, 0);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
+        reg_dec<FAN>();
         if (lane == 0) {
             const uint32_t q_addr = smem_u32(q_smem);
-            const uint32_t kv_addr = smem_u32(kv_smem);
-            // low descriptor words: Q tiles and KV stages (K with LBO 16 B, V with LBO 16 KB)
+            // low descriptor words: Q tiles, K stages (LBO 16 B), V stages (LBO 16 KB)
             const uint32_t q_lo0 = sw128_desc_lo(q_addr, 16);
-            const uint32_t k_lo0 = sw128_desc_lo(kv_addr, 16);
-            const uint32_t v_lo0 = sw128_desc_lo(kv_addr, 16384);
+            const uint32_t k_lo0 = sw128_desc_lo(smem_u32(k_smem), 16);
+            const uint32_t v_lo0 = sw128_desc_lo(smem_u32(v_smem), 16384);
             constexpr uint32_t kStageLo = C::kTileBytes >> 4;
+            StageCtr ck, cv;  // K tile i, V tile i - 1
             bool ok = mbar_wait(q_full, 0, abort_flag, status, 0x02000000u);
             tc_fence_after();
             if (u.split) {
@@ -358,81 +515,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; ok && i <= total; ++i) {
                     if (i < total) {
                         const int t = i & 1;
-                        const int itk = 2 * i;
-                        const int sk = itk % C::kStages;
-                        ok = mbar_wait(&kv_full[sk], (itk / C::kStages) & 1, abort_flag, status, 0x05000000u | itk);
+                        ok = mbar_wait(&k_full[ck.s], ck.ph, abort_flag, status, 0x05000000u | i);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_qk<D>(tmem_base + t * 256, q_lo0, k_lo0 + sk * kStageLo);
+                        issue_qk<D>(tmem_base + t * 256, q_lo0, k_lo0 + ck.s * kStageLo);
                         mma_commit(&s_full[t]);
-                        mma_commit(&kv_empty[sk]);
+                        mma_commit(&k_empty[ck.s]);
+                        ck.next(nK);
                     }
                     if (i > 0) {
                         const int i2 = i - 1;
                         const int t2 = i2 & 1;
                         const int j2 = i2 >> 1;
                         const uint32_t tS2 = tmem_base + t2 * 256;
-                        const int itv = 2 * i2 + 1;
-                        const int sv = itv % C::kStages;
-                        ok = mbar_wait(&kv_full[sv], (itv / C::kStages) & 1, abort_flag, status, 0x03000000u | itv);
+                        ok = mbar_wait(&v_full[cv.s], cv.ph, abort_flag, status, 0x03000000u | i2);
                         if (!ok) break;
                         ok = mbar_wait(&p_full[t2], j2 & 1, abort_flag, status, 0x04000000u | i2);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_pv<D>(tS2 + 128, tS2, v_lo0 + sv * kStageLo, j2 > 0);
+                        issue_pv<D>(tS2 + 128, tS2, v_lo0 + cv.s * kStageLo, j2 > 0);
                         mma_commit(&o_done[t2]);
-                        mma_commit(&kv_empty[sv]);
+                        mma_commit(&v_empty[cv.s]);
+                        cv.next(nV);
                     }
                 }
             }
             // Paired tiles: iteration i issues PV_t(i-1) and QK_t(i) for t = 0, 1.
             RingIter wp;  // at iteration i >= 1: tile i-1 (shard openings restart O in partials mode)
-            walk_start(wp, p, u, w, total);
+            if (!FAN) wp.start(w);
             for (int i = 0; ok && !u.split && i <= total; ++i) {
-                const bool fresh_prev = p.partials ? wp.first() : (i == 1);
+                const bool fresh_prev = (p.partials && !FAN) ? wp.first() : (i == 1);
                 for (int t = 0; t < T && ok; ++t) {
                     const uint32_t tS = tmem_base + t * 256;
                     if (i > 0) {
-                        const int itv = 2 * (i - 1) + 1;
-                        const int sv = itv % C::kStages;
                         if (t == 0) {
-                            ok = mbar_wait(&kv_full[sv], (itv / C::kStages) & 1, abort_flag, status,
-                                           0x03000000u | itv);
+                            ok = mbar_wait(&v_full[cv.s], cv.ph, abort_flag, status, 0x03000000u | (i - 1));
                             if (!ok) break;
                         }
                         ok = mbar_wait(&p_full[t], (i - 1) & 1, abort_flag, status, 0x04000000u | (i - 1));
                         if (!ok) break;
                         tc_fence_after();
-                        issue_pv<D>(tS + 128, tS, v_lo0 + sv * kStageLo, !fresh_prev);
+                        issue_pv<D>(tS + 128, tS, v_lo0 + cv.s * kStageLo, !fresh_prev);
                         mma_commit(&o_done[t]);
                     }
                     if (i < total) {
-                        const int itk = 2 * i;
-                        const int sk = itk % C::kStages;
                         if (t == 0) {
-                            ok = mbar_wait(&kv_full[sk], (itk / C::kStages) & 1, abort_flag, status,
-                                           0x05000000u | itk);
+                            ok = mbar_wait(&k_full[ck.s], ck.ph, abort_flag, status, 0x05000000u | i);
                             if (!ok) break;
                             tc_fence_after();
                         }
-                        issue_qk<D>(tS, q_lo0 + t * kStageLo, k_lo0 + sk * kStageLo);
+                        issue_qk<D>(tS, q_lo0 + t * kStageLo, k_lo0 + ck.s * kStageLo);
                         mma_commit(&s_full[t]);
                     }
                 }
                 if (!ok) break;
-                if (i > 0) mma_commit(&kv_empty[(2 * (i - 1) + 1) % C::kStages]);
-                if (i < total) mma_commit(&kv_empty[(2 * i) % C::kStages]);
-                if (i > 0) wp.next();
+                if (i > 0) {
+                    mma_commit(&v_empty[cv.s]);
+                    cv.next(nV);
+                }
+                if (i < total) {
+                    mma_commit(&k_empty[ck.s]);
+                    ck.next(nK);
+                }
+                if (i > 0 && !FAN) wp.next();
             }
             // all issued MMAs complete before TMEM is released
             mma_commit(drain);
             mbar_wait(drain, 0, abort_flag, status, 0);
         }
     } else if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
+        reg_dec<FAN>();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
+        reg_inc<FAN>();
         const int t = (warp - 4) >> 2;
         if (t < T) {
         const int quad = warp & 3;
@@ -444,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this thread's output row
         int row, head;
         bool row_ok;
-        if (!p.fanout) {
+        if (!FAN) {
             row = u.q_row0 + lane_row;
             head = u.head[t];
             row_ok = true;
@@ -484,24 +639,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Walk tiles of this slot: all of them, or every other one in split mode.
         const int i_step = u.split ? 2 : 1;
         int jj = 0;  // this slot's tile count so far (barrier phase index)
-        RingIter wi;
-        walk_start(wi, p, u, w, total);
-        if (u.split && t == 1) wi.next();
-        int last_shard = wi.j;
+        TileWalk<FAN> wi;
+        wi.start(p, u, w);
+        if (u.split && t == 1) wi.next(p, u);
+        int last_shard = FAN ? 0 : wi.ring.j;
         for (int i = u.split ? t : 0; i < total; i += i_step, ++jj) {
             if (jj > 0) {
-                wi.next();
-                if (u.split) wi.next();
+                wi.next(p, u);
+                if (u.split) wi.next(p, u);
             }
-            if (p.partials && wi.first() && jj > 0) {
+            const bool tile_first = !FAN && wi.ring.first();
+            if (p.partials && tile_first && jj > 0) {
                 // the previous KV shard of the ring is complete: flush it
                 if (!(ok = flush(jj - 1, last_shard))) break;
                 m_use = -INFINITY;
                 l_sum = 0.f;
             }
-            last_shard = wi.j;
-            const int tile_kb = wi.kb;
-            const bool tile_first = wi.first();
+            if (!FAN) last_shard = wi.ring.j;
+            const int tile_kb = wi.key();
             if (!(ok = mbar_wait(&s_full[t], jj & 1, abort_flag, status, 0x07000000u | i))) break;
             tc_fence_after();
             uint32_t sr[kTileN];
@@ -510,10 +665,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             // visible columns of this tile: c <= lim (only diagonal and tail tiles mask)
             int lim = kTileN - 1;
-            if (!p.fanout) {
+            if (!FAN) {
                 if (p.causal) lim = min(lim, row - tile_kb);
             } else {
-                lim = min(lim, u.kv_hi - 1 - tile_kb);
+                lim = min(lim, wi.key_end - 1 - tile_kb);
+                if (row < wi.row_lo || row >= wi.row_hi) lim = -1;  // a folded suffix of another branch
             }
             if (lim < kTileN - 1) {
 #pragma unroll
@@ -642,16 +798,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = have0;
             }
         } else if (ok) {
-            if (!p.fanout && p.partials) {
+            if (!FAN && p.partials) {
                 ok = flush(jj - 1, last_shard);
             } else if (jj > 0) {
-                ok = flush(jj - 1, p.fanout ? u.slot[t] : 0);
+                ok = flush(jj - 1, FAN ? u.slot[t] : 0);
             } else if (row_ok && out.lse) {
                 // a unit with no KV tile: an empty partial (its O is never read)
                 out.lse[lse_base + static_cast<long long>(u.slot[t]) * out.lse_part] = -INFINITY;
             }
         }
-        if (ok && !p.fanout && p.partials) {
+        if (ok && !FAN && p.partials) {
             // KV shards the causal mask empties for this tile: O = 0, lse = -inf
             for (int t2 = w.n_visited; t2 < p.n_shards; ++t2) {
                 const int j = ring_shard_at(w, t2);
@@ -668,6 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
+    if (threadIdx.x == 0) grid_launch_dependents();  // outputs written: the merge may start
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
@@ -706,18 +863,18 @@ bool make_map(CUtensorMap* m, const void* base, const unsigned long long dims[4]
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool FAN>
 cudaError_t launch(const TcParams& p, int grid, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                    const CUtensorMap& k2, const CUtensorMap& v2, cudaStream_t stream) {
     const int smem = Cfg<D>::kSmemBytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, FAN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (grid <= 0) return cudaSuccess;
-    attn_tc_kernel<D><<<grid, kThreads, smem, stream>>>(q, k, v, k2, v2, p);
+    attn_tc_kernel<D, FAN><<<grid, kThreads, smem, stream>>>(q, k, v, k2, v2, p);
     return cudaGetLastError();
 }
 
@@ -748,45 +905,75 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
     if (!make_map(&tq, a.q, qd, qs, box) || !make_map(&tk, a.k, kd, ks, box) || !make_map(&tv, a.v, kd, ks, box))
         return cudaErrorInvalidValue;
     const int grid = p.n_qtiles * a.B * p.n_head_groups;
-    return a.D == 128 ? launch<128>(p, grid, tq, tk, tv, tk, tv, stream)
-                      : launch<64>(p, grid, tq, tk, tv, tk, tv, stream);
+    return a.D == 128 ? launch<128, false>(p, grid, tq, tk, tv, tk, tv, stream)
+                      : launch<64, false>(p, grid, tq, tk, tv, tk, tv, stream);
 }
 
-int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_suffix, int* split_prefix, int* suffix_slot0) {
+int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_prefix, int S_suffix, int* split_prefix,
+                 int* suffix_slot0) {
     const int rows_per_tile = kTileM / (Hq / Hkv);
     if (split_prefix) *split_prefix = (R <= rows_per_tile) ? 1 : 0;
-    if (suffix_slot0) *suffix_slot0 = n_chunks;
-    return n_chunks + (S_suffix > 0 ? 1 : 0);
+    if (suffix_slot0) *suffix_slot0 = 0;
+    // with a prefix the suffixes are folded into prefix units; without one,
+    // suffix units write slot 0
+    return S_prefix > 0 ? n_chunks : (S_suffix > 0 ? 1 : 0);
 }
 
-void fanout_chunking(int R, int S_prefix, int Hq, int Hkv, int n_sm, int* n_chunks, int* chunk_tiles) {
+void fanout_split(int n_chunks, int S_prefix, int S_suffix, int n_branches, int n_mpairs, int* chunk_start) {
+    // Prefix tiles per chunk such that prefix + folded suffix work is even: the
+    // chunk of branch b is b % n_chunks; on average a row pair of a chunk meets
+    // its branches' rows in proportion 1/n_mpairs.
+    const int n_tiles = (S_prefix + kTileN - 1) / kTileN;
+    const double s_tiles = (S_suffix > 0 && S_prefix > 0) ? (S_suffix + kTileN - 1) / kTileN : 0;
+    double want[kMaxChunks];
+    double total = n_tiles + s_tiles * n_branches / n_mpairs;
+    double sum = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+        const int nbr = n_branches / n_chunks + (c < n_branches % n_chunks ? 1 : 0);
+        want[c] = total / n_chunks - s_tiles * nbr / n_mpairs;
+        if (want[c] < 1) want[c] = 1;
+        sum += want[c];
+    }
+    // scale to the prefix tile count, cumulative rounding, at least one tile each
+    int prev = 0;
+    double acc = 0;
+    chunk_start[0] = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+        acc += want[c] * n_tiles / sum;
+        int e = static_cast<int>(acc + 0.5);
+        if (e < prev + 1) e = prev + 1;
+        if (e > n_tiles - (n_chunks - 1 - c)) e = n_tiles - (n_chunks - 1 - c);
+        chunk_start[c + 1] = e;
+        prev = e;
+    }
+    chunk_start[n_chunks] = n_tiles;
+}
+
+void fanout_chunking(int R, int S_prefix, int S_suffix, int n_branches, int Hq, int Hkv, int n_sm, int* n_chunks) {
     const int G = Hq / Hkv;
     const int rows_per_tile = kTileM / G;
     const int n_mpairs = (R + 2 * rows_per_tile - 1) / (2 * rows_per_tile);
     const int n_tiles = (S_prefix + kTileN - 1) / kTileN;
     if (n_tiles == 0 || n_mpairs == 0) {
         *n_chunks = 0;
-        *chunk_tiles = 1;
         return;
     }
-    // Choose the split that minimises (waves x tiles per chunk) on n_sm SMs,
-    // preferring fewer chunks (fewer partials) on ties.
-    long long best = -1;
+    const double s_tiles = S_suffix > 0 ? (S_suffix + kTileN - 1) / kTileN : 0;
+    const double work = n_tiles + s_tiles * n_branches / n_mpairs;  // tiles per (KV head, row pair)
+    // Minimise (waves x tiles per unit) on n_sm SMs; ties: fewer chunks (fewer partials).
+    double best = -1;
     int best_c = 1;
-    const int max_c = n_tiles < 64 ? n_tiles : 64;
+    const int max_c = n_tiles < kMaxChunks ? n_tiles : kMaxChunks;
     for (int c = 1; c <= max_c; ++c) {
-        const int ct = (n_tiles + c - 1) / c;
-        const int cc = (n_tiles + ct - 1) / ct;
-        const long long units = static_cast<long long>(Hkv) * n_mpairs * cc;
+        const long long units = static_cast<long long>(Hkv) * n_mpairs * c;
         const long long waves = (units + n_sm - 1) / n_sm;
-        const long long cost = waves * ct * 1000 + cc;  // tie-break: fewer chunks
+        const double cost = waves * (work / c + 2.0) + 1e-3 * c;  // + per-unit fixed cost
         if (best < 0 || cost < best) {
             best = cost;
-            best_c = cc;
+            best_c = c;
         }
     }
-    *chunk_tiles = (n_tiles + best_c - 1) / best_c;
-    *n_chunks = (n_tiles + *chunk_tiles - 1) / *chunk_tiles;
+    *n_chunks = best_c;
 }
 
 cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
@@ -801,14 +988,16 @@ cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
     p.rows_per_tile = kTileM / p.G;
     p.n_mpairs = (a.R + 2 * p.rows_per_tile - 1) / (2 * p.rows_per_tile);
     p.S_prefix = a.S_prefix;
-    p.chunk_tiles = a.chunk_tiles;
     p.n_chunks = a.n_chunks;
+    for (int c = 0; c <= a.n_chunks && c <= kMaxChunks; ++c) p.chunk_start[c] = a.chunk_start[c];
     p.S_suffix = a.S_suffix;
     p.n_branches = a.n_branches;
     p.suffix_mpairs = p.n_mpairs;  // upper bound: a branch holds at most R rows
     p.offsets = a.offsets;
     p.n_prefix_units = (a.S_prefix > 0) ? a.Hkv * p.n_mpairs * a.n_chunks : 0;
-    fanout_slots(a.R, a.Hq, a.Hkv, a.S_prefix > 0 ? a.n_chunks : 0, a.S_suffix, &p.split_prefix, &p.suffix_slot0);
+    fanout_slots(a.R, a.Hq, a.Hkv, a.S_prefix > 0 ? a.n_chunks : 0, a.S_prefix, a.S_suffix, &p.split_prefix,
+                 &p.suffix_slot0);
+    p.fold = (a.S_prefix > 0 && a.S_suffix > 0) ? 1 : 0;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
     p.out = a.part;
     const unsigned long long D = a.D, esz = 2;
@@ -842,10 +1031,10 @@ cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
         tk2 = tk;
         tv2 = tv;
     }
-    const int n_suffix_units = (a.S_suffix > 0) ? a.n_branches * a.Hkv * p.suffix_mpairs : 0;
+    const int n_suffix_units = (a.S_suffix > 0 && !p.fold) ? a.n_branches * a.Hkv * p.suffix_mpairs : 0;
     const int grid = p.n_prefix_units + n_suffix_units;
-    return a.D == 128 ? launch<128>(p, grid, tq, tk, tv, tk2, tv2, stream)
-                      : launch<64>(p, grid, tq, tk, tv, tk2, tv2, stream);
+    return a.D == 128 ? launch<128, true>(p, grid, tq, tk, tv, tk2, tv2, stream)
+                      : launch<64, true>(p, grid, tq, tk, tv, tk2, tv2, stream);
 }
 
 unsigned read_clear_status_tc(unsigned* where) {

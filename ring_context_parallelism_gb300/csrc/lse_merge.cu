@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const void* __re
                                                                 void* __restrict__ out, float* __restrict__ out_lse,
                                                                 int P, int S, int H, long long rows) {
     constexpr int E = D / 32;
+    grid_dependency_wait();
     const long long rid = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
     if (rid >= rows) return;
     const int lane = threadIdx.x & 31;
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_tiled_kernel(const void
     extern __shared__ float wts[];             // [P][32] weights
     __shared__ float red[kWarps][32];
     __shared__ float Ms[32], inv_sum[32];
+    grid_dependency_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_stiles = (S + 31) / 32;
     const long long bh = blockIdx.x / n_stiles;  // b*H + h
@@ -258,6 +260,7 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_splitp_kernel(const voi
                                                                        int H, long long rows) {
     constexpr int E = D / 32;
     __shared__ float part[kWarps][D];
+    grid_dependency_wait();
     const long long rid = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = static_cast<int>(rid % H);
@@ -342,6 +345,26 @@ int sm_count_cached() {
     return n;
 }
 
+// Launch with programmatic stream serialization: the merge may be scheduled
+// while the kernel before it on the stream (the attention kernel producing
+// the partials) is finishing; grid_dependency_wait() in the merge kernels
+// waits for that kernel's completion and memory before any partial is read.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 template <int D, bool PF, bool OF>
 cudaError_t run(const MergeArgs& a, long long rows, cudaStream_t stream) {
     const long long tiled_blocks = static_cast<long long>(a.B) * a.H * ((a.S + 31) / 32);
@@ -354,19 +377,16 @@ cudaError_t run(const MergeArgs& a, long long rows, cudaStream_t stream) {
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
             if (e != cudaSuccess) return e;
         }
-        lse_merge_tiled_kernel<D, PF, OF><<<static_cast<unsigned>(blocks), kWarps * 32, smem, stream>>>(
-            a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows);
-        return cudaGetLastError();
+        return launch_pdl(lse_merge_tiled_kernel<D, PF, OF>, static_cast<unsigned>(blocks), kWarps * 32, smem, stream,
+                          a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows);
     }
     if (a.P >= 8 && rows <= 64 * n_sm * kWarps) {
-        lse_merge_splitp_kernel<D, PF, OF><<<static_cast<unsigned>(rows), kWarps * 32, 0, stream>>>(
-            a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows);
-        return cudaGetLastError();
+        return launch_pdl(lse_merge_splitp_kernel<D, PF, OF>, static_cast<unsigned>(rows), kWarps * 32, 0, stream,
+                          a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows);
     }
     const long long blocks = (rows + kWarps - 1) / kWarps;
-    lse_merge_kernel<D, PF, OF><<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(
-        a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows);
-    return cudaGetLastError();
+    return launch_pdl(lse_merge_kernel<D, PF, OF>, static_cast<unsigned>(blocks), kWarps * 32, 0, stream, a.part_O,
+                      a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows);
 }
 
 }  // namespace

@@ -99,20 +99,33 @@ ra_status ring_common(const void* q, const void* k, const void* v, void* out, fl
 }
 
 struct FanoutPlan {
-    int n_chunks, chunk_tiles, P;
+    int n_chunks, P;
+    int chunk_start[65];
     size_t part_o_bytes, part_lse_bytes, total;
 };
 
-FanoutPlan plan_fanout(int R, int S_prefix, int S_suffix, int Hq, int Hkv, int D) {
+// Sizes of a plan with a given prefix chunk count.
+FanoutPlan plan_with_chunks(int n_chunks, int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv,
+                            int D) {
     FanoutPlan f{};
-    ra::fanout_chunking(R, S_prefix, Hq, Hkv, sm_count(), &f.n_chunks, &f.chunk_tiles);
-    if (S_prefix == 0) f.n_chunks = 0;
-    f.P = ra::fanout_slots(R, Hq, Hkv, f.n_chunks, S_suffix, nullptr, nullptr);
+    f.n_chunks = S_prefix > 0 ? n_chunks : 0;
+    if (f.n_chunks > 0) {
+        const int rows_per_tile = 128 / (Hq / Hkv);
+        const int n_mpairs = (R + 2 * rows_per_tile - 1) / (2 * rows_per_tile);
+        ra::fanout_split(f.n_chunks, S_prefix, S_suffix, n_branches, n_mpairs > 0 ? n_mpairs : 1, f.chunk_start);
+    }
+    f.P = ra::fanout_slots(R, Hq, Hkv, f.n_chunks, S_prefix, S_suffix, nullptr, nullptr);
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     f.part_o_bytes = up(static_cast<size_t>(f.P) * R * Hq * D * sizeof(float));
     f.part_lse_bytes = up(static_cast<size_t>(f.P) * Hq * R * sizeof(float));
     f.total = f.part_o_bytes + f.part_lse_bytes;
     return f;
+}
+
+FanoutPlan plan_fanout(int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv, int D) {
+    int n_chunks = 0;
+    ra::fanout_chunking(R, S_prefix, S_suffix, n_branches, Hq, Hkv, sm_count(), &n_chunks);
+    return plan_with_chunks(n_chunks, R, n_branches, S_prefix, S_suffix, Hq, Hkv, D);
 }
 
 ra_status check_fanout(const void* q_rows, const int* offsets, int n_branches, int R, const void* k_prefix,
@@ -168,19 +181,12 @@ ra_status scratch_address(void** addr) {
 
 // The usual plan if its partials fit in the scratch array, else the largest
 // chunk count that does; total == 0 if none fits.
-FanoutPlan plan_fanout_bounded(int R, int S_prefix, int S_suffix, int Hq, int Hkv, int D, size_t cap) {
-    FanoutPlan f = plan_fanout(R, S_prefix, S_suffix, Hq, Hkv, D);
+FanoutPlan plan_fanout_bounded(int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv, int D,
+                               size_t cap) {
+    FanoutPlan f = plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D);
     if (f.total <= cap) return f;
-    const int n_tiles = (S_prefix + 127) / 128;
-    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     for (int c = f.n_chunks - 1; c >= 1; --c) {
-        FanoutPlan g{};
-        g.chunk_tiles = (n_tiles + c - 1) / c;
-        g.n_chunks = (n_tiles + g.chunk_tiles - 1) / g.chunk_tiles;
-        g.P = ra::fanout_slots(R, Hq, Hkv, g.n_chunks, S_suffix, nullptr, nullptr);
-        g.part_o_bytes = up(static_cast<size_t>(g.P) * R * Hq * D * sizeof(float));
-        g.part_lse_bytes = up(static_cast<size_t>(g.P) * Hq * R * sizeof(float));
-        g.total = g.part_o_bytes + g.part_lse_bytes;
+        FanoutPlan g = plan_with_chunks(c, R, n_branches, S_prefix, S_suffix, Hq, Hkv, D);
         if (g.total <= cap) return g;
     }
     FanoutPlan none{};
@@ -224,7 +230,7 @@ size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int 
     if (R < 0 || n_branches < 1 || S_prefix < 0 || S_suffix < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
         (D != 64 && D != 128) || dt != RA_BF16 || 128 % (Hq / Hkv) || S_prefix + S_suffix < 1)
         return 0;
-    return plan_fanout(R, S_prefix, S_suffix, Hq, Hkv, D).total;
+    return plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D).total;
 }
 
 ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, int n_branches, int R,
@@ -236,7 +242,7 @@ ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, i
     if (st != RA_OK) return st;
     if (lse && !aligned16(lse)) return fail(RA_ERR_INVALID_ARG, "lse must be 16-byte aligned");
     if (R == 0) return ok();
-    const FanoutPlan f = plan_fanout(R, S_prefix, S_suffix, Hq, Hkv, D);
+    const FanoutPlan f = plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D);
     if (!workspace || workspace_bytes < f.total)
         return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", f.total, workspace_bytes);
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
@@ -259,7 +265,7 @@ ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, i
     a.Hkv = Hkv;
     a.D = D;
     a.n_chunks = f.n_chunks;
-    a.chunk_tiles = f.chunk_tiles;
+    for (int c = 0; c <= f.n_chunks; ++c) a.chunk_start[c] = f.chunk_start[c];
     a.part.o = part_o;
     a.part.lse = part_lse;
     a.part.o_row = static_cast<long long>(Hq) * D;
@@ -287,7 +293,7 @@ ra_status ra_prefix_fanout_attn_noalloc(const void* q_rows, const int* branch_of
     if (lse && !aligned16(lse)) return fail(RA_ERR_INVALID_ARG, "lse must be 16-byte aligned");
     if (R == 0) return ok();
     const size_t cap = RA_NOALLOC_SCRATCH_BYTES;
-    const FanoutPlan f = plan_fanout_bounded(R, S_prefix, S_suffix, Hq, Hkv, D, cap);
+    const FanoutPlan f = plan_fanout_bounded(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D, cap);
     if (f.total == 0)
         return fail(RA_ERR_WORKSPACE,
                     "fan-out partials for R=%d, Hq=%d, D=%d do not fit the %zu-byte static scratch; "
@@ -313,7 +319,7 @@ ra_status ra_prefix_fanout_attn_noalloc(const void* q_rows, const int* branch_of
     a.Hkv = Hkv;
     a.D = D;
     a.n_chunks = f.n_chunks;
-    a.chunk_tiles = f.chunk_tiles;
+    for (int c = 0; c <= f.n_chunks; ++c) a.chunk_start[c] = f.chunk_start[c];
     a.part.o = part_o;
     a.part.lse = part_lse;
     a.part.o_row = static_cast<long long>(Hq) * D;

@@ -224,6 +224,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Dependent kernel: wait until the preceding grid on the stream has completed
+// and its memory is visible (no-op for an ordinary launch).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Primary kernel: this CTA's results are written; dependents may be scheduled.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Small math helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -38,19 +38,27 @@ struct FanoutTcArgs {
     const void *k_suffix, *v_suffix;
     int S_suffix;
     int Hq, Hkv, D;
-    int n_chunks, chunk_tiles;  // prefix split
+    int n_chunks;               // prefix split
+    int chunk_start[65];        // prefix tile where chunk c starts (n_chunks + 1 entries)
     OutDesc part;               // fp32 partials [P][R][Hq][D], lse [P][Hq][R]
 };
 cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream);
 
-// Partial slots of a fan-out call: one per prefix chunk and one for the
-// suffix.  *split_prefix: the stacked rows fit one row tile, so each prefix
-// unit splits its KV tiles over its two softmax slots and combines them
-// before writing.  Returns the slot count P.
-int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_suffix, int* split_prefix, int* suffix_slot0);
+// Partial slots of a fan-out call: one per prefix chunk (each branch's suffix
+// is folded into the chunk b % n_chunks), or one for the suffix units when
+// there is no prefix.  *split_prefix: the stacked rows fit one row tile, so
+// each prefix unit splits its KV tiles over its two softmax slots and combines
+// them before writing.  Returns the slot count P.
+int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_prefix, int S_suffix, int* split_prefix,
+                 int* suffix_slot0);
 
-// Prefix chunking chosen for a fan-out call (shared by the workspace query).
-void fanout_chunking(int R, int S_prefix, int Hq, int Hkv, int n_sm, int* n_chunks, int* chunk_tiles);
+// Number of prefix chunks for a fan-out call (shared by the workspace query),
+// at most 64.
+void fanout_chunking(int R, int S_prefix, int S_suffix, int n_branches, int Hq, int Hkv, int n_sm, int* n_chunks);
+
+// Chunk boundaries (n_chunks + 1 tile indices) balancing prefix tiles against
+// the folded suffix tiles.
+void fanout_split(int n_chunks, int S_prefix, int S_suffix, int n_branches, int n_mpairs, int* chunk_start);
 
 // Exact fp32 path (CUDA-core FMA).
 struct RingSimtArgs {
