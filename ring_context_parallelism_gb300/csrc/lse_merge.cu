@@ -74,6 +74,44 @@ struct Vec<2, false> {
     }
 };
 
+// N consecutive elements (N = 4 or 8) as 16-byte vector accesses.
+template <int N, bool F32>
+__device__ __forceinline__ void load_elems(const void* p, float* x) {
+    if (F32) {
+#pragma unroll
+        for (int k = 0; k < N / 4; ++k) {
+            const float4 v = reinterpret_cast<const float4*>(p)[k];
+            x[4 * k] = v.x; x[4 * k + 1] = v.y; x[4 * k + 2] = v.z; x[4 * k + 3] = v.w;
+        }
+    } else if (N == 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[2 * k] = __uint_as_float(w[k] << 16);
+            x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+    } else {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+        x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    }
+}
+
+template <int N, bool F32>
+__device__ __forceinline__ void store_elems(void* p, const float* x) {
+    if (F32) {
+#pragma unroll
+        for (int k = 0; k < N / 4; ++k)
+            reinterpret_cast<float4*>(p)[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+    } else if (N == 8) {
+        *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                                                  pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+    } else {
+        *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+    }
+}
+
 template <int D, bool PART_F32, bool OUT_F32>
 __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const void* __restrict__ part_O,
                                                                 const float* __restrict__ part_lse,
@@ -213,38 +251,45 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_tiled_kernel(const void
     }
     __syncthreads();
 
-    const size_t esz = PART_F32 ? 4 : 2;
-    const long long o_stride = rows * D;
-    for (int r = warp; r < 32; r += kWarps) {
+    // Phase 2: a half-warp per row, lane l of the half owning D/16 consecutive
+    // elements (16-byte loads for bf16); a warp merges two rows at a time.
+    constexpr int E2 = D / 16;
+    constexpr size_t esz = PART_F32 ? 4 : 2;
+    const int half = lane >> 4, hl = lane & 15;
+    const size_t o_step = static_cast<size_t>(rows) * D * esz;  // bytes between partials
+    for (int r = 2 * warp + half; r < 32; r += 2 * kWarps) {
         const int s = s0 + r;
-        if (s >= S) break;
-        const long long rid = (b * S + s) * H + h;
-        const char* base = static_cast<const char*>(part_O) + (rid * D + lane * E) * esz;
-        float acc[E];
+        const bool live = s < S;
+        const long long rid = (b * S + (live ? s : s0)) * H + h;
+        const char* ptr = static_cast<const char*>(part_O) + (rid * D + hl * E2) * esz;
+        float acc[E2];
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+        for (int e = 0; e < E2; ++e) acc[e] = 0.f;
         for (int p0 = 0; p0 < P; p0 += 8) {
             float w[8];
-            float x[8][E];
+            float x[8][E2];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                w[j] = (p0 + j < P) ? wts[(p0 + j) * 32 + r] : 0.f;
+                w[j] = (live && p0 + j < P) ? wts[(p0 + j) * 32 + r] : 0.f;
                 if (w[j] != 0.f) {
-                    Vec<E, PART_F32>::load(base + static_cast<long long>(p0 + j) * o_stride * esz, x[j]);
+                    load_elems<E2, PART_F32>(ptr + j * o_step, x[j]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < E; ++e) x[j][e] = 0.f;   // O of an empty partial is not read
+                    for (int e = 0; e < E2; ++e) x[j][e] = 0.f;   // O of an empty partial is not read
                 }
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j)
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc[e] = fmaf(w[j], x[j][e], acc[e]);
+                for (int e = 0; e < E2; ++e) acc[e] = fmaf(w[j], x[j][e], acc[e]);
+            ptr += 8 * o_step;
         }
-        const float inv = inv_sum[r];
+        if (live) {
+            const float inv = inv_sum[r];
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] *= inv;
-        Vec<E, OUT_F32>::store(static_cast<char*>(out) + (rid * D + lane * E) * (OUT_F32 ? 4 : 2), acc);
+            for (int e = 0; e < E2; ++e) acc[e] *= inv;
+            store_elems<E2, OUT_F32>(static_cast<char*>(out) + (rid * D + hl * E2) * (OUT_F32 ? 4 : 2), acc);
+        }
     }
 }
 

@@ -186,6 +186,25 @@ def test_lse_merge_kernel(dt, D):
     assert torch.all(mO[0, 0, 0] == 0) and mL[0, 0, 0].item() == -float("inf")
 
 
+@pytest.mark.parametrize("dt,D,S", [(torch.bfloat16, 128, 2047), (torch.float32, 64, 2080), (torch.bfloat16, 64, 1056)])
+def test_lse_merge_many_rows(dt, D, S):
+    """Enough rows for the tiled merge kernel (coalesced lse, half-warp rows); S not a multiple of 32."""
+    P, B, H = 9, 1, 64
+    g = torch.Generator().manual_seed(S + D)
+    pO = torch.randn(P, B, S, H, D, generator=g).to(dt)
+    pL = torch.randn(P, B, H, S, generator=g) * 3
+    pL[2] = -float("inf")
+    pL[:, 0, 5, 7] = -float("inf")
+    pO_nan = pO.clone()
+    pO_nan[2] = float("nan")                    # empty partial: must not be read
+    mO, mL = ra.lse_merge(pO_nan.cuda(), pL.cuda())
+    ra.device_status()
+    rO, rL = oracle.lse_merge(pO.double().numpy(), pL.double().numpy())
+    _close(mO.float().cpu().double().numpy(), rO, 1e-5 if dt == torch.float32 else 2e-2, "merged O")
+    _close(mL.cpu().double().numpy(), rL, 1e-5, "merged lse")
+    assert torch.all(mO[0, 7, 5] == 0) and mL[0, 5, 7].item() == -float("inf")
+
+
 @pytest.mark.parametrize("P,B,S,H,D", [(40, 1, 16, 64, 128), (9, 1, 3, 4, 64), (33, 2, 7, 3, 128)])
 def test_lse_merge_few_rows_many_partials(P, B, S, H, D):
     """The fan-out join shape: few rows, many partials (block-per-row merge)."""
