@@ -37,7 +37,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) per launch of the headline kernel from an ncu
 # capture, valid only while the kernel source hashes to the recorded value.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the timed 32768-token configuration
+    # (bench.py --profile-case prefill_32k, third launch): 404034816 read + 238921216 written
+    "87dea903d356aba1": 642956032,
+}
 
 
 # ----------------------------------------------------------------------------------------------
@@ -440,7 +444,7 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-PROFILE_CASES = ("prefill_16k", "fanout_decode", "fanout_decode1", "merge_16k")
+PROFILE_CASES = ("prefill_32k", "prefill_16k", "fanout_decode", "fanout_decode1", "merge_16k")
 
 
 def run_profile_case(case):
@@ -454,8 +458,9 @@ def run_profile_case(case):
 
     build()
     ra.load()
-    if case == "prefill_16k":
-        w = small(WORKLOADS[HEADLINE], S=16384)
+    if case in ("prefill_32k", "prefill_16k"):
+        # prefill_32k is the timed headline configuration itself (0.6 GB on the device, ~7 ms a launch)
+        w = WORKLOADS[HEADLINE] if case == "prefill_32k" else small(WORKLOADS[HEADLINE], S=16384)
         q, k, v = attention_inputs(w, "cuda")
         o = torch.empty_like(q)
         l = torch.empty(w.B, w.Hq, w.S, device="cuda")

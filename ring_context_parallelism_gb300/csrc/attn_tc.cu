@@ -108,12 +108,17 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
     u.split = 0;
     const int idx = blockIdx.x;
     if (!FAN) {
-        const int groups = p.B * p.n_head_groups;
-        const int qt_rev = idx / groups;
-        const int rem = idx % groups;
-        u.b = rem / p.n_head_groups;
-        const int hg = rem % p.n_head_groups;
-        const int qt = p.causal ? p.n_qtiles - 1 - qt_rev : qt_rev;  // heaviest tiles launch first
+        // (batch, KV head) outermost: the CTAs resident at one time share one or
+        // two KV heads, whose K and V stay in L2 while every query tile of the
+        // group walks them.  Within a group the heaviest query tiles launch first.
+        const int hg_per_kv = p.n_head_groups / p.Hkv;
+        const int per_kv = p.n_qtiles * hg_per_kv;
+        const int g = idx / per_kv;
+        const int rem = idx - g * per_kv;
+        const int qt_rev = rem / hg_per_kv;
+        u.b = g / p.Hkv;
+        const int hg = (g - u.b * p.Hkv) * hg_per_kv + (rem - qt_rev * hg_per_kv);
+        const int qt = p.causal ? p.n_qtiles - 1 - qt_rev : qt_rev;
         u.q_row0 = qt * kTileM;
         u.T = p.T2 ? 2 : 1;
         for (int t = 0; t < 2; ++t) {
