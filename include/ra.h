@@ -102,7 +102,9 @@ ra_status ra_ring_partials_fwd(const void* q, const void* k, const void* v, void
  * index is merged across sequence shards, never different rows).  Per
  * (b, s, h):  M = max_p lse_p;  w_p = exp(lse_p - M);  O = sum_p w_p O_p / sum_p w_p;
  * lse = M + ln(sum_p w_p).  A partial with lse_p = -inf has weight 0 and its
- * O_p is not read; if every partial is empty the result is O = 0, lse = -inf.
+ * O_p does not enter the result, whatever it holds (NaN included; the memory
+ * must still lie inside the partials_O buffer); if every partial is empty the
+ * result is O = 0, lse = -inf.
  *
  *   partials_O   [P, B, S, H, D] dtype dt     partials_lse [P, B, H, S] fp32
  *   out          [B, S, H, D]    dtype dt     out_lse      [B, H, S] fp32 (may be NULL)

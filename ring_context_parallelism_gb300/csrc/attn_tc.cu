@@ -440,64 +440,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Register split, set inside each role (reg_dec / reg_inc).
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ producers
+        // Lane 0 of warp 0 loads Q and streams the K ring, lane 0 of warp 2 the
+        // V ring: one issuing thread alone cannot keep both rings filled at the
+        // rate the MMAs (or HBM, for the fan-out) consume them.
         reg_dec<FAN>();
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            if (FAN) {
-                tma_prefetch_desc(&tm_k2);
-                tma_prefetch_desc(&tm_v2);
+            const bool is_k = (warp == 0);
+            uint64_t* full = is_k ? k_full : v_full;
+            uint64_t* empty = is_k ? k_empty : v_empty;
+            uint8_t* ring = is_k ? k_smem : v_smem;
+            const int n_stages = is_k ? nK : nV;
+            const CUtensorMap* map1 = is_k ? &tm_k : &tm_v;
+            const CUtensorMap* map2 = is_k ? &tm_k2 : &tm_v2;
+            tma_prefetch_desc(map1);
+            if (FAN) tma_prefetch_desc(map2);
+            if (is_k) {
+                tma_prefetch_desc(&tm_q);
+                mbar_arrive_expect_tx(q_full, u.n_q * C::kTileBytes);
+                for (int t = 0; t < u.n_q; ++t)
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_4d(&tm_q, q_full, q_smem + t * C::kTileBytes + c * 16384, c * 64, u.qc1[t],
+                                    u.qc2[t], u.qc3[t]);
             }
-            mbar_arrive_expect_tx(q_full, u.n_q * C::kTileBytes);
-            for (int t = 0; t < u.n_q; ++t)
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(&tm_q, q_full, q_smem + t * C::kTileBytes + c * 16384, c * 64, u.qc1[t], u.qc2[t],
-                                u.qc3[t]);
             int issued = 0;
-            StageCtr ck, cv;
+            StageCtr cs;
             TileWalk<FAN> wi;
             wi.start(p, u, w);
             bool ok = true;
             for (int i = 0; ok && i < total; ++i, wi.next(p, u)) {
                 const bool from_suffix = FAN && wi.seg == 1;
-                const CUtensorMap* kmap = from_suffix ? &tm_k2 : &tm_k;
-                const CUtensorMap* vmap = from_suffix ? &tm_v2 : &tm_v;
+                const CUtensorMap* map = from_suffix ? map2 : map1;
                 const int z = FAN ? (from_suffix ? wi.b : 0) : u.kv_z;
-                // K ring, then V ring: K tiles run ahead of the V tiles PV is still reading
-                ok = mbar_wait(&k_empty[ck.s], ck.ph ^ 1, abort_flag, status, 0x01000000u | (2 * i));
+                ok = mbar_wait(&empty[cs.s], cs.ph ^ 1, abort_flag, status, 0x01000000u | (2 * i + (is_k ? 0 : 1)));
                 if (!ok) break;
-                mbar_arrive_expect_tx(&k_full[ck.s], C::kTileBytes);
+                mbar_arrive_expect_tx(&full[cs.s], C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(kmap, &k_full[ck.s], k_smem + ck.s * C::kTileBytes + c * 16384, c * 64, u.kv_head,
+                    tma_load_4d(map, &full[cs.s], ring + cs.s * C::kTileBytes + c * 16384, c * 64, u.kv_head,
                                 wi.key(), z);
-                ck.next(nK);
-                ++issued;
-                ok = mbar_wait(&v_empty[cv.s], cv.ph ^ 1, abort_flag, status, 0x01000000u | (2 * i + 1));
-                if (!ok) break;
-                mbar_arrive_expect_tx(&v_full[cv.s], C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(vmap, &v_full[cv.s], v_smem + cv.s * C::kTileBytes + c * 16384, c * 64, u.kv_head,
-                                wi.key(), z);
-                cv.next(nV);
+                cs.next(n_stages);
                 ++issued;
             }
             if (*abort_flag) {
                 // let copies already in flight land before the CTA exits: the
-                // last nK K loads and nV V loads issued
-                StageCtr lk, lv;
-                const int nk_issued = (issued + 1) / 2, nv_issued = issued / 2;
-                for (int n = 0; n < nk_issued; ++n) {
-                    if (n >= nk_issued - nK) mbar_wait_landing(&k_full[lk.s], lk.ph);
-                    lk.next(nK);
+                // last n_stages loads of this ring (and Q)
+                StageCtr ls;
+                for (int n = 0; n < issued; ++n) {
+                    if (n >= issued - n_stages) mbar_wait_landing(&full[ls.s], ls.ph);
+                    ls.next(n_stages);
                 }
-                for (int n = 0; n < nv_issued; ++n) {
-                    if (n >= nv_issued - nV) mbar_wait_landing(&v_full[lv.s], lv.ph);
-                    lv.next(nV);
-                }
-                mbar_wait_landing(q_full, 0);
+                if (is_k) mbar_wait_landing(q_full, 0);
             }
         }
     } else if (warp == 1) {
@@ -588,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(drain);
             mbar_wait(drain, 0, abort_flag, status, 0);
         }
-    } else if (warp < 4) {
+    } else if (warp == 3) {
         reg_dec<FAN>();
     } else {
         // ------------------------------------------------------------ softmax + epilogue

@@ -8,14 +8,15 @@
 //   O = sum_p w_p O_p / sum_p w_p,  lse = M + ln(sum_p w_p),
 // which is the exactness identity of "RingAttention and Context Parallelism",
 // section 2, applied to whole shards.  An empty partial (lse = -inf) gets
-// weight 0 and its O is not read.
+// weight 0 and its O does not enter the result, whatever it holds.
 //
 // Lane l owns D/32 consecutive head dims, so a warp reads each partial row as
 // one contiguous 128- to 512-byte segment.  fp32 arithmetic.  Bandwidth-bound:
-// each non-empty partial row is read once.  Three kernels, chosen by shape: a
-// tiled one for many rows and up to 256 partials (coalesced lse reads, weights
-// in shared memory), a block-per-row one for few rows with many partials, and
-// a warp-per-row one otherwise.
+// each partial row is read once.  Four kernels, chosen by shape: a tiled one
+// for many rows and up to 256 partials (coalesced lse reads, weights in shared
+// memory); for fewer rows, bulk copies of up to 32 partials' rows into shared
+// memory (every byte a CTA needs in flight at once), a block per row for more
+// partials than that, and a looping warp per row otherwise.
 #include <cmath>
 
 #include "ra_device.cuh"
@@ -195,6 +196,88 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_kernel(const void* __re
 // Phase 2: each warp merges four of the 32 rows, streaming each non-empty
 // partial row (D contiguous elements) with eight loads in flight.
 constexpr int kMaxTiledP = 256;
+
+// Few rows, up to 32 partials: a CTA takes rb <= 8 consecutive rows.  The
+// rows of one partial are contiguous, so thread 0 fetches each partial's rb
+// rows with one bulk copy into shared memory (all P copies in flight at once,
+// no register or L1 miss slots held), while warp w reads lse of its row, one
+// partial per lane.  Warp w then combines row w from shared memory.  Rows of
+// empty partials are copied (they lie inside the caller's buffer) but dropped
+// by a select, never multiplied in, so whatever they hold (NaN included)
+// cannot reach the result.
+constexpr int kBulkMaxP = 32;
+template <int D, bool PART_F32, bool OUT_F32>
+__global__ void __launch_bounds__(kWarps * 32) lse_merge_bulk_kernel(const void* __restrict__ part_O,
+                                                                     const float* __restrict__ part_lse,
+                                                                     void* __restrict__ out,
+                                                                     float* __restrict__ out_lse, int P, int S, int H,
+                                                                     long long rows, int rb) {
+    constexpr int E = D / 32;
+    constexpr int esz = PART_F32 ? 4 : 2;
+    constexpr int kRowBytes = D * esz;
+    extern __shared__ __align__(128) uint8_t smem[];  // [P][rb][D] partial rows, then the barrier
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + P * rb * kRowBytes);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long rid0 = static_cast<long long>(blockIdx.x) * rb;
+    const int nr = static_cast<int>(rows - rid0 < rb ? rows - rid0 : rb);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    grid_dependency_wait();
+    if (threadIdx.x == 0) {
+        const uint32_t seg = static_cast<uint32_t>(nr) * kRowBytes;
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(P) * seg);
+        for (int p = 0; p < P; ++p)
+            bulk_load(smem + p * rb * kRowBytes,
+                      static_cast<const char*>(part_O) + (static_cast<long long>(p) * rows + rid0) * kRowBytes, seg,
+                      bar);
+    }
+    const long long rid = rid0 + warp;
+    long long lse_idx = 0;
+    float L = -INFINITY;
+    if (warp < nr) {
+        const int h = static_cast<int>(rid % H);
+        const long long bs = rid / H;
+        const int s = static_cast<int>(bs % S);
+        const long long b = bs / S;
+        lse_idx = (b * H + h) * S + s;
+        if (lane < P) L = part_lse[lane * rows + lse_idx];
+    }
+    if (!mbar_wait(bar, 0, abort_flag, g_merge_status, 0x31000000u | (blockIdx.x & 0xffffffu))) {
+        if (threadIdx.x == 0) mbar_wait_landing(bar, 0);  // copies in flight land before the CTA exits
+        return;
+    }
+    if (warp >= nr) return;
+    float M = L;
+#pragma unroll
+    for (int sh = 16; sh; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
+    const float myw = (L == -INFINITY) ? 0.f : expf(L - M);  // empty partial: weight 0
+    float wsum = myw;
+#pragma unroll
+    for (int sh = 16; sh; sh >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, sh);
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    const uint8_t* mine = smem + warp * kRowBytes + lane * E * esz;
+    for (int p = 0; p < P; ++p) {
+        const float w = __shfl_sync(0xffffffffu, myw, p);
+        if (w != 0.f) {
+            float x[E];
+            Vec<E, PART_F32>::load(mine + p * rb * kRowBytes, x);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] *= inv;
+    Vec<E, OUT_F32>::store(static_cast<char*>(out) + (rid * D + lane * E) * (OUT_F32 ? 4 : 2), acc);
+    if (out_lse && lane == 0) out_lse[lse_idx] = wsum > 0.f ? M + logf(wsum) : -INFINITY;
+}
 
 template <int D, bool PART_F32, bool OUT_F32>
 __global__ void __launch_bounds__(kWarps * 32) lse_merge_tiled_kernel(const void* __restrict__ part_O,
@@ -424,6 +507,20 @@ cudaError_t run(const MergeArgs& a, long long rows, cudaStream_t stream) {
         }
         return launch_pdl(lse_merge_tiled_kernel<D, PF, OF>, static_cast<unsigned>(blocks), kWarps * 32, smem, stream,
                           a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows);
+    }
+    if (a.P <= kBulkMaxP) {
+        // rows per CTA: 8, halved while that leaves fewer than two CTAs per SM
+        int rb = kWarps;
+        while (rb > 1 && (rows + rb - 1) / rb < 2 * n_sm) rb >>= 1;
+        const size_t smem = static_cast<size_t>(a.P) * rb * D * (PF ? 4 : 2) + 16;
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(lse_merge_bulk_kernel<D, PF, OF>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+        }
+        const long long blocks = (rows + rb - 1) / rb;
+        return launch_pdl(lse_merge_bulk_kernel<D, PF, OF>, static_cast<unsigned>(blocks), kWarps * 32, smem, stream,
+                          a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.S, a.H, rows, rb);
     }
     if (a.P >= 8 && rows <= 64 * n_sm * kWarps) {
         return launch_pdl(lse_merge_splitp_kernel<D, PF, OF>, static_cast<unsigned>(rows), kWarps * 32, 0, stream,

@@ -205,14 +205,19 @@ def test_lse_merge_many_rows(dt, D, S):
     assert torch.all(mO[0, 7, 5] == 0) and mL[0, 5, 7].item() == -float("inf")
 
 
-@pytest.mark.parametrize("P,B,S,H,D", [(40, 1, 16, 64, 128), (9, 1, 3, 4, 64), (33, 2, 7, 3, 128)])
+@pytest.mark.parametrize("P,B,S,H,D", [(40, 1, 16, 64, 128), (9, 1, 3, 4, 64), (33, 2, 7, 3, 128),
+                                       (19, 1, 16, 64, 128), (32, 1, 5, 3, 64), (17, 2, 9, 8, 128),
+                                       (16, 1, 147, 64, 128), (1, 1, 4, 2, 64), (2, 1, 3, 2, 128)])
 def test_lse_merge_few_rows_many_partials(P, B, S, H, D):
-    """The fan-out join shape: few rows, many partials (block-per-row merge)."""
+    """The fan-out join shape: few rows, many partials (register-resident warp-per-row merge up to 32
+    partials, block-per-row beyond).  Empty partials hold NaN, which must not reach the result."""
     g = torch.Generator().manual_seed(P + S)
     pO = torch.randn(P, B, S, H, D, generator=g)
     pL = torch.randn(P, B, H, S, generator=g) * 3
     pL[1::4] = -float("inf")
-    mO, mL = ra.lse_merge(pO.cuda(), pL.cuda())
+    pO_nan = pO.clone()
+    pO_nan[1::4] = float("nan")
+    mO, mL = ra.lse_merge(pO_nan.cuda(), pL.cuda())
     ra.device_status()
     rO, rL = oracle.lse_merge(pO.double().numpy(), pL.double().numpy())
     _close(mO.cpu().double().numpy(), rO, 1e-5, "merged O")
