@@ -76,7 +76,9 @@ struct Cfg {
     static constexpr int kMaxKV = D == 128 ? 3 : 4;          // per ring
     static constexpr int kQOff = 0;
     static constexpr int kBarOff = kDataTiles * kTileBytes;
-    static constexpr int kNumBars = 1 + 4 * kMaxKV + 7;
+    static constexpr int kIterRing = 4;  // iteration-done barriers (stage release in paired mode)
+    static_assert(kMaxKV <= kIterRing, "a producer may lag at most kIterRing iterations");
+    static constexpr int kNumBars = 1 + 4 * kMaxKV + 7 + kIterRing;
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 };
@@ -395,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* p_full = s_full + 2;             // [2]
     uint64_t* o_done = p_full + 2;             // [2]
     uint64_t* drain = o_done + 2;
+    uint64_t* iter_done = drain + 1;           // [kIterRing]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -424,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&o_done[t], 1);
         }
         mbar_init(drain, 1);
+        for (int r = 0; r < C::kIterRing; ++r) mbar_init(&iter_done[r], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -473,7 +477,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool from_suffix = FAN && wi.seg == 1;
                 const CUtensorMap* map = from_suffix ? map2 : map1;
                 const int z = FAN ? (from_suffix ? wi.b : 0) : u.kv_z;
-                ok = mbar_wait(&empty[cs.s], cs.ph ^ 1, abort_flag, status, 0x01000000u | (2 * i + (is_k ? 0 : 1)));
+                // Stage free: split units release K and V stages one by one; paired
+                // units once per MMA iteration (K tile j is done with after
+                // iteration j, V tile j after iteration j + 1).
+                const unsigned where = 0x01000000u | (2 * i + (is_k ? 0 : 1));
+                if (u.split) {
+                    ok = mbar_wait(&empty[cs.s], cs.ph ^ 1, abort_flag, status, where);
+                } else if (i >= n_stages) {
+                    const int j = is_k ? i - n_stages : i - n_stages + 1;
+                    ok = mbar_wait(&iter_done[j & (C::kIterRing - 1)], (j / C::kIterRing) & 1, abort_flag, status,
+                                   where);
+                }
                 if (!ok) break;
                 mbar_arrive_expect_tx(&full[cs.s], C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
@@ -554,7 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv<D>(tS + 128, tS, v_lo0 + cv.s * kStageLo, !fresh_prev);
-                        mma_commit(&o_done[t]);
                     }
                     if (i < total) {
                         if (t == 0) {
@@ -567,14 +580,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                if (i > 0) {
-                    mma_commit(&v_empty[cv.s]);
-                    cv.next(nV);
-                }
-                if (i < total) {
-                    mma_commit(&k_empty[ck.s]);
-                    ck.next(nK);
-                }
+                // one commit frees K tile i and V tile i - 1; s_full of the next
+                // tile tells the softmax that this iteration's PV is done
+                mma_commit(&iter_done[i & (C::kIterRing - 1)]);
+                if (i > 0) cv.next(nV);
+                if (i < total) ck.next(nK);
                 if (i > 0 && !FAN) wp.next();
             }
             // all issued MMAs complete before TMEM is released
@@ -614,10 +624,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_use = -INFINITY, l_sum = 0.f;
         bool ok = true;
 
-        // Normalise the O accumulator (after this slot's PV number j_done) and write it as part `part`.
-        auto flush = [&](int j_done, int part) -> bool {
-            if (!mbar_wait(&o_done[t], j_done & 1, abort_flag, status, 0x06000000u | j_done)) return false;
-            tc_fence_after();
+        // Normalise the O accumulator and write it as part `part`, once `done`
+        // (if given) shows its last PV complete.
+        auto flush = [&](uint64_t* done, uint32_t phase, int part) -> bool {
+            if (done) {
+                if (!mbar_wait(done, phase, abort_flag, status, 0x06000000u)) return false;
+                tc_fence_after();
+            }
             const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
             const long long ob = o_row_base + static_cast<long long>(part) * out.o_part;
 #pragma unroll
@@ -647,16 +660,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u.split) wi.next(p, u);
             }
             const bool tile_first = !FAN && wi.ring.first();
+            const int tile_kb = wi.key();
+            if (!(ok = mbar_wait(&s_full[t], jj & 1, abort_flag, status, 0x07000000u | i))) break;
+            tc_fence_after();
             if (p.partials && tile_first && jj > 0) {
-                // the previous KV shard of the ring is complete: flush it
-                if (!(ok = flush(jj - 1, last_shard))) break;
+                // The previous KV shard of the ring is complete (this tile's S was
+                // committed after its last PV): flush it.
+                flush(nullptr, 0, last_shard);
                 m_use = -INFINITY;
                 l_sum = 0.f;
             }
             if (!FAN) last_shard = wi.ring.j;
-            const int tile_kb = wi.key();
-            if (!(ok = mbar_wait(&s_full[t], jj & 1, abort_flag, status, 0x07000000u | i))) break;
-            tc_fence_after();
             uint32_t sr[kTileN];
 #pragma unroll
             for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
@@ -719,9 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float rs = (a0 + a1) + (a2 + a3);
             l_sum = l_sum * alpha + rs;
             if (__any_sync(0xffffffffu, resc)) {
-                // O of the previous tiles must be complete before it is rescaled
-                if (!(ok = mbar_wait(&o_done[t], (jj - 1) & 1, abort_flag, status, 0x08000000u | i))) break;
-                tc_fence_after();
+                // O of the previous tiles is complete: this tile's S was committed
+                // after their PV.
                 const float a = resc ? alpha : 1.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -796,10 +809,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = have0;
             }
         } else if (ok) {
+            // the last PV: every MMA of the CTA is complete once `drain` is
             if (!FAN && p.partials) {
-                ok = flush(jj - 1, last_shard);
+                ok = flush(drain, 0, last_shard);
             } else if (jj > 0) {
-                ok = flush(jj - 1, FAN ? u.slot[t] : 0);
+                ok = flush(drain, 0, FAN ? u.slot[t] : 0);
             } else if (row_ok && out.lse) {
                 // a unit with no KV tile: an empty partial (its O is never read)
                 out.lse[lse_base + static_cast<long long>(u.slot[t]) * out.lse_part] = -INFINITY;
