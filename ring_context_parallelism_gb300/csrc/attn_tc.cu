@@ -351,22 +351,23 @@ struct StageCtr {
     }
 };
 
-// Register split per warpgroup (sum = the launch's 384 x 168 = 64512): ring
-// mode 128 x 40 + 2 x 128 x 232; fan-out mode, whose producer also walks the
-// folded suffixes, 128 x 56 + 2 x 128 x 224.
+// Register split per warpgroup (at most the launch's 384 x 168 = 64512): ring
+// mode 128 x 48 + 2 x 128 x 224 (the MMA issuer's loop fits without spills);
+// fan-out mode, whose producers also walk the folded suffixes, 128 x 56 +
+// 2 x 128 x 224.
 template <bool FAN>
 __device__ __forceinline__ void reg_dec() {
     if (FAN)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     else
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 48;" ::: "memory");
 }
 template <bool FAN>
 __device__ __forceinline__ void reg_inc() {
     if (FAN)
         asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
     else
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
 }
 
 template <int D, bool FAN>
