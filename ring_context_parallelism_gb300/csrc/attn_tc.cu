@@ -554,9 +554,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Paired tiles: iteration i issues PV_t(i-1) and QK_t(i) for t = 0, 1.
+            // Two tiles (the common case): straight-line issue, stage descriptor
+            // words advanced in place, ring position tracked only for partials.
+            if (!u.split && T == 2) {
+                const uint32_t tS0 = tmem_base, tS1 = tmem_base + 256;
+                const uint32_t q0 = q_lo0, q1 = q_lo0 + kStageLo;
+                const uint32_t k_end = k_lo0 + nK * kStageLo, v_end = v_lo0 + nV * kStageLo;
+                uint32_t k_lo = k_lo0, v_lo = v_lo0;
+                const bool track = p.partials && !FAN;
+                RingIter wp;  // tile i - 1 (shard openings restart O in partials mode)
+                if (track) wp.start(w);
+                for (int i = 0; i <= total; ++i) {
+                    const uint32_t par = (i - 1) & 1;
+                    const bool acc_prev = track ? !wp.first() : (i != 1);
+                    if (i > 0) {
+                        if (!(ok = mbar_wait(&v_full[cv.s], cv.ph, abort_flag, status, 0x03000000u | (i - 1)))) break;
+                        if (!(ok = mbar_wait(&p_full[0], par, abort_flag, status, 0x04000000u | (i - 1)))) break;
+                        tc_fence_after();
+                        issue_pv<D>(tS0 + 128, tS0, v_lo, acc_prev);
+                    }
+                    if (i < total) {
+                        if (!(ok = mbar_wait(&k_full[ck.s], ck.ph, abort_flag, status, 0x05000000u | i))) break;
+                        tc_fence_after();
+                        issue_qk<D>(tS0, q0, k_lo);
+                        mma_commit(&s_full[0]);
+                    }
+                    if (i > 0) {
+                        if (!(ok = mbar_wait(&p_full[1], par, abort_flag, status, 0x04000000u | (i - 1)))) break;
+                        tc_fence_after();
+                        issue_pv<D>(tS1 + 128, tS1, v_lo, acc_prev);
+                    }
+                    if (i < total) {
+                        issue_qk<D>(tS1, q1, k_lo);
+                        mma_commit(&s_full[1]);
+                    }
+                    // one commit frees K tile i and V tile i - 1; s_full of the
+                    // next tile tells the softmax that this iteration's PV is done
+                    mma_commit(&iter_done[i & (C::kIterRing - 1)]);
+                    if (i > 0) {
+                        cv.next(nV);
+                        v_lo = (v_lo + kStageLo == v_end) ? v_lo0 : v_lo + kStageLo;
+                        if (track) wp.next();
+                    }
+                    if (i < total) {
+                        ck.next(nK);
+                        k_lo = (k_lo + kStageLo == k_end) ? k_lo0 : k_lo + kStageLo;
+                    }
+                }
+            }
             RingIter wp;  // at iteration i >= 1: tile i-1 (shard openings restart O in partials mode)
             if (!FAN) wp.start(w);
-            for (int i = 0; ok && !u.split && i <= total; ++i) {
+            for (int i = 0; ok && !u.split && T == 1 && i <= total; ++i) {
                 const bool fresh_prev = (p.partials && !FAN) ? wp.first() : (i == 1);
                 for (int t = 0; t < T && ok; ++t) {
                     const uint32_t tS = tmem_base + t * 256;
