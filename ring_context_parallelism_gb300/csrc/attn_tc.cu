@@ -76,8 +76,17 @@ struct Cfg {
     static constexpr int kMaxKV = D == 128 ? 3 : 4;          // per ring
     static constexpr int kQOff = 0;
     static constexpr int kBarOff = kDataTiles * kTileBytes;
-    static constexpr int kIterRing = 4;  // iteration-done barriers (stage release in paired mode)
-    static_assert(kMaxKV <= kIterRing, "a producer may lag at most kIterRing iterations");
+    // Iteration-done barriers (stage release in paired mode): a producer waits
+    // for iteration j while the MMA issuer is at most max(stages) iterations
+    // past it, so that many slots keep the parity of slot j unambiguous.
+    static constexpr int kNVPair = kDataTiles - 2 - kMaxKV;  // V stages with two Q tiles
+    static constexpr int kIterRing = kMaxKV > kNVPair ? kMaxKV : kNVPair;
+    // Issue loop unrolled over a whole cycle of the three rings: every K and
+    // V stage used an even number of times (its barrier phase back where it
+    // started) and every iteration-done slot equally often.
+    static constexpr int kGcd(int a, int b) { return b == 0 ? a : kGcd(b, a % b); }
+    static constexpr int kLcm(int a, int b) { return a / kGcd(a, b) * b; }
+    static constexpr int kBlk = kLcm(kLcm(2 * kMaxKV, 2 * kNVPair), kIterRing);
     static constexpr int kNumBars = 1 + 4 * kMaxKV + 7 + kIterRing;
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
@@ -303,6 +312,7 @@ struct TileWalk {
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_lo, uint32_t k_lo) {
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, false, false);
+    asm volatile("" : "+r"(q_lo), "+r"(k_lo));  // descriptor words formed here, next to their MMAs
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * (32 >> 4);
@@ -315,6 +325,7 @@ __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_lo, uint32_t k_
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo, bool accumulate_first) {
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, D, false, true);
+    asm volatile("" : "+r"(tP), "+r"(v_lo));
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk)
         mma_ts(tO, tP + kk * 8, sw128_desc(v_lo + kk * (2048 >> 4)), idesc, (kk > 0 || accumulate_first) ? 1u : 0u);
@@ -486,8 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait(&empty[cs.s], cs.ph ^ 1, abort_flag, status, where);
                 } else if (i >= n_stages) {
                     const int j = is_k ? i - n_stages : i - n_stages + 1;
-                    ok = mbar_wait(&iter_done[j & (C::kIterRing - 1)], (j / C::kIterRing) & 1, abort_flag, status,
-                                   where);
+                    ok = mbar_wait(&iter_done[j % C::kIterRing], (j / C::kIterRing) & 1, abort_flag, status, where);
                 }
                 if (!ok) break;
                 mbar_arrive_expect_tx(&full[cs.s], C::kTileBytes);
@@ -564,23 +574,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool track = p.partials && !FAN;
                 RingIter wp;  // tile i - 1 (shard openings restart O in partials mode)
                 if (track) wp.start(w);
-                for (int i = 0; i <= total; ++i) {
+                // One iteration with runtime stage indices.
+                auto step = [&](int i) -> bool {
                     const uint32_t par = (i - 1) & 1;
                     const bool acc_prev = track ? !wp.first() : (i != 1);
                     if (i > 0) {
-                        if (!(ok = mbar_wait(&v_full[cv.s], cv.ph, abort_flag, status, 0x03000000u | (i - 1)))) break;
-                        if (!(ok = mbar_wait(&p_full[0], par, abort_flag, status, 0x04000000u | (i - 1)))) break;
+                        if (!mbar_wait(&v_full[cv.s], cv.ph, abort_flag, status, 0x03000000u | (i - 1))) return false;
+                        if (!mbar_wait(&p_full[0], par, abort_flag, status, 0x04000000u | (i - 1))) return false;
                         tc_fence_after();
                         issue_pv<D>(tS0 + 128, tS0, v_lo, acc_prev);
                     }
                     if (i < total) {
-                        if (!(ok = mbar_wait(&k_full[ck.s], ck.ph, abort_flag, status, 0x05000000u | i))) break;
+                        if (!mbar_wait(&k_full[ck.s], ck.ph, abort_flag, status, 0x05000000u | i)) return false;
                         tc_fence_after();
                         issue_qk<D>(tS0, q0, k_lo);
                         mma_commit(&s_full[0]);
                     }
                     if (i > 0) {
-                        if (!(ok = mbar_wait(&p_full[1], par, abort_flag, status, 0x04000000u | (i - 1)))) break;
+                        if (!mbar_wait(&p_full[1], par, abort_flag, status, 0x04000000u | (i - 1))) return false;
                         tc_fence_after();
                         issue_pv<D>(tS1 + 128, tS1, v_lo, acc_prev);
                     }
@@ -590,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // one commit frees K tile i and V tile i - 1; s_full of the
                     // next tile tells the softmax that this iteration's PV is done
-                    mma_commit(&iter_done[i & (C::kIterRing - 1)]);
+                    mma_commit(&iter_done[i % C::kIterRing]);
                     if (i > 0) {
                         cv.next(nV);
                         v_lo = (v_lo + kStageLo == v_end) ? v_lo0 : v_lo + kStageLo;
@@ -600,7 +611,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ck.next(nK);
                         k_lo = (k_lo + kStageLo == k_end) ? k_lo0 : k_lo + kStageLo;
                     }
+                    return true;
+                };
+                int i = 0;
+                ok = total < 0 || step(0);
+                i = 1;
+                // Steady state in blocks of kBlk iterations from i = 1: kBlk is a
+                // multiple of twice each ring size and of the iteration-barrier
+                // ring, so every stage, barrier and parity below is a constant, and
+                // the runtime state after a block equals the state at i = 1.
+                constexpr int kBlk = C::kBlk;
+                constexpr int nKc = C::kMaxKV, nVc = C::kNVPair;
+                // (ring prefill only: the fan-out kernel's larger roles and this
+                // block together do not stay in the instruction cache)
+                for (; !FAN && ok && i + kBlk <= total; i += kBlk) {
+                    const uint32_t kb = k_lo0, vb = v_lo0, qa = q0, qb = q1;
+#pragma unroll
+                    for (int pos = 0; pos < kBlk; ++pos) {
+                        const int ks = (1 + pos) % nKc, kph = ((1 + pos) / nKc) & 1;
+                        const int vs = pos % nVc, vph = (pos / nVc) & 1;
+                        const uint32_t par = pos & 1;
+                        const bool acc_prev = track ? !wp.first() : (i + pos != 1);
+                        if (!(ok = mbar_wait(&v_full[vs], vph, abort_flag, status, 0x03000000u))) break;
+                        if (!(ok = mbar_wait(&p_full[0], par, abort_flag, status, 0x04000000u))) break;
+                        tc_fence_after();
+                        issue_pv<D>(tS0 + 128, tS0, vb + vs * kStageLo, acc_prev);
+                        if (!(ok = mbar_wait(&k_full[ks], kph, abort_flag, status, 0x05000000u))) break;
+                        tc_fence_after();
+                        issue_qk<D>(tS0, qa, kb + ks * kStageLo);
+                        mma_commit(&s_full[0]);
+                        if (!(ok = mbar_wait(&p_full[1], par, abort_flag, status, 0x04000000u))) break;
+                        tc_fence_after();
+                        issue_pv<D>(tS1 + 128, tS1, vb + vs * kStageLo, acc_prev);
+                        issue_qk<D>(tS1, qb, kb + ks * kStageLo);
+                        mma_commit(&s_full[1]);
+                        mma_commit(&iter_done[(1 + pos) % C::kIterRing]);
+                        if (track) wp.next();
+                    }
                 }
+                for (; ok && i <= total; ++i) ok = step(i);
             }
             RingIter wp;  // at iteration i >= 1: tile i-1 (shard openings restart O in partials mode)
             if (!FAN) wp.start(w);
@@ -631,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 // one commit frees K tile i and V tile i - 1; s_full of the next
                 // tile tells the softmax that this iteration's PV is done
-                mma_commit(&iter_done[i & (C::kIterRing - 1)]);
+                mma_commit(&iter_done[i % C::kIterRing]);
                 if (i > 0) cv.next(nV);
                 if (i < total) ck.next(nK);
                 if (i > 0 && !FAN) wp.next();
