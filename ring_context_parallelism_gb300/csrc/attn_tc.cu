@@ -786,9 +786,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kTileN; ++c)
                     if (c > lim) sr[c] = 0xff800000u;  // -inf
             }
-            float mraw = -INFINITY;
+            // row max as four independent chains (a quarter of the dependent latency)
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < kTileN; c += 2) mraw = fmax3(mraw, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            for (int c = 0; c < kTileN; c += 8) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    m4[q] = fmax3(m4[q], __uint_as_float(sr[c + 2 * q]), __uint_as_float(sr[c + 2 * q + 1]));
+            }
+            const float mraw = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
             const float mx = mraw * p.scale_log2;  // scores in log2 units
             const bool fresh = (jj == 0) || (p.partials && tile_first);
             float alpha = 1.f;
