@@ -595,12 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         issue_pv<D>(tS1 + 128, tS1, v_lo, acc_prev);
                     }
-                    if (i < total) {
-                        issue_qk<D>(tS1, q1, k_lo);
-                        mma_commit(&s_full[1]);
-                    }
-                    // one commit frees K tile i and V tile i - 1; s_full of the
-                    // next tile tells the softmax that this iteration's PV is done
+                    if (i < total) issue_qk<D>(tS1, q1, k_lo);
+                    // One commit frees K tile i and V tile i - 1 and hands S of tile
+                    // 1 to its softmax; s_full / iter_done of the next tile tell the
+                    // softmax that this iteration's PV is done.
                     mma_commit(&iter_done[i % C::kIterRing]);
                     if (i > 0) {
                         cv.next(nV);
@@ -644,7 +642,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         issue_pv<D>(tS1 + 128, tS1, vb + vs * kStageLo, acc_prev);
                         issue_qk<D>(tS1, qb, kb + ks * kStageLo);
-                        mma_commit(&s_full[1]);
                         mma_commit(&iter_done[(1 + pos) % C::kIterRing]);
                         if (track) wp.next();
                     }
@@ -759,7 +756,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool tile_first = !FAN && wi.ring.first();
             const int tile_kb = wi.key();
-            if (!(ok = mbar_wait(&s_full[t], jj & 1, abort_flag, status, 0x07000000u | i))) break;
+            // S of tile 1 of a two-tile unit is signalled by the iteration-done
+            // commit that follows its QK (no separate commit)
+            uint64_t* s_bar = &s_full[t];
+            uint32_t s_par = jj & 1;
+            if (t == 1 && !u.split && T == 2) {
+                s_bar = &iter_done[jj % C::kIterRing];
+                s_par = (jj / C::kIterRing) & 1;
+            }
+            if (!(ok = mbar_wait(s_bar, s_par, abort_flag, status, 0x07000000u | i))) break;
             tc_fence_after();
             if (p.partials && tile_first && jj > 0) {
                 // The previous KV shard of the ring is complete (this tile's S was
