@@ -81,12 +81,15 @@ struct Cfg {
     // past it, so that many slots keep the parity of slot j unambiguous.
     static constexpr int kNVPair = kDataTiles - 2 - kMaxKV;  // V stages with two Q tiles
     static constexpr int kIterRing = kMaxKV > kNVPair ? kMaxKV : kNVPair;
-    // Issue loop unrolled over a whole cycle of the three rings: every K and
-    // V stage used an even number of times (its barrier phase back where it
-    // started) and every iteration-done slot equally often.
+    // Issue loop unrolled over a whole cycle of the rings (and of the two
+    // tile-slot parities): every stage and iteration-done slot used equally
+    // often per block.  A ring whose stages are used an odd number of times
+    // per block sees its barrier parities flip from one block to the next.
     static constexpr int kGcd(int a, int b) { return b == 0 ? a : kGcd(b, a % b); }
     static constexpr int kLcm(int a, int b) { return a / kGcd(a, b) * b; }
-    static constexpr int kBlk = kLcm(kLcm(2 * kMaxKV, 2 * kNVPair), kIterRing);
+    static constexpr int kBlk = kLcm(kLcm(kLcm(kMaxKV, kNVPair), kIterRing), 2);
+    static constexpr bool kKFlip = (kBlk / kMaxKV) % 2 == 1;
+    static constexpr bool kVFlip = (kBlk / kNVPair) % 2 == 1;
     static constexpr int kNumBars = 1 + 4 * kMaxKV + 7 + kIterRing;
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
@@ -615,19 +618,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = total < 0 || step(0);
                 i = 1;
                 // Steady state in blocks of kBlk iterations from i = 1: kBlk is a
-                // multiple of twice each ring size and of the iteration-barrier
-                // ring, so every stage, barrier and parity below is a constant, and
-                // the runtime state after a block equals the state at i = 1.
+                // multiple of each ring size, of the iteration-barrier ring and of
+                // 2, so every stage, barrier and slot parity below is a constant;
+                // a ring's phase parity is a constant up to a per-block flip.
                 constexpr int kBlk = C::kBlk;
                 constexpr int nKc = C::kMaxKV, nVc = C::kNVPair;
-                // (ring prefill only: the fan-out kernel's larger roles and this
-                // block together do not stay in the instruction cache)
+                uint32_t kflip = 0, vflip = 0;
+                // (ring prefill only: in the fan-out kernel the unrolled block
+                // measured slower, its split path included)
                 for (; !FAN && ok && i + kBlk <= total; i += kBlk) {
                     const uint32_t kb = k_lo0, vb = v_lo0, qa = q0, qb = q1;
 #pragma unroll
                     for (int pos = 0; pos < kBlk; ++pos) {
-                        const int ks = (1 + pos) % nKc, kph = ((1 + pos) / nKc) & 1;
-                        const int vs = pos % nVc, vph = (pos / nVc) & 1;
+                        const int ks = (1 + pos) % nKc;
+                        const uint32_t kph = (((1 + pos) / nKc) & 1) ^ kflip;
+                        const int vs = pos % nVc;
+                        const uint32_t vph = ((pos / nVc) & 1) ^ vflip;
                         const uint32_t par = pos & 1;
                         const bool acc_prev = track ? !wp.first() : (i + pos != 1);
                         if (!(ok = mbar_wait(&v_full[vs], vph, abort_flag, status, 0x03000000u))) break;
@@ -645,7 +651,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_commit(&iter_done[(1 + pos) % C::kIterRing]);
                         if (track) wp.next();
                     }
+                    if (C::kKFlip) kflip ^= 1;
+                    if (C::kVFlip) vflip ^= 1;
                 }
+                // the runtime rings resume where the blocks left them
+                ck.ph ^= kflip;
+                cv.ph ^= vflip;
                 for (; ok && i <= total; ++i) ok = step(i);
             }
             RingIter wp;  // at iteration i >= 1: tile i-1 (shard openings restart O in partials mode)
