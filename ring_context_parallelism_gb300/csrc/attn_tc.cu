@@ -384,14 +384,22 @@ __device__ __forceinline__ void reg_inc() {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
 }
 
-template <int D, bool FAN>
+// Kernel variants: ring prefill, and fan-out launches whose units all split
+// their KV tiles over the two tile slots (one row tile), all pair two row
+// tiles, or mix both (suffix units without a prefix).  The uniform fan-out
+// variants compile only their own issue and softmax paths.
+enum KernelMode : int { kModeRing = 0, kModeFanMixed = 1, kModeFanSplit = 2, kModeFanPaired = 3 };
+
+template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k2,
                    const __grid_constant__ CUtensorMap tm_v2, const TcParams p) {
     using C = Cfg<D>;
+    constexpr bool FAN = MODE != kModeRing;
     const Unit u = decode_unit<FAN>(p);
     if (!u.valid) return;
+    const bool split = MODE == kModeFanSplit ? true : (MODE == kModeRing || MODE == kModeFanPaired) ? false : u.split != 0;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -496,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // units once per MMA iteration (K tile j is done with after
                 // iteration j, V tile j after iteration j + 1).
                 const unsigned where = 0x01000000u | (2 * i + (is_k ? 0 : 1));
-                if (u.split) {
+                if (split) {
                     ok = mbar_wait(&empty[cs.s], cs.ph ^ 1, abort_flag, status, where);
                 } else if (i >= n_stages) {
                     const int j = is_k ? i - n_stages : i - n_stages + 1;
@@ -534,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             StageCtr ck, cv;  // K tile i, V tile i - 1
             bool ok = mbar_wait(q_full, 0, abort_flag, status, 0x02000000u);
             tc_fence_after();
-            if (u.split) {
+            if (split) {
                 // Both tile slots use Q tile 0; KV tile i goes to slot i % 2.
                 // Issue order QK(i), PV(i-1) keeps one slot's softmax running
                 // while the other slot's MMAs execute.
@@ -569,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Paired tiles: iteration i issues PV_t(i-1) and QK_t(i) for t = 0, 1.
             // Two tiles (the common case): straight-line issue, stage descriptor
             // words advanced in place, ring position tracked only for partials.
-            if (!u.split && T == 2) {
+            if (!split && T == 2) {
                 const uint32_t tS0 = tmem_base, tS1 = tmem_base + 256;
                 const uint32_t q0 = q_lo0, q1 = q_lo0 + kStageLo;
                 const uint32_t k_end = k_lo0 + nK * kStageLo, v_end = v_lo0 + nV * kStageLo;
@@ -624,9 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr int kBlk = C::kBlk;
                 constexpr int nKc = C::kMaxKV, nVc = C::kNVPair;
                 uint32_t kflip = 0, vflip = 0;
-                // (ring prefill only: in the fan-out kernel the unrolled block
-                // measured slower, its split path included)
-                for (; !FAN && ok && i + kBlk <= total; i += kBlk) {
+                // (ring prefill only: the fan-out variants measured slower with it)
+                for (; MODE == kModeRing && ok && i + kBlk <= total; i += kBlk) {
                     const uint32_t kb = k_lo0, vb = v_lo0, qa = q0, qb = q1;
 #pragma unroll
                     for (int pos = 0; pos < kBlk; ++pos) {
@@ -661,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             RingIter wp;  // at iteration i >= 1: tile i-1 (shard openings restart O in partials mode)
             if (!FAN) wp.start(w);
-            for (int i = 0; ok && !u.split && T == 1 && i <= total; ++i) {
+            for (int i = 0; ok && !split && T == 1 && i <= total; ++i) {
                 const bool fresh_prev = (p.partials && !FAN) ? wp.first() : (i == 1);
                 for (int t = 0; t < T && ok; ++t) {
                     const uint32_t tS = tmem_base + t * 256;
@@ -754,16 +761,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         // Walk tiles of this slot: all of them, or every other one in split mode.
-        const int i_step = u.split ? 2 : 1;
+        const int i_step = split ? 2 : 1;
         int jj = 0;  // this slot's tile count so far (barrier phase index)
         TileWalk<FAN> wi;
         wi.start(p, u, w);
-        if (u.split && t == 1) wi.next(p, u);
+        if (split && t == 1) wi.next(p, u);
         int last_shard = FAN ? 0 : wi.ring.j;
-        for (int i = u.split ? t : 0; i < total; i += i_step, ++jj) {
+        for (int i = split ? t : 0; i < total; i += i_step, ++jj) {
             if (jj > 0) {
                 wi.next(p, u);
-                if (u.split) wi.next(p, u);
+                if (split) wi.next(p, u);
             }
             const bool tile_first = !FAN && wi.ring.first();
             const int tile_kb = wi.key();
@@ -771,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // commit that follows its QK (no separate commit)
             uint64_t* s_bar = &s_full[t];
             uint32_t s_par = jj & 1;
-            if (t == 1 && !u.split && T == 2) {
+            if (t == 1 && !split && T == 2) {
                 s_bar = &iter_done[jj % C::kIterRing];
                 s_par = (jj / C::kIterRing) & 1;
             }
@@ -870,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&p_full[t]);
         }
-        if (u.split) {
+        if (split) {
             // The two slots hold online-softmax states of disjoint KV tiles of the
             // same rows.  Slot 1 hands (m, l, O) to slot 0 through shared memory
             // (the KV stages are idle once every MMA has completed), and slot 0
@@ -995,18 +1002,18 @@ bool make_map(CUtensorMap* m, const void* base, const unsigned long long dims[4]
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool FAN>
+template <int D, int MODE>
 cudaError_t launch(const TcParams& p, int grid, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                    const CUtensorMap& k2, const CUtensorMap& v2, cudaStream_t stream) {
     const int smem = Cfg<D>::kSmemBytes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, FAN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (grid <= 0) return cudaSuccess;
-    attn_tc_kernel<D, FAN><<<grid, kThreads, smem, stream>>>(q, k, v, k2, v2, p);
+    attn_tc_kernel<D, MODE><<<grid, kThreads, smem, stream>>>(q, k, v, k2, v2, p);
     return cudaGetLastError();
 }
 
@@ -1037,8 +1044,8 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
     if (!make_map(&tq, a.q, qd, qs, box) || !make_map(&tk, a.k, kd, ks, box) || !make_map(&tv, a.v, kd, ks, box))
         return cudaErrorInvalidValue;
     const int grid = p.n_qtiles * a.B * p.n_head_groups;
-    return a.D == 128 ? launch<128, false>(p, grid, tq, tk, tv, tk, tv, stream)
-                      : launch<64, false>(p, grid, tq, tk, tv, tk, tv, stream);
+    return a.D == 128 ? launch<128, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream)
+                      : launch<64, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream);
 }
 
 int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_prefix, int S_suffix, int* split_prefix,
@@ -1165,8 +1172,15 @@ cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
     }
     const int n_suffix_units = (a.S_suffix > 0 && !p.fold) ? a.n_branches * a.Hkv * p.suffix_mpairs : 0;
     const int grid = p.n_prefix_units + n_suffix_units;
-    return a.D == 128 ? launch<128, true>(p, grid, tq, tk, tv, tk2, tv2, stream)
-                      : launch<64, true>(p, grid, tq, tk, tv, tk2, tv2, stream);
+    // uniform launches (prefix units only) get the variant compiled for their mode
+    if (n_suffix_units == 0 && p.split_prefix)
+        return a.D == 128 ? launch<128, kModeFanSplit>(p, grid, tq, tk, tv, tk2, tv2, stream)
+                          : launch<64, kModeFanSplit>(p, grid, tq, tk, tv, tk2, tv2, stream);
+    if (n_suffix_units == 0)
+        return a.D == 128 ? launch<128, kModeFanPaired>(p, grid, tq, tk, tv, tk2, tv2, stream)
+                          : launch<64, kModeFanPaired>(p, grid, tq, tk, tv, tk2, tv2, stream);
+    return a.D == 128 ? launch<128, kModeFanMixed>(p, grid, tq, tk, tv, tk2, tv2, stream)
+                      : launch<64, kModeFanMixed>(p, grid, tq, tk, tv, tk2, tv2, stream);
 }
 
 unsigned read_clear_status_tc(unsigned* where) {
