@@ -172,25 +172,10 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         u.total = (u.kv_hi - u.kv_lo + kTileN - 1) / kTileN;
         u.unit_row_lo = u.row0[0];
         u.unit_row_hi = min(p.R, u.row0[0] + (u.split ? 1 : 2) * p.rows_per_tile);
-        u.fold_b0 = -1;
-        if (p.fold) {
-            // suffixes of branches chunk, chunk + n_chunks, ... whose rows meet this unit's rows
-            const int s_tiles = (p.S_suffix + kTileN - 1) / kTileN;
-            for (int b = chunk; b < p.n_branches; b += p.n_chunks) {
-                const int lo = p.offsets[b], hi = p.offsets[b + 1];
-                if (lo < 0 || hi < lo || hi > p.R) {
-                    if (threadIdx.x == 0) {
-                        atomicCAS(&g_tc_status[0], 0u, kDevInvalidArg);
-                        atomicCAS(&g_tc_status[1], 0u, 0x0F000000u | static_cast<unsigned>(b));
-                    }
-                    continue;
-                }
-                if (hi > lo && lo < u.unit_row_hi && hi > u.unit_row_lo) {
-                    if (u.fold_b0 < 0) u.fold_b0 = b;
-                    u.total += s_tiles;
-                }
-            }
-        }
+        // First branch whose suffix may fold into this chunk; which ones do
+        // (their rows meet the unit's) needs branch_offsets from memory, read
+        // by fold_tiles() after the launch's first loads are in flight.
+        u.fold_b0 = (p.fold && chunk < p.n_branches) ? chunk : -1;
     } else {
         const int j = idx - p.n_prefix_units;
         mp = j % p.suffix_mpairs;
@@ -232,6 +217,27 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
     return u;
 }
 
+// KV tiles of the suffixes folded into a fan-out prefix unit: branches
+// fold_b0, fold_b0 + n_chunks, ... whose rows meet the unit's rows.  A branch
+// with invalid offsets is skipped and recorded in the status word.
+__device__ int fold_tiles(const TcParams& p, const Unit& u, bool report) {
+    if (u.fold_b0 < 0) return 0;
+    const int s_tiles = (p.S_suffix + kTileN - 1) / kTileN;
+    int n = 0;
+    for (int b = u.fold_b0; b < p.n_branches; b += p.n_chunks) {
+        const int lo = p.offsets[b], hi = p.offsets[b + 1];
+        if (lo < 0 || hi < lo || hi > p.R) {
+            if (report) {
+                atomicCAS(&g_tc_status[0], 0u, kDevInvalidArg);
+                atomicCAS(&g_tc_status[1], 0u, 0x0F000000u | static_cast<unsigned>(b));
+            }
+            continue;
+        }
+        if (hi > lo && lo < u.unit_row_hi && hi > u.unit_row_lo) n += s_tiles;
+    }
+    return n;
+}
+
 // Position in a unit's walk of KV tiles.  Ring prefill: the ring order of
 // ra_walk.h.  Fan-out: the unit's prefix range, then the suffix of every
 // branch folded into it (only that branch's rows see those keys); a suffix
@@ -246,6 +252,7 @@ struct TileWalk {
     int tin, tcount;      // tile within the segment, tiles in it
     int row_lo, row_hi;   // stacked rows that see the segment
     int stride;           // next folded branch: b + stride (0: none)
+    bool more;            // fan-out: the walk has a current tile
 
     __device__ __forceinline__ bool seek_branch(const TcParams& p, const Unit& u, int from) {
         for (int bb = from; stride > 0 && bb < p.n_branches; bb += stride) {
@@ -270,6 +277,7 @@ struct TileWalk {
             ring.start(w);
             return;
         }
+        more = true;
         if (u.suffix) {  // a suffix unit: one branch's suffix, rows = the unit's branch
             seg = 1;
             b = u.kv_z;
@@ -291,6 +299,7 @@ struct TileWalk {
         row_lo = 0;
         row_hi = p.R;
         stride = p.fold ? p.n_chunks : 0;
+        if (tcount == 0) more = u.fold_b0 >= 0 && seek_branch(p, u, u.fold_b0);
     }
     __device__ __forceinline__ void next(const TcParams& p, const Unit& u) {
         if (!fan) {
@@ -300,11 +309,10 @@ struct TileWalk {
         ++tin;
         kb += kTileN;
         if (tin == tcount) {
-            if (seg == 0) {
-                if (u.fold_b0 >= 0) seek_branch(p, u, u.fold_b0);
-            } else {
-                seek_branch(p, u, b + stride);
-            }
+            if (seg == 0)
+                more = u.fold_b0 >= 0 && seek_branch(p, u, u.fold_b0);
+            else
+                more = seek_branch(p, u, b + stride);
         }
     }
     __device__ __forceinline__ int key() const { return fan ? kb : ring.kb; }
@@ -345,6 +353,29 @@ __device__ __forceinline__ void store_row(const OutDesc& out, long long o_base, 
                                  vals[4 * j + 3] * inv_l);
     } else {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out.o) + o_base + chunk * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(pack_bf16x2(vals[8 * j] * inv_l, vals[8 * j + 1] * inv_l),
+                                pack_bf16x2(vals[8 * j + 2] * inv_l, vals[8 * j + 3] * inv_l),
+                                pack_bf16x2(vals[8 * j + 4] * inv_l, vals[8 * j + 5] * inv_l),
+                                pack_bf16x2(vals[8 * j + 6] * inv_l, vals[8 * j + 7] * inv_l));
+    }
+}
+
+// The same values written to a row of shared memory (the final flush stages
+// each row there and hands it to one bulk copy: a thread per row writing its
+// row straight to global memory touches 32 lines per warp instruction).
+template <int D>
+__device__ __forceinline__ void stage_row(const OutDesc& out, uint8_t* srow, int chunk, const float* vals,
+                                          float inv_l) {
+    if (out.o_f32) {
+        float4* dst = reinterpret_cast<float4*>(srow) + chunk * 8;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(vals[4 * j] * inv_l, vals[4 * j + 1] * inv_l, vals[4 * j + 2] * inv_l,
+                                 vals[4 * j + 3] * inv_l);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(srow) + chunk * 4;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             dst[j] = make_uint4(pack_bf16x2(vals[8 * j] * inv_l, vals[8 * j + 1] * inv_l),
@@ -464,6 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int T = u.T;
     unsigned* status = g_tc_status;
+    // Folded suffix tiles extend the walk.  The producers find them as they
+    // walk (their first loads are issued before branch_offsets is read); the
+    // other roles count them here, while those loads are in flight.
+    if (FAN && u.fold_b0 >= 0 && warp != 0 && warp != 2) total += fold_tiles(p, u, threadIdx.x == 32);
 
     // Register split, set inside each role (reg_dec / reg_inc).
 
@@ -496,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             TileWalk<FAN> wi;
             wi.start(p, u, w);
             bool ok = true;
-            for (int i = 0; ok && i < total; ++i, wi.next(p, u)) {
+            for (int i = 0; ok && (FAN ? wi.more : i < total); ++i, wi.next(p, u)) {
                 const bool from_suffix = FAN && wi.seg == 1;
                 const CUtensorMap* map = from_suffix ? map2 : map1;
                 const int z = FAN ? (from_suffix ? wi.b : 0) : u.kv_z;
@@ -739,6 +774,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // Normalise the O accumulator and write it as part `part`, once `done`
         // (if given) shows its last PV complete.
+        // Rows staged in shared memory for the final flush: the K/V stages are
+        // idle once every MMA has completed.  Rows are padded by 16 bytes so
+        // that a warp's 16-byte writes of 32 rows spread over all banks.
+        const int row_bytes = D * (out.o_f32 ? 4 : 2);
+        const int stage_stride = row_bytes + 16;
+        constexpr int kSplitXBytes = (D * 128 + 2 * 128) * 4;  // split combine exchange ahead of the stage
+        uint8_t* srow = kv_smem + (split ? kSplitXBytes : 0) + (t * 128 + lane_row) * stage_stride;
+        bool staged = false;  // a bulk store of this thread is in flight
         auto flush = [&](uint64_t* done, uint32_t phase, int part) -> bool {
             if (done) {
                 if (!mbar_wait(done, phase, abort_flag, status, 0x06000000u)) return false;
@@ -746,12 +789,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
             const long long ob = o_row_base + static_cast<long long>(part) * out.o_part;
+            // the final flush (after `drain`) stages the row; mid-walk flushes
+            // (per-shard partials, K/V stages busy) write it directly
+            const bool stage = (done == drain);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tO + c * 32, r);
                 tmem_wait_ld();
-                if (row_ok) store_row<D>(out, ob, c, reinterpret_cast<const float*>(r), inv_l);
+                if (stage)
+                    stage_row<D>(out, srow, c, reinterpret_cast<const float*>(r), inv_l);
+                else if (row_ok)
+                    store_row<D>(out, ob, c, reinterpret_cast<const float*>(r), inv_l);
+            }
+            if (stage && row_ok) {
+                bulk_store(static_cast<char*>(out.o) + ob * (out.o_f32 ? 4 : 2), srow, row_bytes);
+                staged = true;
             }
             if (row_ok && out.lse) {
                 const float L = l_sum > 0.f ? (m_use + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
@@ -927,7 +980,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float o1 = (a1 != 0.f) ? xo[(c * 32 + j) * 128 + lane_row] : 0.f;
                             v[j] = a0 * __uint_as_float(r[j]) + a1 * o1;
                         }
-                        if (row_ok) store_row<D>(out, ob, c, v, inv);
+                        stage_row<D>(out, srow, c, v, inv);
+                    }
+                    if (row_ok) {
+                        bulk_store(static_cast<char*>(out.o) + ob * (out.o_f32 ? 4 : 2), srow, row_bytes);
+                        staged = true;
                     }
                     if (row_ok && out.lse)
                         out.lse[lse_base + static_cast<long long>(u.slot[0]) * out.lse_part] =
@@ -958,6 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (out.lse) out.lse[lse_base + static_cast<long long>(j) * out.lse_part] = -INFINITY;
             }
         }
+        if (staged) bulk_store_wait();  // the staged rows have left shared memory
         }
         tc_fence_before();
     }
