@@ -779,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // that a warp's 16-byte writes of 32 rows spread over all banks.
         const int row_bytes = D * (out.o_f32 ? 4 : 2);
         const int stage_stride = row_bytes + 16;
-        constexpr int kSplitXBytes = (D * 128 + 2 * 128) * 4;  // split combine exchange ahead of the stage
+        constexpr int kSplitXBytes = (D * 128 + 4 * 128) * 4;  // split combine exchange ahead of the stage
         uint8_t* srow = kv_smem + (split ? kSplitXBytes : 0) + (t * 128 + lane_row) * stage_stride;
         bool staged = false;  // a bulk store of this thread is in flight
         auto flush = [&](uint64_t* done, uint32_t phase, int part) -> bool {
@@ -932,66 +932,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (split) {
             // The two slots hold online-softmax states of disjoint KV tiles of the
-            // same rows.  Slot 1 hands (m, l, O) to slot 0 through shared memory
-            // (the KV stages are idle once every MMA has completed), and slot 0
-            // writes their log-sum-exp combination as the unit's one partial.
-            // Slot 1 always arrives on the named barrier, so slot 0 never blocks.
-            float* xo = reinterpret_cast<float*>(kv_smem);  // [D][128], column-major: conflict-free
-            float* xm = xo + D * 128;
-            float* xl = xm + 128;
-            if (t == 1) {
-                bool have = ok && jj > 0 && mbar_wait(drain, 0, abort_flag, status, 0x09000000u);
-                have = __all_sync(0xffffffffu, have);
-                if (have) {
-                    tc_fence_after();
+            // same rows.  Each slot combines half of the head dims: it hands the
+            // other half of its O (with m and l) to the other slot through shared
+            // memory (the KV stages are idle once every MMA has completed), then
+            // writes the log-sum-exp combination of its half; slot 0 writes lse.
+            // Both slots always meet at the named barrier (an empty or failed
+            // slot offers m = -inf, which the other ignores).
+            constexpr int kHalf = D / 2;
+            float* xo = reinterpret_cast<float*>(kv_smem);  // [2 slots][kHalf][128], column-major: conflict-free
+            float* xm = xo + 2 * kHalf * 128;               // [2][128]
+            float* xl = xm + 2 * 128;                       // [2][128]
+            const int give = t == 0 ? kHalf : 0;            // columns this slot hands over
+            const int keep = t == 0 ? 0 : kHalf;            // columns this slot combines
+            bool have = ok && jj > 0 &&
+                        (t == 0 ? mbar_wait(&o_done[0], (jj - 1) & 1, abort_flag, status, 0x0A000000u | jj)
+                                : mbar_wait(drain, 0, abort_flag, status, 0x09000000u));
+            have = __all_sync(0xffffffffu, have);
+            if (have) {
+                tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(tO + c * 32, r);
-                        tmem_wait_ld();
+                for (int c = 0; c < kHalf / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + give + c * 32, r);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) xo[(c * 32 + j) * 128 + lane_row] = __uint_as_float(r[j]);
-                    }
+                    for (int j = 0; j < 32; ++j) xo[(t * kHalf + c * 32 + j) * 128 + lane_row] = __uint_as_float(r[j]);
                 }
-                xm[lane_row] = have ? m_use : -INFINITY;
-                xl[lane_row] = have ? l_sum : 0.f;
-                asm volatile("bar.arrive 1, 256;" ::: "memory");
-            } else {
-                bool have0 = ok && mbar_wait(&o_done[0], (jj - 1) & 1, abort_flag, status, 0x0A000000u | jj);
-                asm volatile("bar.sync 1, 256;" ::: "memory");
-                have0 = __all_sync(0xffffffffu, have0);
-                if (have0) {
-                    tc_fence_after();
-                    const float m1 = xm[lane_row], l1 = xl[lane_row];
-                    const float m = fmaxf(m_use, m1);
-                    const float a0 = (m_use == -INFINITY) ? 0.f : ex2_approx(m_use - m);
-                    const float a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - m);
-                    const float L = a0 * l_sum + a1 * l1;
-                    const float inv = L > 0.f ? 1.f / L : 0.f;
-                    const long long ob = o_row_base + static_cast<long long>(u.slot[0]) * out.o_part;
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(tO + c * 32, r);
-                        tmem_wait_ld();
-                        float v[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float o1 = (a1 != 0.f) ? xo[(c * 32 + j) * 128 + lane_row] : 0.f;
-                            v[j] = a0 * __uint_as_float(r[j]) + a1 * o1;
-                        }
-                        stage_row<D>(out, srow, c, v, inv);
-                    }
-                    if (row_ok) {
-                        bulk_store(static_cast<char*>(out.o) + ob * (out.o_f32 ? 4 : 2), srow, row_bytes);
-                        staged = true;
-                    }
-                    if (row_ok && out.lse)
-                        out.lse[lse_base + static_cast<long long>(u.slot[0]) * out.lse_part] =
-                            L > 0.f ? (m + log2f(L)) * 0.69314718055994531f : -INFINITY;
-                }
-                ok = have0;
             }
+            xm[t * 128 + lane_row] = have ? m_use : -INFINITY;
+            xl[t * 128 + lane_row] = have ? l_sum : 0.f;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            const float m1 = xm[(t ^ 1) * 128 + lane_row], l1 = xl[(t ^ 1) * 128 + lane_row];
+            const float m0 = have ? m_use : -INFINITY, l0 = have ? l_sum : 0.f;
+            const float m = fmaxf(m0, m1);
+            const float a0 = (m0 == -INFINITY) ? 0.f : ex2_approx(m0 - m);
+            const float a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - m);
+            const float L = a0 * l0 + a1 * l1;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const long long ob = o_row_base + static_cast<long long>(u.slot[0]) * out.o_part + keep;
+            const int half_bytes = kHalf * (out.o_f32 ? 4 : 2);
+            uint8_t* hrow = kv_smem + kSplitXBytes + (t * 128 + lane_row) * (half_bytes + 16);
+#pragma unroll
+            for (int c = 0; c < kHalf / 32; ++c) {
+                uint32_t r[32];
+                if (have) {
+                    tmem_ld32(tO + keep + c * 32, r);
+                    tmem_wait_ld();
+                }
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float o0 = have ? __uint_as_float(r[j]) : 0.f;
+                    const float o1 = (a1 != 0.f) ? xo[((t ^ 1) * kHalf + c * 32 + j) * 128 + lane_row] : 0.f;
+                    v[j] = a0 * o0 + a1 * o1;
+                }
+                stage_row<D>(out, hrow, c, v, inv);
+            }
+            if (row_ok) {
+                bulk_store(static_cast<char*>(out.o) + ob * (out.o_f32 ? 4 : 2), hrow, half_bytes);
+                staged = true;
+            }
+            if (t == 0 && row_ok && out.lse)
+                out.lse[lse_base + static_cast<long long>(u.slot[0]) * out.lse_part] =
+                    L > 0.f ? (m + log2f(L)) * 0.69314718055994531f : -INFINITY;
         } else if (ok) {
             // the last PV: every MMA of the CTA is complete once `drain` is
             if (!FAN && p.partials) {
