@@ -1167,7 +1167,9 @@ void fanout_chunking(int R, int S_prefix, int S_suffix, int n_branches, int Hq, 
     for (int c = 1; c <= max_c; ++c) {
         const long long units = static_cast<long long>(Hkv) * n_mpairs * c;
         const long long waves = (units + n_sm - 1) / n_sm;
-        const double cost = waves * (work / c + 2.0) + 1e-3 * c;  // + per-unit fixed cost
+        // + per-unit fixed cost (first loads from HBM, epilogue, partial written
+        // and merged), measured at about ten tiles of work
+        const double cost = waves * (work / c + 10.0) + 1e-3 * c;
         if (best < 0 || cost < best) {
             best = cost;
             best_c = c;
