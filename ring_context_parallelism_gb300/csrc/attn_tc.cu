@@ -845,19 +845,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l_sum = 0.f;
             }
             if (!FAN) last_shard = wi.ring.j;
-            uint32_t sr[kTileN];
-#pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
-            tmem_wait_ld();
             // visible columns of this tile: c <= lim (only diagonal and tail tiles mask)
             int lim = kTileN - 1;
             if (!FAN) {
                 if (p.causal) lim = min(lim, row - tile_kb);
             } else {
                 lim = min(lim, wi.key_end - 1 - tile_kb);
-                if (row < wi.row_lo || row >= wi.row_hi) lim = -1;  // a folded suffix of another branch
+                // rows of another branch (a folded suffix) or past the stacked rows
+                if (row < wi.row_lo || row >= wi.row_hi) lim = -1;
             }
-            if (lim < kTileN - 1) {
+            if (FAN && __all_sync(0xffffffffu, lim < 0)) {
+                // No row of this warp sees a key of this tile: P = 0 (written over
+                // S, after the QK above has landed) and the running state stays.
+                const uint32_t z = 0;
+#pragma unroll
+                for (int c0 = 0; c0 < kTileN; c0 += 32)
+                    asm volatile(
+                        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                        "{%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};" ::"r"(tS + c0 / 2),
+                        "r"(z)
+                        : "memory");
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&p_full[t]);
+                continue;
+            }
+            uint32_t sr[kTileN];
+#pragma unroll
+            for (int c = 0; c < kTileN / 32; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
+            tmem_wait_ld();
+            // A row that sees no key of this tile keeps its state and gets P = 0
+            // through the exponent (scale 0, offset -inf) rather than a masking
+            // pass; only partially visible rows (diagonal, segment tails) mask.
+            const bool dead_row = lim < 0;
+            if (lim < kTileN - 1 && !dead_row) {
 #pragma unroll
                 for (int c = 0; c < kTileN; ++c)
                     if (c > lim) sr[c] = 0xff800000u;  // -inf
@@ -870,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int q = 0; q < 4; ++q)
                     m4[q] = fmax3(m4[q], __uint_as_float(sr[c + 2 * q]), __uint_as_float(sr[c + 2 * q + 1]));
             }
-            const float mraw = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+            const float mraw = dead_row ? -INFINITY : fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
             const float mx = mraw * p.scale_log2;  // scores in log2 units
             const bool fresh = (jj == 0) || (p.partials && tile_first);
             float alpha = 1.f;
@@ -883,8 +904,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_use = mx;
                 resc = true;
             }
-            const float neg_ms = (m_use == -INFINITY) ? 0.f : -m_use;
-            const float sc = p.scale_log2;
+            const float neg_ms = dead_row ? -INFINITY : ((m_use == -INFINITY) ? 0.f : -m_use);
+            const float sc = dead_row ? 0.f : p.scale_log2;
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
             for (int c0 = 0; c0 < kTileN; c0 += 32) {
