@@ -92,6 +92,9 @@ BF16_CASES = [
     (1, 1024, 8, 2, 128, 8, 64, True),      # block 64 walked as 128-key tiles
     (2, 256, 2, 2, 64, 1, 128, False),
     (1, 2048, 4, 1, 128, 16, 128, True),    # one tile per shard
+    (1, 2048, 4, 2, 64, 4, 128, True),      # D = 64 walks long enough for the unrolled issue block
+    (1, 1536, 2, 1, 64, 3, 128, False),
+    (1, 2304, 6, 2, 128, 3, 128, True),     # odd group (3): one head per CTA, 18-tile walks
 ]
 
 
@@ -155,6 +158,28 @@ def test_ring_partials_and_merge(dtype, causal):
     tO, tL = TOL[dtype]
     L = S // N
     for j in range(N):
+        rO, rL = _oracle_full(q, k, v, causal, kv_range=(j * L, (j + 1) * L))
+        _close(pO[j].float().cpu().double().numpy(), rO, tO, f"partial O[{j}]")
+        _close(pL[j].cpu().double().numpy(), rL, tL, f"partial lse[{j}]")
+    mO, mL = ra.lse_merge(pO, pL)
+    ra.device_status()
+    rO, rL = _oracle_full(q, k, v, causal)
+    _close(mO.float().cpu().double().numpy(), rO, tO, "merged O")
+    _close(mL.cpu().double().numpy(), rL, tL, "merged lse")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_ring_partials_d64_long(causal):
+    """D = 64 partials over walks long enough for the unrolled issue block, shard openings inside it."""
+    S, N = 2048, 8
+    w = small(WORKLOADS["gqa_causal_prefill_32k"], B=1, S=S, Hq=4, Hkv=2, D=64, n_shards=N, block=128,
+              causal=causal, seed=37)
+    q, k, v = attention_inputs(w, "cpu")
+    pO, pL = ra.ring_partials(q.cuda(), k.cuda(), v.cuda(), N, w.block, causal)
+    ra.device_status()
+    tO, tL = TOL["bf16"]
+    L = S // N
+    for j in (0, 3, N - 1):
         rO, rL = _oracle_full(q, k, v, causal, kv_range=(j * L, (j + 1) * L))
         _close(pO[j].float().cpu().double().numpy(), rO, tO, f"partial O[{j}]")
         _close(pL[j].cpu().double().numpy(), rL, tL, f"partial lse[{j}]")
@@ -262,6 +287,9 @@ def _oracle_fanout(x, sel=None):
     (640, 128, [33, 5], 8, 2, 64),                 # a branch with more rows than one tile pair
     (0, 300, [2, 9], 8, 1, 128),                   # no shared prefix
     (2048, 0, [4, 4, 4], 16, 4, 64),               # no private suffix
+    (3000, 256, [16, 16, 16], 64, 8, 128),         # last row pair holds a single row tile
+    (1500, 100, [40, 40, 16], 16, 4, 64),          # the same with D = 64
+    (2500, 384, [5, 4, 6, 2, 9, 1, 7, 3, 8, 2, 10, 6, 4, 11, 3, 12, 5], 64, 8, 128),  # R = 98, 17 branches
 ])
 def test_fanout_full(Sp, Ss, rows, Hq, Hkv, D):
     w = small(WORKLOADS["fanout_decode"], S_prefix=Sp, S_suffix=Ss, n_branches=len(rows), Hq=Hq, Hkv=Hkv, D=D,
@@ -308,7 +336,10 @@ def test_fanout_decode_full_size():
     w = WORKLOADS["fanout_decode"]
     x, O, L = _run_fanout(w)
     R, Hq = x["R"], w.Hq
-    ids = torch.randperm(R * Hq, generator=torch.Generator().manual_seed(4))[:384].sort().values.numpy()
+    # 384 random (row, head) pairs plus every head of the rows in the last, partly filled row tile
+    tail = torch.arange(((R - 1) // 16) * 16 * Hq, R * Hq)
+    ids = torch.cat([torch.randperm(R * Hq, generator=torch.Generator().manual_seed(4))[:384], tail])
+    ids = torch.unique(ids).numpy()
     rO, rL = _oracle_fanout(x, sel=ids)
     _close(O.reshape(-1, w.D).float().cpu().numpy()[ids], rO, 2e-2, "O (sampled)")
     _close(L.t().reshape(-1).cpu().numpy()[ids], rL, 1e-3, "lse (sampled)")
