@@ -39,8 +39,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, valid only while the kernel source hashes to the recorded value.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the timed 32768-token configuration
-    # (bench.py --profile-case prefill_32k, third launch): 403342848 read + 239900928 written
-    "6cf4dd6555b4dbbd": 643243776,
+    # (bench.py --profile-case prefill_32k, third launch): 402892800 read + 242887168 written
+    "cb3b4188d4885b12": 645779968,
 }
 
 
