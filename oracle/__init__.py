@@ -59,7 +59,7 @@ def use_library(path: str | None):
 
 def _bind(lib):
     vp, i, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
-    lib.oracle_attention.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, i, vp, i64, vp, vp]
+    lib.oracle_attention.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, i, i, vp, i64, vp, vp]
     lib.oracle_attention.restype = i
     lib.oracle_fanout.argtypes = [vp, vp, i, i, vp, vp, i, vp, vp, i, i, i, i, i, vp, i64, vp, vp]
     lib.oracle_fanout.restype = i
@@ -97,13 +97,15 @@ def _ptr(a: np.ndarray | None):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def attention(q, k, v, *, dtype: str, causal: bool, kv_range=None, sel=None):
+def attention(q, k, v, *, dtype: str, causal: bool, kv_range=None, sel=None, pos=None):
     """Materialised softmax attention in fp64.
 
     Follows "RingAttention and Context Parallelism: Mathematical Foundations",
     section 1 (A = softmax(QK^T/sqrt(d_k) + M) V), section 5 (causal j <= i) and
     section 7 (L = m + ln l, natural log).  GQA: q head h reads kv head
-    h // (Hq // Hkv).
+    h // (Hq // Hkv).  ``pos`` (int32 [S], optional): sequence position of each
+    stored row, for rows kept in a striped or zigzag shard layout (section 5);
+    the causal mask then compares positions, pos[key] <= pos[query].
 
     q [B,S,Hq,D], k/v [B,S,Hkv,D] as numpy arrays in storage form (float32,
     float64, or uint16 bit patterns for bf16).  ``kv_range=(lo, hi)`` restricts
@@ -116,6 +118,9 @@ def attention(q, k, v, *, dtype: str, causal: bool, kv_range=None, sel=None):
     Hkv = k.shape[2]
     assert k.shape == (B, S, Hkv, D) and v.shape == k.shape
     lo, hi = kv_range if kv_range is not None else (0, S)
+    if pos is not None:
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        assert pos.shape == (S,)
     if sel is not None:
         sel = np.ascontiguousarray(sel, dtype=np.int64)
         out = np.empty((sel.size, D), np.float64)
@@ -124,7 +129,7 @@ def attention(q, k, v, *, dtype: str, causal: bool, kv_range=None, sel=None):
         out = np.empty((B, S, Hq, D), np.float64)
         lse = np.empty((B, Hq, S), np.float64)
     rc = _load().oracle_attention(_ptr(q), _ptr(k), _ptr(v), DTYPES[dtype], B, S, Hq, Hkv, D,
-                                  int(bool(causal)), int(lo), int(hi), _ptr(sel),
+                                  int(bool(causal)), _ptr(pos), int(lo), int(hi), _ptr(sel),
                                   0 if sel is None else sel.size, _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_attention rejected its arguments")

@@ -16,7 +16,9 @@
  *     the concatenated sequence (the exactness identity after the online-softmax
  *     equations).
  *   - Causal masking on global positions: token i sees keys j <= i (same page,
- *     section 5, first paragraph).
+ *     section 5, first paragraph).  Rows may be stored out of sequence order
+ *     (the striped and zigzag shard layouts of section 5): then pos[r] gives the
+ *     sequence position of stored row r and the mask compares positions.
  *   - The log-sum-exp statistic L = m + ln(l) kept for the backward pass (same
  *     page, section 7, "RingAttention backward pass logic" figure), which is the
  *     natural log of sum_j exp(s_j).
@@ -125,13 +127,15 @@ static double softmax_row(const double* q_row, const key_ref* keys, int64_t n, i
 /*
  * Attention for the queries listed in `sel` (or every query when sel == NULL).
  *   q [B,S,Hq,D], k/v [B,S,Hkv,D] in `dtype`.
- *   Visible keys of query (b,i,h): j in [kv_begin, kv_end) and, if causal, j <= i.
+ *   Visible keys of query (b,i,h): j in [kv_begin, kv_end) and, if causal,
+ *   pos[j] <= pos[i] (pos == NULL: the stored order is the sequence order,
+ *   pos[r] = r).
  *   sel ids encode (b,i,h) as (b*S + i)*Hq + h.
  *   sel == NULL: out [B,S,Hq,D], lse [B,Hq,S].  Otherwise out [n_sel,D], lse [n_sel].
  * Returns 0, or -1 on bad arguments.
  */
 int oracle_attention(const void* q, const void* k, const void* v, int dtype,
-                     int B, int S, int Hq, int Hkv, int D, int causal,
+                     int B, int S, int Hq, int Hkv, int D, int causal, const int32_t* pos,
                      int kv_begin, int kv_end, const int64_t* sel, int64_t n_sel,
                      double* out, double* lse) {
     if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv) return -1;
@@ -172,7 +176,12 @@ int oracle_attention(const void* q, const void* k, const void* v, int dtype,
 #else
             if (causal && i + 1 < hi) hi = i + 1;
 #endif
-            for (int j = kv_begin; j < hi; ++j) {
+            for (int j = kv_begin; j < (pos ? kv_end : hi); ++j) {
+#if ORACLE_MUTANT == 8
+                if (pos && causal && j > i) continue; /* mutant: mask on stored order, not positions */
+#else
+                if (pos && causal && pos[j] > pos[i]) continue;
+#endif
                 keys[n].k = k;
                 keys[n].v = v;
                 keys[n].off = (((int64_t)b * S + j) * Hkv + hk) * D;

@@ -5,6 +5,7 @@ import os
 import pytest
 
 import oracle
+import test_layouts as layouts
 import test_oracle_pins as pins
 
 PINS = [
@@ -16,6 +17,7 @@ PINS = [
     pins.test_lse_gradient_is_attention_over_keys,
     lambda: pins.test_shard_partials_merge_to_unsharded(True),
     pins.test_fanout_equals_per_branch_attention_over_prefix_plus_suffix,
+    lambda: layouts.test_oracle_on_stored_layout_equals_sequence_order("zigzag"),
 ]
 
 MUTANTS = {
@@ -26,6 +28,7 @@ MUTANTS = {
     5: "scores against V instead of K",
     6: "last visible key dropped",
     7: "merge forgets to normalise",
+    8: "causal mask on the stored order instead of sequence positions",
 }
 
 
