@@ -53,6 +53,24 @@ typedef enum {
 typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
 
 /*
+ * Shard layouts: how the rows of q/k/v/out are arranged over the n_shards ring
+ * shards ("RingAttention and Context Parallelism: Mathematical Foundations",
+ * section 5).  Shard s holds storage rows [s*L, (s+1)*L), L = S / n_shards; the
+ * layout fixes the sequence position of each row, which is what the causal mask
+ * compares (query at position i sees keys at positions j <= i):
+ *   RA_LAYOUT_CONTIGUOUS  shard s holds tokens [s*L, (s+1)*L) in order.
+ *   RA_LAYOUT_ZIGZAG      the sequence is cut into 2N chunks c_0..c_{2N-1} of
+ *                         L/2 tokens; shard s holds c_s then c_{2N-1-s}
+ *                         (zigzag ring attention: one early and one late chunk
+ *                         per shard, which balances the causal work).
+ *   RA_LAYOUT_STRIPED     shard s holds the tokens i with i mod N = s, in
+ *                         increasing order (striped attention).
+ * Without a causal mask the layout changes nothing: output row p is the
+ * attention of query row p over every key row.
+ */
+typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_ZIGZAG = 1, RA_LAYOUT_STRIPED = 2 } ra_layout;
+
+/*
  * Blockwise exact attention with online softmax, KV walked in ring order.
  *
  * Defined by "RingAttention and Context Parallelism: Mathematical Foundations":
@@ -80,6 +98,23 @@ ra_status ra_blockwise_attn_fwd(const void* q, const void* k, const void* v, voi
                                 int causal, ra_dtype dt, void* stream);
 
 /*
+ * ra_blockwise_attn_fwd for rows stored in a zigzag or striped shard layout
+ * (ra_layout above; same page, section 5).  q/k/v/out/lse are indexed by
+ * storage row; the causal mask compares the rows' sequence positions.  Each
+ * query tile walks the KV shards in the same ring order, taking from each
+ * shard the prefix of its rows that the tile can see (positions increase
+ * along a shard's rows in every layout).
+ *   layout : an ra_layout value.  RA_LAYOUT_ZIGZAG needs an even shard length,
+ *            and (S / n_shards / 2) % 128 == 0 on the bf16 path, % 32 == 0 on
+ *            the fp32 path.
+ * Other arguments and errors as ra_blockwise_attn_fwd; layout = RA_LAYOUT_CONTIGUOUS
+ * is that call.
+ */
+ra_status ra_blockwise_attn_fwd_layout(const void* q, const void* k, const void* v, void* out, float* lse,
+                                       int B, int S, int Hq, int Hkv, int D, int n_shards, int block,
+                                       int causal, int layout, ra_dtype dt, void* stream);
+
+/*
  * Per-shard partial states: the same ring walk, but the state is normalised and
  * written out after every KV shard instead of being carried across shards --
  * the per-shard partials that the "AHBM Agentic Runtime Architecture" page
@@ -95,6 +130,17 @@ ra_status ra_blockwise_attn_fwd(const void* q, const void* k, const void* v, voi
 ra_status ra_ring_partials_fwd(const void* q, const void* k, const void* v, void* partials_O,
                                float* partials_lse, int B, int S, int Hq, int Hkv, int D,
                                int n_shards, int block, int causal, ra_dtype dt, void* stream);
+
+/*
+ * ra_ring_partials_fwd for a zigzag or striped shard layout: partial j holds
+ * the attention of every query row over the key rows of storage shard j under
+ * the layout's causal mask; a row that sees none of them gets O = 0,
+ * lse = -inf.  Arguments as ra_blockwise_attn_fwd_layout.
+ */
+ra_status ra_ring_partials_fwd_layout(const void* q, const void* k, const void* v, void* partials_O,
+                                      float* partials_lse, int B, int S, int Hq, int Hkv, int D,
+                                      int n_shards, int block, int causal, int layout, ra_dtype dt,
+                                      void* stream);
 
 /*
  * Row-indexed log-sum-exp merge of P partial states computed over disjoint key
@@ -192,6 +238,26 @@ ra_status ra_prefix_fanout_attn_noalloc(const void* q_rows, const int* branch_of
  * shard_order must hold n_shards ints.
  */
 int ra_ring_shard_order(int S, int n_shards, int causal, int q_row0, int* shard_order);
+
+/*
+ * Host-side (no GPU): pos[p] = sequence position of storage row p under
+ * `layout` (ra_layout) for S rows in n_shards shards.  pos holds S ints.
+ * Returns 0, or -1 on invalid arguments (zigzag needs an even shard length).
+ */
+int ra_layout_positions(int S, int n_shards, int layout, int* pos);
+
+/*
+ * Host-side view of the walk of one query tile under a layout: the query rows
+ * [q_row0, q_row0 + q_rows) (inside one shard; for zigzag inside one half of
+ * it), KV tiles of `tile` keys.  Writes, for each visited shard in ring order,
+ * shard_order[t] and visible_keys[t] (the keys of that shard the tile's last
+ * row can see, a prefix of the shard's rows; the shard length when not
+ * causal), and *total_tiles = the KV tiles the kernels walk for this tile.
+ * Shards after the returned count see nothing.  Arrays hold n_shards ints.
+ * Returns the number of visited shards, or -1 on invalid arguments.
+ */
+int ra_ring_walk_layout(int S, int n_shards, int causal, int layout, int q_row0, int q_rows, int tile,
+                        int* shard_order, int* visible_keys, int* total_tiles);
 
 /* Synchronises `stream`, then returns and clears the device status word:
  * RA_OK, RA_ERR_DEVICE_TIMEOUT or RA_ERR_INVALID_ARG (device-side check), or

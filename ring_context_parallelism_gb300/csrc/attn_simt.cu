@@ -27,7 +27,7 @@ constexpr int kChunk = 32;  // keys staged per step
 
 struct SimtParams {
     const float *q, *k, *v;
-    int B, S, Hq, Hkv, n_shards, block, causal, partials, n_qtiles;
+    int B, S, Hq, Hkv, n_shards, block, causal, partials, n_qtiles, layout;
     float scale;
     OutDesc out;
 };
@@ -47,11 +47,11 @@ __global__ void __launch_bounds__(kRows * (D / 32)) attn_simt_kernel(const SimtP
     const int rem = idx % groups;
     const int b = rem / p.Hq;
     const int h = rem % p.Hq;
-    const int qt = p.causal ? p.n_qtiles - 1 - qt_rev : qt_rev;
-    const int r0 = qt * kRows;
+    const int r0 = p.causal ? heavy_tile_row0(p.layout, p.S, p.n_shards, kRows, qt_rev) : qt_rev * kRows;
     const int row = r0 + r_local;
     const int hk = h / (p.Hq / p.Hkv);
     const int L = p.S / p.n_shards;
+    const int row_pos = layout_pos(p.layout, L, p.n_shards, row);  // sequence position (causal mask)
 
     float q[32], o[32];
     const float* qp = p.q + ((static_cast<long long>(b) * p.S + row) * p.Hq + h) * D + sub;
@@ -76,12 +76,12 @@ __global__ void __launch_bounds__(kRows * (D / 32)) attn_simt_kernel(const SimtP
             out.lse[lse_base + static_cast<long long>(part) * out.lse_part] = l > 0.f ? m + logf(l) : -INFINITY;
     };
 
-    const RingWalk w = make_ring_walk(p.S, p.n_shards, kRows, p.causal, r0, kRows);
+    const RingWalk w = make_ring_walk(p.S, p.n_shards, kRows, p.causal, r0, kRows, p.layout);
     for (int t = 0; t < w.n_visited; ++t) {
         const int j = ring_shard_at(w, t);
         const int key_lo = j * L;
-        int key_hi = key_lo + L;
-        if (p.causal && j == w.k) key_hi = min(key_hi, r0 + kRows);
+        // causal: the prefix of the shard the tile's last row can see
+        const int key_hi = key_lo + (p.causal ? shard_visible(p.layout, L, p.n_shards, j, w.maxpos) : L);
         for (int blk = key_lo; blk < key_hi; blk += p.block) {
             const int blk_hi = min(blk + p.block, key_hi);
             for (int c0 = blk; c0 < blk_hi; c0 += kChunk) {
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kRows * (D / 32)) attn_simt_kernel(const SimtP
                     for (int d = 0; d < 32; ++d) acc = fmaf(q[d], ks[c][d * TPR + sub], acc);
 #pragma unroll
                     for (int x = 1; x < TPR; x <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
-                    const bool vis = c < n && (!p.causal || c0 + c <= row);
+                    const bool vis = c < n && (!p.causal || layout_pos(p.layout, L, p.n_shards, c0 + c) <= row_pos);
                     s[c] = vis ? acc * p.scale : -INFINITY;
                     mx = fmaxf(mx, s[c]);
                 }
@@ -160,6 +160,7 @@ cudaError_t launch_ring_simt(const RingSimtArgs& a, cudaStream_t stream) {
     p.block = a.block;
     p.causal = a.causal;
     p.partials = a.partials;
+    p.layout = a.layout;
     p.n_qtiles = a.S / kRows;
     p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(a.D)));
     p.out = a.out;

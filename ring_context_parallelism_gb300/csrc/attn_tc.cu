@@ -51,6 +51,7 @@ struct TcParams {
     int fanout;     // 0 ring prefill, 1 fan-out
     int partials;   // ring: one partial per KV shard
     int causal;
+    int layout;     // ring: shard layout (ra_walk.h), used when causal
     int T2;         // ring: two heads per CTA (GQA group size even)
     // ring
     int B, S, Hq, Hkv, n_shards, n_qtiles, n_head_groups;
@@ -132,8 +133,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         const int qt_rev = rem / hg_per_kv;
         u.b = g / p.Hkv;
         const int hg = (g - u.b * p.Hkv) * hg_per_kv + (rem - qt_rev * hg_per_kv);
-        const int qt = p.causal ? p.n_qtiles - 1 - qt_rev : qt_rev;
-        u.q_row0 = qt * kTileM;
+        u.q_row0 = p.causal ? heavy_tile_row0(p.layout, p.S, p.n_shards, kTileM, qt_rev) : qt_rev * kTileM;
         u.T = p.T2 ? 2 : 1;
         for (int t = 0; t < 2; ++t) {
             u.head[t] = hg * u.T + (t < u.T ? t : 0);
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     RingWalk w{};
     int total;
     if (!FAN) {
-        w = make_ring_walk(p.S, p.n_shards, kTileN, p.causal, u.q_row0, kTileM);
+        w = make_ring_walk(p.S, p.n_shards, kTileN, p.causal, u.q_row0, kTileM, p.layout);
         total = w.total;
     } else {
         total = u.total;
@@ -771,6 +771,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         float m_use = -INFINITY, l_sum = 0.f;
         bool ok = true;
+        // zigzag / striped causal walks: this row's sequence position
+        const int shard_len = FAN ? 0 : p.S / p.n_shards;
+        const int row_pos = (FAN || p.layout == kLayoutContiguous) ? row : layout_pos(p.layout, shard_len, p.n_shards, row);
 
         // Normalise the O accumulator and write it as part `part`, once `done`
         // (if given) shows its last PV complete.
@@ -848,7 +851,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // visible columns of this tile: c <= lim (only diagonal and tail tiles mask)
             int lim = kTileN - 1;
             if (!FAN) {
-                if (p.causal) lim = min(lim, row - tile_kb);
+                // keys of this tile the row sees: a prefix of the tile (positions
+                // increase along a shard), ending where the shard's visible keys end
+                if (p.causal)
+                    lim = min(lim, p.layout == kLayoutContiguous
+                                       ? row - tile_kb
+                                       : shard_visible(p.layout, shard_len, p.n_shards, wi.ring.j, row_pos) -
+                                             (tile_kb - wi.ring.j * shard_len) - 1);
             } else {
                 lim = min(lim, wi.key_end - 1 - tile_kb);
                 // rows of another branch (a folded suffix) or past the stacked rows
@@ -1106,6 +1115,7 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
     p.fanout = 0;
     p.partials = a.partials;
     p.causal = a.causal;
+    p.layout = a.layout;
     p.B = a.B;
     p.S = a.S;
     p.Hq = a.Hq;

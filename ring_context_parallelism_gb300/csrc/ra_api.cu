@@ -43,7 +43,7 @@ int sm_count() {
 
 // Checks shared by the fused and partial ring entry points.
 ra_status check_ring(const void* q, const void* k, const void* v, const void* out, int B, int S, int Hq, int Hkv,
-                     int D, int n_shards, int block, int causal, ra_dtype dt) {
+                     int D, int n_shards, int block, int causal, ra_dtype dt, int layout) {
     if (!q || !k || !v || !out) return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return fail(RA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
@@ -54,6 +54,13 @@ ra_status check_ring(const void* q, const void* k, const void* v, const void* ou
     const int L = S / n_shards;
     if (block < 1 || L % block) return fail(RA_ERR_INVALID_ARG, "shard length %d %% block %d != 0", L, block);
     if (causal != 0 && causal != 1) return fail(RA_ERR_INVALID_ARG, "causal must be 0 or 1");
+    if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIPED)
+        return fail(RA_ERR_INVALID_ARG, "unknown layout %d", layout);
+    if (layout == RA_LAYOUT_ZIGZAG && L % 2)
+        return fail(RA_ERR_INVALID_ARG, "zigzag layout needs an even shard length (got %d)", L);
+    const int tile = dt == RA_BF16 ? 128 : 32;  // query rows / keys per tile of the kernels
+    if (layout == RA_LAYOUT_ZIGZAG && (L / 2) % tile)
+        return fail(RA_ERR_UNSUPPORTED, "zigzag layout needs (shard length / 2) %% %d == 0 (got %d)", tile, L / 2);
     if (dt == RA_BF16) {
         if (L % 128) return fail(RA_ERR_UNSUPPORTED, "bf16 path needs shard length %% 128 == 0 (got %d)", L);
         if (block != 64 && block % 128)
@@ -69,8 +76,9 @@ ra_status check_ring(const void* q, const void* k, const void* v, const void* ou
 }
 
 ra_status ring_common(const void* q, const void* k, const void* v, void* out, float* lse, int B, int S, int Hq,
-                      int Hkv, int D, int n_shards, int block, int causal, ra_dtype dt, void* stream, int partials) {
-    ra_status st = check_ring(q, k, v, out, B, S, Hq, Hkv, D, n_shards, block, causal, dt);
+                      int Hkv, int D, int n_shards, int block, int causal, ra_dtype dt, void* stream, int partials,
+                      int layout) {
+    ra_status st = check_ring(q, k, v, out, B, S, Hq, Hkv, D, n_shards, block, causal, dt, layout);
     if (st != RA_OK) return st;
     if (lse && !aligned16(lse)) return fail(RA_ERR_INVALID_ARG, "lse must be 16-byte aligned");
     ra::OutDesc od;
@@ -88,10 +96,12 @@ ra_status ring_common(const void* q, const void* k, const void* v, void* out, fl
     cudaError_t e;
     if (dt == RA_BF16) {
         ra::RingTcArgs a{q, k, v, B, S, Hq, Hkv, D, n_shards, causal, partials, od};
+        a.layout = layout;
         e = ra::launch_ring_tc(a, s);
     } else {
         ra::RingSimtArgs a{static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
                            B, S, Hq, Hkv, D, n_shards, block, causal, partials, od};
+        a.layout = layout;
         e = ra::launch_ring_simt(a, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, partials ? "ring partials launch" : "ring attention launch");
@@ -200,14 +210,30 @@ extern "C" {
 ra_status ra_blockwise_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int S,
                                 int Hq, int Hkv, int D, int n_shards, int block, int causal, ra_dtype dt,
                                 void* stream) {
-    return ring_common(q, k, v, out, lse, B, S, Hq, Hkv, D, n_shards, block, causal, dt, stream, 0);
+    return ring_common(q, k, v, out, lse, B, S, Hq, Hkv, D, n_shards, block, causal, dt, stream, 0,
+                       RA_LAYOUT_CONTIGUOUS);
+}
+
+ra_status ra_blockwise_attn_fwd_layout(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                                       int S, int Hq, int Hkv, int D, int n_shards, int block, int causal,
+                                       int layout, ra_dtype dt, void* stream) {
+    return ring_common(q, k, v, out, lse, B, S, Hq, Hkv, D, n_shards, block, causal, dt, stream, 0, layout);
 }
 
 ra_status ra_ring_partials_fwd(const void* q, const void* k, const void* v, void* partials_O, float* partials_lse,
                                int B, int S, int Hq, int Hkv, int D, int n_shards, int block, int causal,
                                ra_dtype dt, void* stream) {
     if (!partials_lse) return fail(RA_ERR_INVALID_ARG, "partials_lse must not be NULL");
-    return ring_common(q, k, v, partials_O, partials_lse, B, S, Hq, Hkv, D, n_shards, block, causal, dt, stream, 1);
+    return ring_common(q, k, v, partials_O, partials_lse, B, S, Hq, Hkv, D, n_shards, block, causal, dt, stream, 1,
+                       RA_LAYOUT_CONTIGUOUS);
+}
+
+ra_status ra_ring_partials_fwd_layout(const void* q, const void* k, const void* v, void* partials_O,
+                                      float* partials_lse, int B, int S, int Hq, int Hkv, int D, int n_shards,
+                                      int block, int causal, int layout, ra_dtype dt, void* stream) {
+    if (!partials_lse) return fail(RA_ERR_INVALID_ARG, "partials_lse must not be NULL");
+    return ring_common(q, k, v, partials_O, partials_lse, B, S, Hq, Hkv, D, n_shards, block, causal, dt, stream, 1,
+                       layout);
 }
 
 ra_status ra_lse_merge(const void* partials_O, const float* partials_lse, void* out, float* out_lse, int P, int B,
@@ -341,6 +367,38 @@ int ra_ring_shard_order(int S, int n_shards, int causal, int q_row0, int* shard_
     if (S < 1 || n_shards < 1 || S % n_shards || q_row0 < 0 || q_row0 >= S || !shard_order) return -1;
     const ra::RingWalk w = ra::make_ring_walk(S, n_shards, 1, causal ? 1 : 0, q_row0, 1);
     for (int t = 0; t < w.n_visited; ++t) shard_order[t] = ra::ring_shard_at(w, t);
+    return w.n_visited;
+}
+
+int ra_layout_positions(int S, int n_shards, int layout, int* pos) {
+    if (S < 1 || n_shards < 1 || S % n_shards || !pos) return -1;
+    if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIPED) return -1;
+    const int L = S / n_shards;
+    if (layout == RA_LAYOUT_ZIGZAG && L % 2) return -1;
+    for (int p = 0; p < S; ++p) pos[p] = ra::layout_pos(layout, L, n_shards, p);
+    return 0;
+}
+
+int ra_ring_walk_layout(int S, int n_shards, int causal, int layout, int q_row0, int q_rows, int tile,
+                        int* shard_order, int* visible_keys, int* total_tiles) {
+    if (S < 1 || n_shards < 1 || S % n_shards || !shard_order || !visible_keys || !total_tiles) return -1;
+    if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIPED) return -1;
+    const int L = S / n_shards;
+    const int span = layout == RA_LAYOUT_ZIGZAG ? L / 2 : L;  // a query tile stays inside one span
+    if (layout == RA_LAYOUT_ZIGZAG && L % 2) return -1;
+    if (tile < 1 || span % tile || q_rows < 1 || q_row0 < 0 || q_row0 + q_rows > S) return -1;
+    if (q_row0 / span != (q_row0 + q_rows - 1) / span) return -1;
+    const ra::RingWalk w = ra::make_ring_walk(S, n_shards, tile, causal ? 1 : 0, q_row0, q_rows, layout);
+    ra::RingIter it;
+    it.start(w);
+    for (int t = 0; t < w.n_visited; ++t) {
+        // the iterator's shard sequence, and the keys of each shard the last query row sees
+        shard_order[t] = it.j;
+        visible_keys[t] = causal ? ra::shard_visible(layout, L, n_shards, it.j, w.maxpos) : L;
+        const int n = it.count;
+        for (int i = 0; i < n; ++i) it.next();
+    }
+    *total_tiles = w.total;
     return w.n_visited;
 }
 

@@ -24,6 +24,7 @@ struct RingTcArgs {
     const void *q, *k, *v;
     int B, S, Hq, Hkv, D, n_shards, causal, partials;
     OutDesc out;
+    int layout = 0;  // shard layout of the rows (ra_walk.h kLayout*)
 };
 cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream);
 
@@ -65,6 +66,7 @@ struct RingSimtArgs {
     const float *q, *k, *v;
     int B, S, Hq, Hkv, D, n_shards, block, causal, partials;
     OutDesc out;
+    int layout = 0;
 };
 cudaError_t launch_ring_simt(const RingSimtArgs& a, cudaStream_t stream);
 

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libra.so")
 
 RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_CUDA, RA_ERR_DEVICE_TIMEOUT, RA_ERR_WORKSPACE = range(6)
 RA_F32, RA_BF16 = 0, 1
+LAYOUTS = {"contiguous": 0, "zigzag": 1, "striped": 2}
 STATUS_NAMES = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
                 4: "RA_ERR_DEVICE_TIMEOUT", 5: "RA_ERR_WORKSPACE"}
 
@@ -26,6 +27,11 @@ _vp, _i, _sz, _fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_voi
 SIGNATURES = {
     "ra_blockwise_attn_fwd": (_i, [_vp, _vp, _vp, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
     "ra_ring_partials_fwd": (_i, [_vp, _vp, _vp, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
+    "ra_blockwise_attn_fwd_layout": (_i, [_vp, _vp, _vp, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
+    "ra_ring_partials_fwd_layout": (_i, [_vp, _vp, _vp, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
+    "ra_layout_positions": (_i, [_i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
+    "ra_ring_walk_layout": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int),
+                                 ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "ra_lse_merge": (_i, [_vp, _fp, _vp, _fp, _i, _i, _i, _i, _i, _i, _vp]),
     "ra_prefix_fanout_attn": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _fp, _i, _i, _i, _i,
                                    _vp, _sz, _vp]),
@@ -98,8 +104,18 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
-def attn(q, k, v, n_shards: int, block: int, causal: bool, out=None, lse=None, want_lse: bool = True):
-    """Blockwise ring-order attention.  q [B,S,Hq,D], k/v [B,S,Hkv,D] (bf16 or fp32).
+def _layout(layout) -> int:
+    if isinstance(layout, str):
+        if layout not in LAYOUTS:
+            raise ValueError(f"unknown layout {layout!r} (one of {sorted(LAYOUTS)})")
+        return LAYOUTS[layout]
+    return int(layout)
+
+
+def attn(q, k, v, n_shards: int, block: int, causal: bool, out=None, lse=None, want_lse: bool = True,
+         layout="contiguous"):
+    """Blockwise ring-order attention.  q [B,S,Hq,D], k/v [B,S,Hkv,D] (bf16 or fp32), rows stored in
+    the given shard layout ("contiguous", "zigzag" or "striped").
     Returns (out [B,S,Hq,D], lse [B,Hq,S] fp32 or None)."""
     B, S, Hq, D = q.shape
     Hkv = k.shape[2]
@@ -110,12 +126,19 @@ def attn(q, k, v, n_shards: int, block: int, causal: bool, out=None, lse=None, w
     if lse is None and want_lse:
         lse = torch.empty(B, Hq, S, device=q.device, dtype=torch.float32)
     dev = _cuda(q, k, v, out, lse)
-    _check(load().ra_blockwise_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, Hq, Hkv, D,
-                                        n_shards, block, int(bool(causal)), _dt(q), _stream(dev)))
+    lay = _layout(layout)
+    if lay == 0:
+        _check(load().ra_blockwise_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, Hq, Hkv, D,
+                                            n_shards, block, int(bool(causal)), _dt(q), _stream(dev)))
+    else:
+        _check(load().ra_blockwise_attn_fwd_layout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, Hq, Hkv,
+                                                   D, n_shards, block, int(bool(causal)), lay, _dt(q),
+                                                   _stream(dev)))
     return out, lse
 
 
-def ring_partials(q, k, v, n_shards: int, block: int, causal: bool, partials_O=None, partials_lse=None):
+def ring_partials(q, k, v, n_shards: int, block: int, causal: bool, partials_O=None, partials_lse=None,
+                  layout="contiguous"):
     """Per-KV-shard partials: (partials_O [N,B,S,Hq,D], partials_lse [N,B,Hq,S] fp32)."""
     B, S, Hq, D = q.shape
     Hkv = k.shape[2]
@@ -124,8 +147,14 @@ def ring_partials(q, k, v, n_shards: int, block: int, causal: bool, partials_O=N
     if partials_lse is None:
         partials_lse = torch.empty((n_shards, B, Hq, S), device=q.device, dtype=torch.float32)
     dev = _cuda(q, k, v, partials_O, partials_lse)
-    _check(load().ra_ring_partials_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(partials_O), _ptr(partials_lse), B, S, Hq,
-                                       Hkv, D, n_shards, block, int(bool(causal)), _dt(q), _stream(dev)))
+    lay = _layout(layout)
+    if lay == 0:
+        _check(load().ra_ring_partials_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(partials_O), _ptr(partials_lse), B, S,
+                                           Hq, Hkv, D, n_shards, block, int(bool(causal)), _dt(q), _stream(dev)))
+    else:
+        _check(load().ra_ring_partials_fwd_layout(_ptr(q), _ptr(k), _ptr(v), _ptr(partials_O), _ptr(partials_lse),
+                                                  B, S, Hq, Hkv, D, n_shards, block, int(bool(causal)), lay,
+                                                  _dt(q), _stream(dev)))
     return partials_O, partials_lse
 
 
@@ -202,6 +231,27 @@ def ring_shard_order(S: int, n_shards: int, causal: bool, q_row0: int) -> list[i
     if n < 0:
         raise ValueError("invalid arguments")
     return list(buf[:n])
+
+
+def layout_positions(S: int, n_shards: int, layout) -> list[int]:
+    """Sequence position of every storage row under a shard layout (host-side, no GPU)."""
+    buf = (ctypes.c_int * max(S, 1))()
+    if load().ra_layout_positions(S, n_shards, _layout(layout), buf) != 0:
+        raise ValueError("invalid arguments")
+    return list(buf[:S])
+
+
+def ring_walk(S: int, n_shards: int, causal: bool, layout, q_row0: int, q_rows: int, tile: int):
+    """The walk of one query tile (host-side, no GPU): ([visited shards in ring order],
+    [keys of each the tile's last row sees], total KV tiles walked)."""
+    order = (ctypes.c_int * max(n_shards, 1))()
+    keys = (ctypes.c_int * max(n_shards, 1))()
+    total = ctypes.c_int(0)
+    n = load().ra_ring_walk_layout(S, n_shards, int(bool(causal)), _layout(layout), q_row0, q_rows, tile, order,
+                                   keys, ctypes.byref(total))
+    if n < 0:
+        raise ValueError("invalid arguments")
+    return list(order[:n]), list(keys[:n]), total.value
 
 
 def device_status(stream=None) -> None:
