@@ -255,6 +255,15 @@ def run_ours(args, rank, world):
         ms_step = total_ms / args.steps
         value = job_throughput(flops, args.steps, total_ms, world)
 
+        # the same workload stored in the zigzag and striped shard layouts (same FLOPs)
+        for lay in ("zigzag", "striped"):
+            lms = timed_steps(lambda: ra.attn(q, k, v, w.n_shards, w.block, w.causal, out=out, lse=lse, layout=lay),
+                              min(args.steps, 10), 3, flush)
+            ra.device_status()
+            t = statistics.median(lms) * 1e-3
+            result.setdefault("layouts", {})[lay] = {
+                "ms": t * 1e3, "TFLOP_per_s": flops / t / 1e12, "frac_bf16_peak": flops / t / 1e12 / pk["bf16_tflops"]}
+
         # e2e through the public API with host buffers
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
         oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)

@@ -115,7 +115,7 @@ struct Unit {
     int unit_row_lo, unit_row_hi;  // stacked rows the unit's tiles cover
 };
 
-template <bool FAN>
+template <bool FAN, bool LAY = false>
 __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
     Unit u;
     u.valid = 1;
@@ -133,7 +133,9 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         const int qt_rev = rem / hg_per_kv;
         u.b = g / p.Hkv;
         const int hg = (g - u.b * p.Hkv) * hg_per_kv + (rem - qt_rev * hg_per_kv);
-        u.q_row0 = p.causal ? heavy_tile_row0(p.layout, p.S, p.n_shards, kTileM, qt_rev) : qt_rev * kTileM;
+        u.q_row0 = !p.causal ? qt_rev * kTileM
+                   : LAY     ? heavy_tile_row0(p.layout, p.S, p.n_shards, kTileM, qt_rev)
+                             : (p.n_qtiles - 1 - qt_rev) * kTileM;
         u.T = p.T2 ? 2 : 1;
         for (int t = 0; t < 2; ++t) {
             u.head[t] = hg * u.T + (t < u.T ? t : 0);
@@ -242,10 +244,10 @@ __device__ int fold_tiles(const TcParams& p, const Unit& u, bool report) {
 // ra_walk.h.  Fan-out: the unit's prefix range, then the suffix of every
 // branch folded into it (only that branch's rows see those keys); a suffix
 // unit walks one branch's suffix.
-template <bool FAN>
+template <bool FAN, bool LAY = false>
 struct TileWalk {
     static constexpr bool fan = FAN;
-    RingIter ring;
+    RingIterT<LAY> ring;
     int seg;              // fan-out: 0 prefix, 1 suffix
     int b;                // fan-out suffix segment: branch
     int kb, key_end;      // first key of the tile, end of the segment's keys
@@ -419,7 +421,8 @@ __device__ __forceinline__ void reg_inc() {
 // their KV tiles over the two tile slots (one row tile), all pair two row
 // tiles, or mix both (suffix units without a prefix).  The uniform fan-out
 // variants compile only their own issue and softmax paths.
-enum KernelMode : int { kModeRing = 0, kModeFanMixed = 1, kModeFanSplit = 2, kModeFanPaired = 3 };
+// kModeRingLayout: a causal ring walk over zigzag or striped shards.
+enum KernelMode : int { kModeRing = 0, kModeFanMixed = 1, kModeFanSplit = 2, kModeFanPaired = 3, kModeRingLayout = 4 };
 
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -427,10 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k2,
                    const __grid_constant__ CUtensorMap tm_v2, const TcParams p) {
     using C = Cfg<D>;
-    constexpr bool FAN = MODE != kModeRing;
-    const Unit u = decode_unit<FAN>(p);
+    constexpr bool RING = MODE == kModeRing || MODE == kModeRingLayout;
+    constexpr bool FAN = !RING;
+    constexpr bool LAY = MODE == kModeRingLayout;
+    const Unit u = decode_unit<FAN, LAY>(p);
     if (!u.valid) return;
-    const bool split = MODE == kModeFanSplit ? true : (MODE == kModeRing || MODE == kModeFanPaired) ? false : u.split != 0;
+    const bool split = MODE == kModeFanSplit ? true : (RING || MODE == kModeFanPaired) ? false : u.split != 0;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -461,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     RingWalk w{};
     int total;
     if (!FAN) {
-        w = make_ring_walk(p.S, p.n_shards, kTileN, p.causal, u.q_row0, kTileM, p.layout);
+        w = make_ring_walk(p.S, p.n_shards, kTileN, p.causal, u.q_row0, kTileM, LAY ? p.layout : kLayoutContiguous);
         total = w.total;
     } else {
         total = u.total;
@@ -528,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int issued = 0;
             StageCtr cs;
-            TileWalk<FAN> wi;
+            TileWalk<FAN, LAY> wi;
             wi.start(p, u, w);
             bool ok = true;
             for (int i = 0; ok && (FAN ? wi.more : i < total); ++i, wi.next(p, u)) {
@@ -618,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t k_end = k_lo0 + nK * kStageLo, v_end = v_lo0 + nV * kStageLo;
                 uint32_t k_lo = k_lo0, v_lo = v_lo0;
                 const bool track = p.partials && !FAN;
-                RingIter wp;  // tile i - 1 (shard openings restart O in partials mode)
+                RingIterT<LAY> wp;  // tile i - 1 (shard openings restart O in partials mode)
                 if (track) wp.start(w);
                 // One iteration with runtime stage indices.
                 auto step = [&](int i) -> bool {
@@ -668,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr int nKc = C::kMaxKV, nVc = C::kNVPair;
                 uint32_t kflip = 0, vflip = 0;
                 // (ring prefill only: the fan-out variants measured slower with it)
-                for (; MODE == kModeRing && ok && i + kBlk <= total; i += kBlk) {
+                for (; RING && ok && i + kBlk <= total; i += kBlk) {
                     const uint32_t kb = k_lo0, vb = v_lo0, qa = q0, qb = q1;
 #pragma unroll
                     for (int pos = 0; pos < kBlk; ++pos) {
@@ -701,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cv.ph ^= vflip;
                 for (; ok && i <= total; ++i) ok = step(i);
             }
-            RingIter wp;  // at iteration i >= 1: tile i-1 (shard openings restart O in partials mode)
+            RingIterT<LAY> wp;  // at iteration i >= 1: tile i-1 (shard openings restart O in partials mode)
             if (!FAN) wp.start(w);
             for (int i = 0; ok && !split && T == 1 && i <= total; ++i) {
                 const bool fresh_prev = (p.partials && !FAN) ? wp.first() : (i == 1);
@@ -772,8 +777,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_use = -INFINITY, l_sum = 0.f;
         bool ok = true;
         // zigzag / striped causal walks: this row's sequence position
-        const int shard_len = FAN ? 0 : p.S / p.n_shards;
-        const int row_pos = (FAN || p.layout == kLayoutContiguous) ? row : layout_pos(p.layout, shard_len, p.n_shards, row);
+        const int shard_len = LAY ? p.S / p.n_shards : 0;
+        const int row_pos = LAY ? layout_pos(p.layout, shard_len, p.n_shards, row) : row;
 
         // Normalise the O accumulator and write it as part `part`, once `done`
         // (if given) shows its last PV complete.
@@ -819,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Walk tiles of this slot: all of them, or every other one in split mode.
         const int i_step = split ? 2 : 1;
         int jj = 0;  // this slot's tile count so far (barrier phase index)
-        TileWalk<FAN> wi;
+        TileWalk<FAN, LAY> wi;
         wi.start(p, u, w);
         if (split && t == 1) wi.next(p, u);
         int last_shard = FAN ? 0 : wi.ring.j;
@@ -853,11 +858,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!FAN) {
                 // keys of this tile the row sees: a prefix of the tile (positions
                 // increase along a shard), ending where the shard's visible keys end
-                if (p.causal)
-                    lim = min(lim, p.layout == kLayoutContiguous
-                                       ? row - tile_kb
-                                       : shard_visible(p.layout, shard_len, p.n_shards, wi.ring.j, row_pos) -
-                                             (tile_kb - wi.ring.j * shard_len) - 1);
+                if (LAY)
+                    lim = min(lim, shard_visible(p.layout, shard_len, p.n_shards, wi.ring.j, row_pos) -
+                                       (tile_kb - wi.ring.j * shard_len) - 1);
+                else if (p.causal)
+                    lim = min(lim, row - tile_kb);
             } else {
                 lim = min(lim, wi.key_end - 1 - tile_kb);
                 // rows of another branch (a folded suffix) or past the stacked rows
@@ -1136,6 +1141,11 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
     if (!make_map(&tq, a.q, qd, qs, box) || !make_map(&tk, a.k, kd, ks, box) || !make_map(&tv, a.v, kd, ks, box))
         return cudaErrorInvalidValue;
     const int grid = p.n_qtiles * a.B * p.n_head_groups;
+    // without a causal mask every layout is the same walk
+    if (a.causal && a.layout != kLayoutContiguous)
+        return a.D == 128 ? launch<128, kModeRingLayout>(p, grid, tq, tk, tv, tk, tv, stream)
+                          : launch<64, kModeRingLayout>(p, grid, tq, tk, tv, tk, tv, stream);
+    p.layout = kLayoutContiguous;
     return a.D == 128 ? launch<128, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream)
                       : launch<64, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream);
 }

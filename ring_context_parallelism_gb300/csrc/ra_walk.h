@@ -130,12 +130,15 @@ RA_HD RingWalk make_ring_walk(int S, int n_shards, int tile, int causal, int q_r
 RA_HD int ring_shard_at(const RingWalk& w, int t) { return (w.k - t + w.n_shards) % w.n_shards; }
 
 // Incremental form of the same walk, for kernel loops: advancing within a
-// shard costs adds and compares only; a shard switch of a causal zigzag or
-// striped walk recomputes that shard's visible prefix.
-struct RingIter {
+// shard costs adds and compares only.  LAYOUTS = false walks contiguous shards
+// (every shard after the first is walked whole); LAYOUTS = true also handles
+// causal zigzag and striped walks, where a shard switch recomputes that shard's
+// visible prefix.
+template <bool LAYOUTS>
+struct RingIterT {
     int n_shards, L, tile, tiles_per_shard;
-    int lay;    // layout when causal and not contiguous (0: every later shard is walked whole)
-    int maxpos;
+    int lay;    // LAYOUTS: layout when causal (contiguous otherwise)
+    int maxpos; // LAYOUTS: position of the query tile's last row
     int t;      // ring step of the current shard
     int j;      // current shard
     int in;     // tile index within the current shard's visited tiles
@@ -147,8 +150,10 @@ struct RingIter {
         L = w.shard_len;
         tile = w.tile;
         tiles_per_shard = w.tiles_per_shard;
-        lay = w.causal ? w.layout : kLayoutContiguous;
-        maxpos = w.maxpos;
+        if (LAYOUTS) {
+            lay = w.causal ? w.layout : kLayoutContiguous;
+            maxpos = w.maxpos;
+        }
         t = 0;
         j = w.k;
         in = 0;
@@ -161,8 +166,10 @@ struct RingIter {
         L = 0;
         tile = tile_keys;
         tiles_per_shard = n_tiles;
-        lay = kLayoutContiguous;
-        maxpos = 0;
+        if (LAYOUTS) {
+            lay = kLayoutContiguous;
+            maxpos = 0;
+        }
         t = 0;
         j = 0;
         in = 0;
@@ -180,12 +187,14 @@ struct RingIter {
             ++t;
             j = (j == 0) ? n_shards - 1 : j - 1;
             in = 0;
-            count = lay == kLayoutContiguous ? tiles_per_shard
-                                             : ceil_div(shard_visible(lay, L, n_shards, j, maxpos), tile);
+            count = (!LAYOUTS || lay == kLayoutContiguous)
+                        ? tiles_per_shard
+                        : ceil_div(shard_visible(lay, L, n_shards, j, maxpos), tile);
             kb = j * L;
         }
     }
 };
+using RingIter = RingIterT<true>;
 
 // Query tiles of a launch in heaviest-first order under the causal mask: the
 // r-th tile launched holds the r-th largest last-row position.  n_qtiles tiles

@@ -95,3 +95,23 @@ def online_softmax_walk(q_row, K, V, order, scale):
         O = alpha * O + p @ V[idx]
         m = m_new
     return O / l, m + math.log(l)
+
+
+def page_positions(S, N, layout):
+    """Sequence position of each storage row, written from the statements of
+    "RingAttention and Context Parallelism: Mathematical Foundations", section 5:
+    shard k holds chunks c_k and c_(2N-1-k) of 2N equal chunks (zigzag) or the
+    tokens i with i = k (mod N) in increasing order (striped); shards are stored
+    one after another."""
+    if layout == "contiguous":
+        return list(range(S))
+    pos = []
+    for k in range(N):
+        if layout == "zigzag":
+            H = S // (2 * N)
+            for c in (k, 2 * N - 1 - k):
+                pos += list(range(c * H, (c + 1) * H))
+        else:
+            pos += [i for i in range(S) if i % N == k]
+    return pos
+

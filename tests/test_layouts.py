@@ -14,7 +14,7 @@ import pytest
 import oracle
 import ring_context_parallelism_gb300 as ra
 from ring_context_parallelism_gb300.build import build
-from helpers import read_golden_arrows
+from helpers import page_positions, read_golden_arrows
 
 LAYOUTS = ("contiguous", "zigzag", "striped")
 
@@ -27,23 +27,6 @@ def lib():
 
 def _fields(lhs):
     return dict(x.split("=") for x in lhs.split()[1:])
-
-
-def page_positions(S, N, layout):
-    """Sequence position of each storage row, written from the pages' statements:
-    shard k holds chunks c_k and c_(2N-1-k) (zigzag) or the tokens i = k mod N in
-    increasing order (striped), shards stored one after another."""
-    if layout == "contiguous":
-        return list(range(S))
-    pos = []
-    for k in range(N):
-        if layout == "zigzag":
-            H = S // (2 * N)
-            for c in (k, 2 * N - 1 - k):
-                pos += list(range(c * H, (c + 1) * H))
-        else:
-            pos += [i for i in range(S) if i % N == k]
-    return pos
 
 
 def test_zigzag_positions_match_page_figure(lib):
