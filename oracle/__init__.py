@@ -65,6 +65,11 @@ def _bind(lib):
     lib.oracle_fanout.restype = i
     lib.oracle_lse_merge.argtypes = [vp, vp, i, i, i, i, i, vp, vp]
     lib.oracle_lse_merge.restype = i
+    lib.oracle_attention_bwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, vp]
+    lib.oracle_attention_bwd.restype = i
+    lib.oracle_attention_bwd_rows.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, i64, vp, vp, i64, vp,
+                                              vp]
+    lib.oracle_attention_bwd_rows.restype = i
     lib.oracle_set_threads.argtypes = [i]
     lib.oracle_max_threads.restype = i
     return lib
@@ -134,6 +139,59 @@ def attention(q, k, v, *, dtype: str, causal: bool, kv_range=None, sel=None, pos
     if rc != 0:
         raise ValueError("oracle_attention rejected its arguments")
     return out, lse
+
+
+def attention_bwd(q, k, v, dout, *, dtype: str, causal: bool, pos=None):
+    """Gradients (dQ, dK, dV) of softmax attention for the upstream gradient dO, fp64.
+
+    Follows "RingAttention and Context Parallelism: Mathematical Foundations",
+    section 7 (backward pass: scores recomputed from Q and K, dQ, dK, dV
+    accumulated), written as the plain chain rule through each query's full
+    softmax row: P = softmax(s), dV += P dO, dP = dO . v, dS = P (dP - sum P dP),
+    dQ = dS K / sqrt(d), dK += dS q / sqrt(d).  GQA heads of a group add into
+    their kv head's dK and dV.
+
+    q, dout [B,S,Hq,D]; k, v [B,S,Hkv,D] in storage form (dout in the same dtype).
+    Returns (dq [B,S,Hq,D], dk [B,S,Hkv,D], dv [B,S,Hkv,D]) float64.
+    """
+    q, k, v, dout = (_as_storage(t, dtype) for t in (q, k, v, dout))
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    assert k.shape == (B, S, Hkv, D) and v.shape == k.shape and dout.shape == q.shape
+    if pos is not None:
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        assert pos.shape == (S,)
+    dq = np.empty((B, S, Hq, D), np.float64)
+    dk = np.empty((B, S, Hkv, D), np.float64)
+    dv = np.empty((B, S, Hkv, D), np.float64)
+    rc = _load().oracle_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), DTYPES[dtype], B, S, Hq, Hkv, D,
+                                      int(bool(causal)), _ptr(pos), _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd rejected its arguments")
+    return dq, dk, dv
+
+
+def attention_bwd_rows(q, k, v, dout, *, dtype: str, causal: bool, qsel=None, ksel=None, pos=None):
+    """Selected rows of the same gradients, each computed on its own (for
+    workloads too large for the full oracle).  qsel: query ids (b*S + i)*Hq + h
+    -> dq rows [n_q, D]; ksel: key ids (b*S + j)*Hkv + hk -> dk, dv rows [n_k, D]
+    (a key's rows sum over every query that sees it)."""
+    q, k, v, dout = (_as_storage(t, dtype) for t in (q, k, v, dout))
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    qsel = np.ascontiguousarray(np.zeros(0) if qsel is None else qsel, dtype=np.int64)
+    ksel = np.ascontiguousarray(np.zeros(0) if ksel is None else ksel, dtype=np.int64)
+    if pos is not None:
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+    dq = np.empty((qsel.size, D), np.float64)
+    dk = np.empty((ksel.size, D), np.float64)
+    dv = np.empty((ksel.size, D), np.float64)
+    rc = _load().oracle_attention_bwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), DTYPES[dtype], B, S, Hq, Hkv,
+                                           D, int(bool(causal)), _ptr(pos), _ptr(qsel), qsel.size, _ptr(dq),
+                                           _ptr(ksel), ksel.size, _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd_rows rejected its arguments")
+    return dq, dk, dv
 
 
 def fanout(q_rows, offsets, k_prefix, v_prefix, k_suffix, v_suffix, *, dtype: str, sel=None):

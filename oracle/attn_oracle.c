@@ -316,3 +316,199 @@ int oracle_lse_merge(const double* part_O, const double* part_lse, int P, int B,
     }
     return 0;
 }
+
+/*
+ * Backward pass: gradients of the attention output with respect to q, k and v,
+ * given the upstream gradient dO ("RingAttention and Context Parallelism:
+ * Mathematical Foundations", section 7, "RingAttention backward pass logic":
+ * the scores of every block are recomputed and dQ, dK, dV accumulated).  The
+ * oracle does not recompute blockwise: it materialises each query's full
+ * softmax row and applies the chain rule to A = softmax(s) V, s = q K^T / sqrt(d):
+ *
+ *   P_j   = exp(s_j) / sum_j' exp(s_j')          (visible keys j only)
+ *   dV_j += P_j dO_i                             (every query i that sees j)
+ *   dP_j  = dO_i . v_j
+ *   dS_j  = P_j (dP_j - sum_j' P_j' dP_j')       (softmax Jacobian)
+ *   dQ_i  = scale sum_j dS_j k_j
+ *   dK_j += scale dS_j q_i
+ *
+ * GQA: the q heads of a group add into their kv head's dK and dV.
+ */
+
+/* One query row's softmax-backward terms over its visible keys: fills P[j]
+ * and dS[j] for the n keys listed (n == 0: nothing to fill). */
+static void backward_row(const double* q_row, const double* do_row, const key_ref* keys, int64_t n, int D,
+                         int dtype, double scale, double* P, double* dS) {
+    if (n == 0) return;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += q_row[d] * load_elem(keys[j].k, dtype, keys[j].off + d);
+        P[j] = acc * scale;
+        if (P[j] > m) m = P[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        P[j] = exp(P[j] - m);
+        l += P[j];
+    }
+    double delta = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        P[j] /= l;
+        double dp = 0.0;
+        for (int d = 0; d < D; ++d) dp += do_row[d] * load_elem(keys[j].v, dtype, keys[j].off + d);
+        dS[j] = dp;
+        delta += P[j] * dp;
+    }
+    for (int64_t j = 0; j < n; ++j) {
+#if ORACLE_MUTANT == 9
+        dS[j] = P[j] * dS[j]; /* mutant: the softmax Jacobian's row term dropped */
+#else
+        dS[j] = P[j] * (dS[j] - delta);
+#endif
+    }
+}
+
+/* Visible keys of query (b, i) with kv head hk: all, or pos[j] <= pos[i] when
+ * causal (pos == NULL: stored order = sequence order).  Returns the count. */
+static int64_t visible_keys(const void* k, const void* v, int b, int i, int hk, int S, int Hkv, int D,
+                            int causal, const int32_t* pos, key_ref* keys) {
+    int64_t n = 0;
+    for (int j = 0; j < S; ++j) {
+        if (causal && (pos ? pos[j] > pos[i] : j > i)) continue;
+        keys[n].k = k;
+        keys[n].v = v;
+        keys[n].off = (((int64_t)b * S + j) * Hkv + hk) * D;
+        ++n;
+    }
+    return n;
+}
+
+/*
+ * Full gradients.  q, dout [B,S,Hq,D]; k, v [B,S,Hkv,D] in `dtype` (dout in the
+ * same storage type).  dq [B,S,Hq,D], dk / dv [B,S,Hkv,D] double.
+ * Parallel over (b, kv head): each thread owns its group's dK and dV.
+ */
+int oracle_attention_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                         int B, int S, int Hq, int Hkv, int D, int causal, const int32_t* pos,
+                         double* dq, double* dk, double* dv) {
+    if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || D > 512 || Hq % Hkv) return -1;
+    const int group = Hq / Hkv;
+    const double scale = 1.0 / sqrt((double)D);
+    memset(dk, 0, sizeof(double) * (size_t)B * S * Hkv * D);
+    memset(dv, 0, sizeof(double) * (size_t)B * S * Hkv * D);
+#pragma omp parallel
+    {
+        double q_row[512], do_row[512];
+        double* P = (double*)malloc(sizeof(double) * (size_t)S);
+        double* dS = (double*)malloc(sizeof(double) * (size_t)S);
+        key_ref* keys = (key_ref*)malloc(sizeof(key_ref) * (size_t)S);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t g = 0; g < (int64_t)B * Hkv; ++g) {
+            const int b = (int)(g / Hkv), hk = (int)(g % Hkv);
+            for (int h = hk * group; h < (hk + 1) * group; ++h) {
+                for (int i = 0; i < S; ++i) {
+                    const int64_t qoff = (((int64_t)b * S + i) * Hq + h) * D;
+                    for (int d = 0; d < D; ++d) {
+                        q_row[d] = load_elem(q, dtype, qoff + d);
+                        do_row[d] = load_elem(dout, dtype, qoff + d);
+                    }
+                    const int64_t n = visible_keys(k, v, b, i, hk, S, Hkv, D, causal, pos, keys);
+                    backward_row(q_row, do_row, keys, n, D, dtype, scale, P, dS);
+                    double* dqi = dq + qoff;
+                    for (int d = 0; d < D; ++d) dqi[d] = 0.0;
+                    for (int64_t jj = 0; jj < n; ++jj) {
+                        const int64_t koff = keys[jj].off;  /* the key's row in k, v, dk, dv */
+                        for (int d = 0; d < D; ++d) {
+                            dqi[d] += scale * dS[jj] * load_elem(k, dtype, koff + d);
+#if ORACLE_MUTANT == 10
+                            dk[koff + d] += dS[jj] * q_row[d]; /* mutant: dK without the softmax scale */
+#else
+                            dk[koff + d] += scale * dS[jj] * q_row[d];
+#endif
+                            dv[koff + d] += P[jj] * do_row[d];
+                        }
+                    }
+                }
+            }
+        }
+        free(P);
+        free(dS);
+        free(keys);
+    }
+    return 0;
+}
+
+/*
+ * Selected rows of the same gradients, each computed on its own:
+ *   qsel ids (b*S + i)*Hq + h   -> dq_rows [n_q, D]
+ *   ksel ids (b*S + j)*Hkv + hk -> dk_rows, dv_rows [n_k, D]; a key's gradient
+ *   sums over every query (of every q head of the group) that sees it, each
+ *   with its full softmax row.
+ */
+int oracle_attention_bwd_rows(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                              int B, int S, int Hq, int Hkv, int D, int causal, const int32_t* pos,
+                              const int64_t* qsel, int64_t n_q, double* dq_rows,
+                              const int64_t* ksel, int64_t n_k, double* dk_rows, double* dv_rows) {
+    if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || D > 512 || Hq % Hkv) return -1;
+    const int group = Hq / Hkv;
+    const double scale = 1.0 / sqrt((double)D);
+    int bad = 0;
+#pragma omp parallel
+    {
+        double q_row[512], do_row[512];
+        double* P = (double*)malloc(sizeof(double) * (size_t)S);
+        double* dS = (double*)malloc(sizeof(double) * (size_t)S);
+        key_ref* keys = (key_ref*)malloc(sizeof(key_ref) * (size_t)S);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < n_q + n_k; ++t) {
+            if (t < n_q) {
+                const int64_t id = qsel[t];
+                if (id < 0 || id >= (int64_t)B * S * Hq) { bad = 1; continue; }
+                const int h = (int)(id % Hq);
+                const int i = (int)((id / Hq) % S), b = (int)(id / Hq / S);
+                for (int d = 0; d < D; ++d) {
+                    q_row[d] = load_elem(q, dtype, id * D + d);
+                    do_row[d] = load_elem(dout, dtype, id * D + d);
+                }
+                const int64_t n = visible_keys(k, v, b, i, h / group, S, Hkv, D, causal, pos, keys);
+                backward_row(q_row, do_row, keys, n, D, dtype, scale, P, dS);
+                double* o = dq_rows + t * D;
+                for (int d = 0; d < D; ++d) o[d] = 0.0;
+                for (int64_t jj = 0; jj < n; ++jj)
+                    for (int d = 0; d < D; ++d) o[d] += scale * dS[jj] * load_elem(k, dtype, keys[jj].off + d);
+            } else {
+                const int64_t u = t - n_q, id = ksel[u];
+                if (id < 0 || id >= (int64_t)B * S * Hkv) { bad = 1; continue; }
+                const int hk = (int)(id % Hkv);
+                const int j = (int)((id / Hkv) % S), b = (int)(id / Hkv / S);
+                double* ok = dk_rows + u * D;
+                double* ov = dv_rows + u * D;
+                for (int d = 0; d < D; ++d) ok[d] = ov[d] = 0.0;
+                for (int h = hk * group; h < (hk + 1) * group; ++h) {
+                    for (int i = 0; i < S; ++i) {
+                        if (causal && (pos ? pos[j] > pos[i] : j > i)) continue;
+                        const int64_t qoff = (((int64_t)b * S + i) * Hq + h) * D;
+                        for (int d = 0; d < D; ++d) {
+                            q_row[d] = load_elem(q, dtype, qoff + d);
+                            do_row[d] = load_elem(dout, dtype, qoff + d);
+                        }
+                        const int64_t n = visible_keys(k, v, b, i, hk, S, Hkv, D, causal, pos, keys);
+                        backward_row(q_row, do_row, keys, n, D, dtype, scale, P, dS);
+                        int64_t jj = 0;  /* the listed index of key j */
+                        const int64_t koff = (((int64_t)b * S + j) * Hkv + hk) * D;
+                        while (keys[jj].off != koff) ++jj;
+                        for (int d = 0; d < D; ++d) {
+                            ok[d] += scale * dS[jj] * q_row[d];
+                            ov[d] += P[jj] * do_row[d];
+                        }
+                    }
+                }
+            }
+        }
+        free(P);
+        free(dS);
+        free(keys);
+    }
+    return bad ? -1 : 0;
+}

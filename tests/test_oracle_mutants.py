@@ -6,6 +6,7 @@ import pytest
 
 import oracle
 import test_layouts as layouts
+import test_oracle_bwd_pins as bwd_pins
 import test_oracle_pins as pins
 
 PINS = [
@@ -18,6 +19,8 @@ PINS = [
     lambda: pins.test_shard_partials_merge_to_unsharded(True),
     pins.test_fanout_equals_per_branch_attention_over_prefix_plus_suffix,
     lambda: layouts.test_oracle_on_stored_layout_equals_sequence_order("zigzag"),
+    lambda: bwd_pins.test_bwd_finite_differences(True),
+    lambda: bwd_pins.test_bwd_matches_torch_float64_autograd(True, 6, 2),
 ]
 
 MUTANTS = {
@@ -29,6 +32,8 @@ MUTANTS = {
     6: "last visible key dropped",
     7: "merge forgets to normalise",
     8: "causal mask on the stored order instead of sequence positions",
+    9: "backward: softmax Jacobian's row term dropped",
+    10: "backward: dK without the softmax scale",
 }
 
 
