@@ -143,6 +143,38 @@ ra_status ra_ring_partials_fwd_layout(const void* q, const void* k, const void* 
                                       void* stream);
 
 /*
+ * Backward pass of ra_blockwise_attn_fwd: dQ, dK, dV for an upstream gradient
+ * dO ("RingAttention and Context Parallelism: Mathematical Foundations",
+ * section 7, "RingAttention backward pass logic": the forward keeps Q and the
+ * log-sum-exp L = m + ln l of every row; the backward recomputes the scores of
+ * each block from Q and K, accumulates dQ locally and carries dK, dV with the
+ * K/V blocks as they rotate through the ring in reverse order).  With
+ * P = exp(q.k/sqrt(D) - L), Delta = rowsum(dO * O) and dS = P (dO.v - Delta):
+ *   dV = P^T dO,   dK = dS^T Q / sqrt(D),   dQ = dS K / sqrt(D);
+ * the q heads of a GQA group add into their kv head's dK and dV.
+ *
+ * Two walks, no atomics: every 128-row query tile walks the KV tiles in the
+ * forward's ring order for dQ; every 128-key KV tile walks the query tiles of
+ * its group's q heads, query shard j, j-1, ... (mod N, causal-empty shards
+ * skipped), for dK and dV.
+ *
+ *   q, out, dout, dq [B, S, Hq, D] dtype dt     k, v, dk, dv [B, S, Hkv, D] dtype dt
+ *   lse [B, Hq, S] fp32: the forward's lse for these q, k, v.  out: its O.
+ *   workspace: device scratch of ra_blockwise_attn_bwd_workspace_size(...)
+ *              bytes, 256-byte aligned, owned by the caller (contents ignored).
+ * Other arguments, shape rules and errors as ra_blockwise_attn_fwd (contiguous
+ * shards); RA_ERR_WORKSPACE if the workspace is missing or too small.
+ * dq, dk, dv are fully overwritten.
+ */
+ra_status ra_blockwise_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                                const void* dout, void* dq, void* dk, void* dv, int B, int S, int Hq, int Hkv,
+                                int D, int n_shards, int block, int causal, ra_dtype dt, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace ra_blockwise_attn_bwd needs (0 if the sizes are invalid). */
+size_t ra_blockwise_attn_bwd_workspace_size(int B, int S, int Hq, int D, ra_dtype dt);
+
+/*
  * Row-indexed log-sum-exp merge of P partial states computed over disjoint key
  * sets ("AHBM Agentic Runtime Architecture", sections 3.4-3.5: the same row
  * index is merged across sequence shards, never different rows).  Per

@@ -1069,7 +1069,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+template <int D, int MODE>
+cudaError_t launch(const TcParams& p, int grid, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                   const CUtensorMap& k2, const CUtensorMap& v2, cudaStream_t stream) {
+    const int smem = Cfg<D>::kSmemBytes;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    if (grid <= 0) return cudaSuccess;
+    attn_tc_kernel<D, MODE><<<grid, kThreads, smem, stream>>>(q, k, v, k2, v2, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -1097,23 +1114,6 @@ bool make_map(CUtensorMap* m, const void* base, const unsigned long long dims[4]
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-template <int D, int MODE>
-cudaError_t launch(const TcParams& p, int grid, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                   const CUtensorMap& k2, const CUtensorMap& v2, cudaStream_t stream) {
-    const int smem = Cfg<D>::kSmemBytes;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
-    if (grid <= 0) return cudaSuccess;
-    attn_tc_kernel<D, MODE><<<grid, kThreads, smem, stream>>>(q, k, v, k2, v2, p);
-    return cudaGetLastError();
-}
-
-}  // namespace
 
 cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
     TcParams p{};

@@ -370,6 +370,51 @@ int ra_ring_shard_order(int S, int n_shards, int causal, int q_row0, int* shard_
     return w.n_visited;
 }
 
+size_t ra_blockwise_attn_bwd_workspace_size(int B, int S, int Hq, int D, ra_dtype dt) {
+    if (B < 1 || S < 1 || Hq < 1 || (D != 64 && D != 128) || (dt != RA_BF16 && dt != RA_F32)) return 0;
+    const size_t vec = (static_cast<size_t>(B) * Hq * S * sizeof(float) + 255) & ~size_t(255);
+    return 2 * vec;  // Delta, then lse in log2 units
+}
+
+ra_status ra_blockwise_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                                const void* dout, void* dq, void* dk, void* dv, int B, int S, int Hq, int Hkv,
+                                int D, int n_shards, int block, int causal, ra_dtype dt, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    ra_status st = check_ring(q, k, v, out, B, S, Hq, Hkv, D, n_shards, block, causal, dt, RA_LAYOUT_CONTIGUOUS);
+    if (st != RA_OK) return st;
+    if (!lse || !dout || !dq || !dk || !dv) return fail(RA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return fail(RA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    const size_t need = ra_blockwise_attn_bwd_workspace_size(B, S, Hq, D, dt);
+    if (!workspace || workspace_bytes < need)
+        return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", need, workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    ra::BwdArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.ws_delta = static_cast<float*>(workspace);
+    a.ws_lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + need / 2);
+    a.B = B;
+    a.S = S;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.n_shards = n_shards;
+    a.causal = causal;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = dt == RA_BF16 ? ra::launch_bwd_tc(a, s) : ra::launch_bwd_simt(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attention backward launch");
+    return ok();
+}
+
 int ra_layout_positions(int S, int n_shards, int layout, int* pos) {
     if (S < 1 || n_shards < 1 || S % n_shards || !pos) return -1;
     if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIPED) return -1;
@@ -414,6 +459,10 @@ ra_status ra_device_status(void* stream) {
     if (!code) {
         code = ra::read_clear_status_merge(&where);
         who = "lse merge";
+    }
+    if (!code) {
+        code = ra::read_clear_status_bwd(&where);
+        who = "attention backward";
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "device status");

@@ -81,10 +81,29 @@ struct MergeArgs {
 };
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t stream);
 
+// 4-D bf16 tensor map (dims innermost first, byte strides of dims 1..3, box
+// (64, b1, b2, b3), 128-byte swizzle) for the TMA loads of the tensor-core
+// kernels.  Returns false if the driver entry point or the encode fails.
+bool make_map(CUtensorMap* m, const void* base, const unsigned long long dims[4], const unsigned long long strides[3],
+              const unsigned box[4]);
+
+// Backward pass (dQ, dK, dV) for an upstream gradient dO.  ws_delta / ws_lse2:
+// workspace [B, Hq, S] fp32 each (rowsum(dO * O), lse * log2 e).
+struct BwdArgs {
+    const void *q, *k, *v, *out, *dout;
+    const float* lse;
+    void *dq, *dk, *dv;
+    float *ws_delta, *ws_lse2;
+    int B, S, Hq, Hkv, D, n_shards, causal;
+};
+cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t stream);    // bf16
+cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t stream);  // fp32
+
 // Status words of each translation unit: read (after the caller synchronised)
 // and clear.  Returns the first non-zero code, 0 if none.
 unsigned read_clear_status_tc(unsigned* where);
 unsigned read_clear_status_simt(unsigned* where);
 unsigned read_clear_status_merge(unsigned* where);
+unsigned read_clear_status_bwd(unsigned* where);
 
 }  // namespace ra

@@ -29,6 +29,9 @@ SIGNATURES = {
     "ra_ring_partials_fwd": (_i, [_vp, _vp, _vp, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
     "ra_blockwise_attn_fwd_layout": (_i, [_vp, _vp, _vp, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
     "ra_ring_partials_fwd_layout": (_i, [_vp, _vp, _vp, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
+    "ra_blockwise_attn_bwd": (_i, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                   _vp, _sz, _vp]),
+    "ra_blockwise_attn_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "ra_layout_positions": (_i, [_i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
     "ra_ring_walk_layout": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int),
                                  ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
@@ -135,6 +138,29 @@ def attn(q, k, v, n_shards: int, block: int, causal: bool, out=None, lse=None, w
                                                    D, n_shards, block, int(bool(causal)), lay, _dt(q),
                                                    _stream(dev)))
     return out, lse
+
+
+def attn_bwd(q, k, v, out, lse, dout, n_shards: int, block: int, causal: bool, dq=None, dk=None, dv=None,
+             workspace=None):
+    """Backward pass: (dq [B,S,Hq,D], dk, dv [B,S,Hkv,D]) for the upstream gradient dout, given the
+    forward's out and lse for the same q, k, v (bf16 or fp32)."""
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, S, Hkv, D) or v.shape != k.shape or out.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("q/k/v/out/dout shapes disagree")
+    if any(t.dtype != q.dtype for t in (k, v, out, dout)) or lse.dtype != torch.float32 or lse.shape != (B, Hq, S):
+        raise ValueError("dtypes disagree or lse is not fp32 [B,Hq,S]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = int(load().ra_blockwise_attn_bwd_workspace_size(B, S, Hq, D, _dt(q)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
+    dev = _cuda(q, k, v, out, lse, dout, dq, dk, dv, workspace)
+    _check(load().ra_blockwise_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                                        _ptr(dk), _ptr(dv), B, S, Hq, Hkv, D, n_shards, block, int(bool(causal)),
+                                        _dt(q), _ptr(workspace), workspace.numel(), _stream(dev)))
+    return dq, dk, dv
 
 
 def ring_partials(q, k, v, n_shards: int, block: int, causal: bool, partials_O=None, partials_lse=None,

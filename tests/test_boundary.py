@@ -142,3 +142,39 @@ def test_ring_order_is_a_permutation(lib):
             o = ra.ring_shard_order(S, N, False, row)
             assert sorted(o) == list(range(N)) and o[0] == row // 256
             assert all((o[t] - o[t + 1]) % N == 1 for t in range(N - 1))
+
+
+def _null_bwd(lib, **kw):
+    a = dict(q=16, k=16, v=16, out=16, lse=16, dout=16, dq=16, dk=16, dv=16, B=1, S=1024, Hq=4, Hkv=2, D=64, N=4,
+             block=64, causal=1, dt=rab.RA_BF16, ws=256, wsb=1 << 30)
+    a.update(kw)
+    return lib.ra_blockwise_attn_bwd(a["q"], a["k"], a["v"], a["out"], a["lse"], a["dout"], a["dq"], a["dk"],
+                                     a["dv"], a["B"], a["S"], a["Hq"], a["Hkv"], a["D"], a["N"], a["block"],
+                                     a["causal"], a["dt"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(lse=None), rab.RA_ERR_INVALID_ARG),
+    (dict(dout=None), rab.RA_ERR_INVALID_ARG),
+    (dict(dk=8), rab.RA_ERR_INVALID_ARG),            # misaligned
+    (dict(q=None), rab.RA_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), rab.RA_ERR_INVALID_ARG),
+    (dict(D=32), rab.RA_ERR_INVALID_ARG),
+    (dict(S=1000), rab.RA_ERR_INVALID_ARG),
+    (dict(S=512, N=8), rab.RA_ERR_UNSUPPORTED),       # bf16 shards shorter than a 128-key tile
+    (dict(ws=None), rab.RA_ERR_WORKSPACE),
+    (dict(wsb=64), rab.RA_ERR_WORKSPACE),
+    (dict(ws=272), rab.RA_ERR_INVALID_ARG),          # not 256-byte aligned
+])
+def test_backward_argument_validation(lib, kw, status):
+    rc = _null_bwd(lib, **kw)
+    assert rc == status, lib.ra_last_error()
+    assert lib.ra_last_error()
+
+
+def test_backward_workspace_size(lib):
+    f = lib.ra_blockwise_attn_bwd_workspace_size
+    n = f(1, 32768, 32, 128, rab.RA_BF16)
+    assert n == 2 * 32768 * 32 * 4                   # Delta and lse2, [B, Hq, S] fp32 each
+    assert f(1, 100, 3, 64, rab.RA_F32) == 2 * 1280   # each rounded up to 256 bytes
+    assert f(1, 1024, 4, 96, rab.RA_BF16) == 0
