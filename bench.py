@@ -264,6 +264,26 @@ def run_ours(args, rank, world):
             result.setdefault("layouts", {})[lay] = {
                 "ms": t * 1e3, "TFLOP_per_s": flops / t / 1e12, "frac_bf16_peak": flops / t / 1e12 / pk["bf16_tflops"]}
 
+        # backward pass on the same workload: dQ, dK, dV for a seeded upstream gradient
+        gb = torch.Generator(device="cuda")
+        gb.manual_seed(w.seed + 4242)
+        from ring_context_parallelism_gb300.inputs import randn
+        dO = randn(tuple(q.shape), gb, q.dtype, "cuda")
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws = torch.empty(ra.load().ra_blockwise_attn_bwd_workspace_size(w.B, w.S, w.Hq, w.D, 1), dtype=torch.uint8,
+                          device="cuda")
+        bms = timed_steps(lambda: ra.attn_bwd(q, k, v, out, lse, dO, w.n_shards, w.block, w.causal, dq, dk, dv, bws),
+                          min(args.steps, 10), 3, flush)
+        ra.device_status()
+        tb = statistics.median(bms) * 1e-3
+        bflops = 2.5 * flops  # 5 GEMMs of the algorithm (QK^T, dO V^T, P^T dO, dS^T Q, dS K) vs 2 forward
+        result["backward"] = {"ms": tb * 1e3, "TFLOP_per_s": bflops / tb / 1e12,
+                              "frac_bf16_peak": bflops / tb / 1e12 / pk["bf16_tflops"], "flops": bflops,
+                              "flop_convention": "2.5x the forward's causal-adjusted FLOPs (5 GEMMs); the kernels "
+                                                 "execute 7 (dQ recomputes S and dP)",
+                              "launches_per_call": 3}
+        del dO, dq, dk, dv, bws
+
         # e2e through the public API with host buffers
         qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
         oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)

@@ -56,13 +56,21 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int D>
 struct BwdCfg {
     static constexpr int kTileBytes = kT * D * 2;
-    static constexpr int kStages = D == 128 ? 2 : 4;     // per streamed ring
-    static constexpr int kSlots = 2 + 2 * kStages;        // two resident tiles + two rings
-    static constexpr int kVecOff = kSlots * kTileBytes;   // dK/dV: lse2[128], delta[128] per stage
-    static constexpr int kBarOff = kVecOff + kStages * 1024;
-    static constexpr int kNumBars = 8 + 4 * kStages;
-    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
-    static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
+    // dQ kernel: Q and dO resident; a K tile is held from S = Q K^T until
+    // dQ += dS K two tiles later, so the K ring has one stage more than V's
+    static constexpr int kDqK = D == 128 ? 3 : 4;
+    static constexpr int kDqV = D == 128 ? 2 : 4;
+    static constexpr int kDqBarOff = (2 + kDqK + kDqV) * kTileBytes;
+    // dK/dV kernel: K and V resident; Q and dO rings, each Q stage with the
+    // lse2 and delta of its 128 rows
+    static constexpr int kKvS = D == 128 ? 2 : 4;
+    static constexpr int kVecOff = (2 + 2 * kKvS) * kTileBytes;
+    static constexpr int kKvBarOff = kVecOff + kKvS * 1024;
+    static constexpr int kNumBars = 24;
+    static constexpr int kDqSmem = kDqBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
+    static constexpr int kKvSmem = kKvBarOff + kNumBars * 8 + 16 + 1024;
+    static_assert(kDqSmem <= 232448 && kKvSmem <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
+    static_assert(1 + 2 * kDqK + 2 * kDqV + 5 <= kNumBars && 1 + 4 * kKvS + 5 <= kNumBars, "barrier slots");
 };
 
 struct BwdParams {
@@ -199,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const BwdParams p) {
     using C = BwdCfg<D>;
-    constexpr int NS = C::kStages;
+    constexpr int NK = C::kDqK, NV = C::kDqV;
     // (batch, KV head) outermost so the resident CTAs share K/V in L2; within
     // it the heaviest query tiles first, the heads of the group fastest
     const int per_kv = p.n_tiles * p.G;
@@ -215,15 +223,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* q_smem = smem;
     uint8_t* do_smem = smem + C::kTileBytes;
     uint8_t* k_smem = smem + 2 * C::kTileBytes;
-    uint8_t* v_smem = k_smem + NS * C::kTileBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint8_t* v_smem = k_smem + NK * C::kTileBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kDqBarOff);
     uint64_t* qd_full = bars;
     uint64_t* k_full = bars + 1;
-    uint64_t* k_empty = k_full + NS;
-    uint64_t* v_full = k_empty + NS;
-    uint64_t* v_empty = v_full + NS;
-    uint64_t* s_full = v_empty + NS;
-    uint64_t* ds_ready = s_full + 1;
+    uint64_t* k_empty = k_full + NK;
+    uint64_t* v_full = k_empty + NK;
+    uint64_t* v_empty = v_full + NV;
+    uint64_t* s_full = v_empty + NV;  // [2]: one per S buffer
+    uint64_t* dp_full = s_full + 2;
+    uint64_t* ds_ready = dp_full + 1;
     uint64_t* dq_done = ds_ready + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -235,13 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(qd_full, 1);
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NK; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < NV; ++s) {
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        mbar_init(s_full, 1);
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(dp_full, 1);
         mbar_init(ds_ready, 256);
         mbar_init(dq_done, 1);
         *abort_flag = 0;
@@ -255,11 +268,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // TMEM columns: S buffer 0 [0, 128), dP [128, 256), dQ [256, 256 + D), S buffer 1 [384, 512)
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ producers
         if (lane == 0) {
             const bool is_k = warp == 0;
+            const int ns = is_k ? NK : NV;
             const CUtensorMap* map = is_k ? &tm_k : &tm_v;
             uint64_t* full = is_k ? k_full : v_full;
             uint64_t* empty = is_k ? k_empty : v_empty;
@@ -281,18 +296,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 mbar_arrive_expect_tx(&full[st.s], C::kTileBytes);
                 load_tile<D>(map, &full[st.s], ring + st.s * C::kTileBytes, hk, it.kb, b);
-                st.next(NS);
+                st.next(ns);
                 ++issued;
             }
             if (*abort_flag) {
-                drain_ring(full, issued, NS);
+                drain_ring(full, issued, ns);
                 if (is_k) mbar_wait_landing(qd_full, 0);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Order: S(0) dP(0) S(1), then per tile i: dQ(i) dP(i+1) S(i+2).  S is
+        // double-buffered, so the softmax warps turn S(i+1) into P while
+        // dQ(i) and dP(i+1) run, and only the dS step waits for dP.
         if (lane == 0) {
-            const uint32_t tS = tmem_base, tdP = tmem_base + 128, tdQ = tmem_base + 256;
+            const uint32_t tSb0 = tmem_base, tSb1 = tmem_base + 384, tdP = tmem_base + 128, tdQ = tmem_base + 256;
             const uint32_t q_lo = sw128_desc_lo(smem_u32(q_smem), 16);
             const uint32_t do_lo = sw128_desc_lo(smem_u32(do_smem), 16);
             const uint32_t k_lo0 = sw128_desc_lo(smem_u32(k_smem), 16);       // K-major: S = Q K^T
@@ -300,28 +318,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t v_lo0 = sw128_desc_lo(smem_u32(v_smem), 16);
             constexpr uint32_t kStageLo = C::kTileBytes >> 4;
             bool ok = mbar_wait(qd_full, 0, abort_flag, status, 0x12000000u);
-            Stage ck, cv;
-            int prev_ks = 0;
-            for (int i = 0; ok && i <= total; ++i) {
-                if (i > 0) {
-                    // dS of tile i-1 is in TMEM: dQ += dS K, then K tile i-1 is free
-                    if (!(ok = mbar_wait(ds_ready, (i - 1) & 1, abort_flag, status, 0x13000000u | i))) break;
-                    tc_fence_after();
-                    mma_tmem_a<D>(tdQ, tS, kmn_lo0 + prev_ks * kStageLo, i > 1);
-                    mma_commit(&k_empty[prev_ks]);
-                }
-                if (i < total) {
-                    if (!(ok = mbar_wait(&k_full[ck.s], ck.ph, abort_flag, status, 0x14000000u | i))) break;
-                    if (!(ok = mbar_wait(&v_full[cv.s], cv.ph, abort_flag, status, 0x15000000u | i))) break;
-                    tc_fence_after();
-                    mma_kmajor<D>(tS, q_lo, k_lo0 + ck.s * kStageLo);
-                    mma_kmajor<D>(tdP, do_lo, v_lo0 + cv.s * kStageLo);
-                    mma_commit(s_full);
-                    mma_commit(&v_empty[cv.s]);
-                    prev_ks = ck.s;
-                    ck.next(NS);
-                    cv.next(NS);
-                }
+            Stage ck, cv, cq;  // next K tile for S, next V tile for dP, K tile of the next dQ
+            auto issue_s = [&](int i) -> bool {
+                if (!mbar_wait(&k_full[ck.s], ck.ph, abort_flag, status, 0x14000000u | i)) return false;
+                tc_fence_after();
+                mma_kmajor<D>((i & 1) ? tSb1 : tSb0, q_lo, k_lo0 + ck.s * kStageLo);
+                mma_commit(&s_full[i & 1]);
+                ck.next(NK);
+                return true;
+            };
+            auto issue_dp = [&](int i) -> bool {
+                if (!mbar_wait(&v_full[cv.s], cv.ph, abort_flag, status, 0x15000000u | i)) return false;
+                tc_fence_after();
+                mma_kmajor<D>(tdP, do_lo, v_lo0 + cv.s * kStageLo);
+                mma_commit(dp_full);
+                mma_commit(&v_empty[cv.s]);
+                cv.next(NV);
+                return true;
+            };
+            if (ok && total > 0) ok = issue_s(0) && issue_dp(0);
+            if (ok && total > 1) ok = issue_s(1);
+            for (int i = 0; ok && i < total; ++i) {
+                // dS of tile i is in its S buffer: dQ += dS K, then K tile i is free
+                if (!(ok = mbar_wait(ds_ready, i & 1, abort_flag, status, 0x13000000u | i))) break;
+                tc_fence_after();
+                mma_tmem_a<D>(tdQ, (i & 1) ? tSb1 : tSb0, kmn_lo0 + cq.s * kStageLo, i > 0);
+                mma_commit(&k_empty[cq.s]);
+                cq.next(NK);
+                if (i + 1 < total && !(ok = issue_dp(i + 1))) break;
+                if (i + 2 < total && !(ok = issue_s(i + 2))) break;
             }
             mma_commit(dq_done);
             mbar_wait(dq_done, 0, abort_flag, status, 0);
@@ -333,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lane_row = quad * 32 + lane;
         const int row = q0 + lane_row;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem_base + lane_off, tdP = tS + 128, tdQ = tS + 256;
+        const uint32_t tS0 = tmem_base + lane_off, tS1 = tS0 + 384, tdP = tS0 + 128, tdQ = tS0 + 256;
         const long long vrow = (static_cast<long long>(b) * p.Hq + h) * p.S + row;
         const float lse2_r = p.lse2[vrow];
         const float delta_r = p.delta[vrow];
@@ -343,28 +368,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int i = 0; i < total; ++i) {
             if (i > 0) it.next();
-            if (!(ok = mbar_wait(s_full, i & 1, abort_flag, status, 0x16000000u | i))) break;
+            const uint32_t tS = (i & 1) ? tS1 : tS0;
+            if (!(ok = mbar_wait(&s_full[i & 1], (i >> 1) & 1, abort_flag, status, 0x16000000u | i))) break;
             tc_fence_after();
             const int lim = p.causal ? min(kT - 1, row - it.kb) : kT - 1;  // visible columns c <= lim
+            // P = exp(S - L) for this thread's half of the columns
+            float pr[64];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int col0 = hw * 64 + c * 32;
-                uint32_t s[32], dp[32], pk[16];
-                tmem_ld32(tS + col0, s);
-                tmem_ld32(tdP + col0, dp);
+                uint32_t sv[32];
+                tmem_ld32(tS + col0, sv);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int cc = col0 + 2 * j;
                     float y0, y1;
-                    ffma2(y0, y1, __uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1]), sl2, sl2, -lse2_r,
+                    ffma2(y0, y1, __uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]), sl2, sl2, -lse2_r,
                           -lse2_r);
-                    const float p0 = cc <= lim ? ex2_approx(y0) : 0.f;
-                    const float p1 = cc + 1 <= lim ? ex2_approx(y1) : 0.f;
-                    pk[j] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * j]) - delta_r),
-                                        p1 * (__uint_as_float(dp[2 * j + 1]) - delta_r));
+                    pr[c * 32 + 2 * j] = col0 + 2 * j <= lim ? ex2_approx(y0) : 0.f;
+                    pr[c * 32 + 2 * j + 1] = col0 + 2 * j + 1 <= lim ? ex2_approx(y1) : 0.f;
                 }
-                tmem_st16(tS + hw * 64 + c * 16, pk);  // dS over this half's own S columns
+            }
+            // dS = P (dP - Delta), packed bf16 over this half's own S columns
+            if (!(ok = mbar_wait(dp_full, i & 1, abort_flag, status, 0x18000000u | i))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int col0 = hw * 64 + c * 32;
+                uint32_t dp[32], pk[16];
+                tmem_ld32(tdP + col0, dp);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    pk[j] = pack_bf16x2(pr[c * 32 + 2 * j] * (__uint_as_float(dp[2 * j]) - delta_r),
+                                        pr[c * 32 + 2 * j + 1] * (__uint_as_float(dp[2 * j + 1]) - delta_r));
+                tmem_st16(tS + hw * 64 + c * 16, pk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -430,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const BwdParams p) {
     using C = BwdCfg<D>;
-    constexpr int NS = C::kStages;
+    constexpr int NS = C::kKvS;
     // (batch, KV head) outermost (its CTAs share the group's Q / dO in L2);
     // within it the key tiles in order, the earliest (most queries) first
     const int grp = blockIdx.x / p.n_tiles;
@@ -447,15 +485,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* q_smem = smem + 2 * C::kTileBytes;
     uint8_t* do_smem = q_smem + NS * C::kTileBytes;
     float* vec = reinterpret_cast<float*>(smem + C::kVecOff);  // [NS][lse2 128 | delta 128]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kKvBarOff);
     uint64_t* kv_full = bars;
     uint64_t* q_full = bars + 1;
     uint64_t* q_empty = q_full + NS;
     uint64_t* do_full = q_empty + NS;
     uint64_t* do_empty = do_full + NS;
     uint64_t* s_full = do_empty + NS;
-    uint64_t* p_ready = s_full + 1;
-    uint64_t* done = p_ready + 1;
+    uint64_t* dp_full = s_full + 1;
+    uint64_t* p_ready = dp_full + 1;
+    uint64_t* ds_ready = p_ready + 1;
+    uint64_t* done = ds_ready + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     unsigned* status = g_bwd_status;
@@ -474,7 +514,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&do_empty[s], 1);
         }
         mbar_init(s_full, 1);
+        mbar_init(dp_full, 1);
         mbar_init(p_ready, 256);
+        mbar_init(ds_ready, 256);
         mbar_init(done, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -487,6 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // TMEM columns: S^T [0, 128) (P^T packed over it), dP^T [128, 256) (dS^T
+    // packed over it), dV [256, 256 + D), dK [256 + D, 256 + 2D)
 
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ producers
@@ -528,6 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Order: S^T(0) dP^T(0), then per unit u: dV(u) S^T(u+1) dK(u) dP^T(u+1).
+        // The softmax warps hand over P^T (for dV) before dS^T (for dK) and keep
+        // P in registers, so S^T(u+1) can overwrite P^T(u) once dV(u) is issued.
         if (lane == 0) {
             const uint32_t tS = tmem_base, tdP = tmem_base + 128, tdV = tmem_base + 256, tdK = tmem_base + 256 + D;
             const uint32_t k_lo = sw128_desc_lo(smem_u32(k_smem), 16);
@@ -538,22 +585,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t domn_lo0 = sw128_desc_lo(smem_u32(do_smem), 16384);
             constexpr uint32_t kStageLo = C::kTileBytes >> 4;
             bool ok = mbar_wait(kv_full, 0, abort_flag, status, 0x22000000u);
-            Stage st;
-            for (int u = 0; ok && u < total; ++u) {
-                if (!(ok = mbar_wait(&q_full[st.s], st.ph, abort_flag, status, 0x23000000u | u))) break;
-                if (!(ok = mbar_wait(&do_full[st.s], st.ph, abort_flag, status, 0x24000000u | u))) break;
+            Stage cs, cd;  // stage of the next S^T (Q ring), of the next dP^T (dO ring)
+            auto issue_s = [&](int u) -> bool {
+                if (!mbar_wait(&q_full[cs.s], cs.ph, abort_flag, status, 0x23000000u | u)) return false;
                 tc_fence_after();
-                const uint32_t so = st.s * kStageLo;
-                mma_kmajor<D>(tS, k_lo, q_lo0 + so);
-                mma_kmajor<D>(tdP, v_lo, do_lo0 + so);
+                mma_kmajor<D>(tS, k_lo, q_lo0 + cs.s * kStageLo);
                 mma_commit(s_full);
+                cs.next(NS);
+                return true;
+            };
+            auto issue_dp = [&](int u) -> bool {
+                if (!mbar_wait(&do_full[cd.s], cd.ph, abort_flag, status, 0x24000000u | u)) return false;
+                tc_fence_after();
+                mma_kmajor<D>(tdP, v_lo, do_lo0 + cd.s * kStageLo);
+                mma_commit(dp_full);
+                cd.next(NS);
+                return true;
+            };
+            if (ok && total > 0) ok = issue_s(0) && issue_dp(0);
+            Stage cu;  // stage of unit u
+            for (int u = 0; ok && u < total; ++u) {
+                const uint32_t so = cu.s * kStageLo;
                 if (!(ok = mbar_wait(p_ready, u & 1, abort_flag, status, 0x25000000u | u))) break;
                 tc_fence_after();
                 mma_tmem_a<D>(tdV, tS, domn_lo0 + so, u > 0);
+                mma_commit(&do_empty[cu.s]);
+                if (u + 1 < total && !(ok = issue_s(u + 1))) break;
+                if (!(ok = mbar_wait(ds_ready, u & 1, abort_flag, status, 0x29000000u | u))) break;
+                tc_fence_after();
                 mma_tmem_a<D>(tdK, tdP, qmn_lo0 + so, u > 0);
-                mma_commit(&q_empty[st.s]);
-                mma_commit(&do_empty[st.s]);
-                st.next(NS);
+                mma_commit(&q_empty[cu.s]);
+                if (u + 1 < total && !(ok = issue_dp(u + 1))) break;
+                cu.next(NS);
             }
             mma_commit(done);
             mbar_wait(done, 0, abort_flag, status, 0);
@@ -572,39 +635,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int u = 0; u < total; ++u, it.next()) {
             if (!(ok = mbar_wait(s_full, u & 1, abort_flag, status, 0x26000000u | u))) break;
-            // the stage's lse2 / delta came with its Q tile (already landed: the MMAs read it)
+            // the stage's lse2 / delta came with its Q tile (already landed: the MMA read it)
             if (!(ok = mbar_wait(&q_full[st.s], st.ph, abort_flag, status, 0x27000000u | u))) break;
             tc_fence_after();
             // the diagonal query tile shows key row `key` to query columns c >= lane_row
             const int lo = (p.causal && it.a == j && it.qt == x_in) ? lane_row : 0;
             const float* lse2v = vec + st.s * 256;
             const float* dltv = lse2v + 128;
+            // P^T = exp(S^T - L) for this thread's half of the columns, packed over its S^T columns
+            float pr[64];
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int col0 = hw * 64 + c * 32;
-                uint32_t s[32], dp[32], pp[16], pd[16];
-                tmem_ld32(tS + col0, s);
-                tmem_ld32(tdP + col0, dp);
+                uint32_t sv[32], pp[16];
+                tmem_ld32(tS + col0, sv);
                 tmem_wait_ld();
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const int cc = col0 + 2 * jj;
                     const float2 L2 = *reinterpret_cast<const float2*>(lse2v + cc);
-                    const float2 DL = *reinterpret_cast<const float2*>(dltv + cc);
                     float y0, y1;
-                    ffma2(y0, y1, __uint_as_float(s[2 * jj]), __uint_as_float(s[2 * jj + 1]), sl2, sl2, -L2.x, -L2.y);
+                    ffma2(y0, y1, __uint_as_float(sv[2 * jj]), __uint_as_float(sv[2 * jj + 1]), sl2, sl2, -L2.x,
+                          -L2.y);
                     const float p0 = cc >= lo ? ex2_approx(y0) : 0.f;
                     const float p1 = cc + 1 >= lo ? ex2_approx(y1) : 0.f;
+                    pr[c * 32 + 2 * jj] = p0;
+                    pr[c * 32 + 2 * jj + 1] = p1;
                     pp[jj] = pack_bf16x2(p0, p1);
-                    pd[jj] = pack_bf16x2(p0 * (__uint_as_float(dp[2 * jj]) - DL.x),
-                                         p1 * (__uint_as_float(dp[2 * jj + 1]) - DL.y));
                 }
-                tmem_st16(tS + hw * 64 + c * 16, pp);   // P^T over this half's own S^T columns
-                tmem_st16(tdP + hw * 64 + c * 16, pd);  // dS^T over its own dP^T columns
+                tmem_st16(tS + hw * 64 + c * 16, pp);
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(p_ready);
+            // dS^T = P^T (dP^T - Delta), packed over this half's own dP^T columns
+            if (!(ok = mbar_wait(dp_full, u & 1, abort_flag, status, 0x2A000000u | u))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int col0 = hw * 64 + c * 32;
+                uint32_t dp[32], pd[16];
+                tmem_ld32(tdP + col0, dp);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int cc = col0 + 2 * jj;
+                    const float2 DL = *reinterpret_cast<const float2*>(dltv + cc);
+                    pd[jj] = pack_bf16x2(pr[c * 32 + 2 * jj] * (__uint_as_float(dp[2 * jj]) - DL.x),
+                                         pr[c * 32 + 2 * jj + 1] * (__uint_as_float(dp[2 * jj + 1]) - DL.y));
+                }
+                tmem_st16(tdP + hw * 64 + c * 16, pd);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(ds_ready);
             st.next(NS);
         }
         if (ok && mbar_wait(done, 0, abort_flag, status, 0x28000000u)) {
@@ -638,18 +722,18 @@ cudaError_t set_smem(K kernel, int bytes) {
 template <int D>
 cudaError_t launch_tc(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                       const CUtensorMap& tv, cudaStream_t stream) {
-    const int smem = BwdCfg<D>::kSmemBytes;
+    using C = BwdCfg<D>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = set_smem(bwd_dkdv_kernel<D>, smem);
-        if (attr_err == cudaSuccess) attr_err = set_smem(bwd_dq_kernel<D>, smem);
+        attr_err = set_smem(bwd_dkdv_kernel<D>, C::kKvSmem);
+        if (attr_err == cudaSuccess) attr_err = set_smem(bwd_dq_kernel<D>, C::kDqSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    bwd_dkdv_kernel<D><<<p.B * p.Hkv * p.n_tiles, kThreads, smem, stream>>>(tq, tdo, tk, tv, p);
+    bwd_dkdv_kernel<D><<<p.B * p.Hkv * p.n_tiles, kThreads, C::kKvSmem, stream>>>(tq, tdo, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_dq_kernel<D><<<p.B * p.Hq * p.n_tiles, kThreads, smem, stream>>>(tq, tdo, tk, tv, p);
+    bwd_dq_kernel<D><<<p.B * p.Hq * p.n_tiles, kThreads, C::kDqSmem, stream>>>(tq, tdo, tk, tv, p);
     return cudaGetLastError();
 }
 
