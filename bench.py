@@ -39,8 +39,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, valid only while the kernel source hashes to the recorded value.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the timed 32768-token configuration
-    # (bench.py --profile-case prefill_32k, third launch): 402892800 read + 242887168 written
-    "cb3b4188d4885b12": 645779968,
+    # (bench.py --profile-case prefill_32k, third launch): 403447808 read + 243494656 written
+    "61406eb08888aadf": 646942464,
 }
 
 
@@ -473,7 +473,7 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-PROFILE_CASES = ("prefill_32k", "prefill_16k", "fanout_decode", "fanout_decode1", "merge_16k")
+PROFILE_CASES = ("prefill_32k", "prefill_16k", "fanout_decode", "fanout_decode1", "merge_16k", "bwd_16k")
 
 
 def run_profile_case(case):
@@ -503,6 +503,17 @@ def run_profile_case(case):
         for _ in range(3):
             ra.fanout(x["q_rows"], x["offsets"], x["k_prefix"], x["v_prefix"], x["k_suffix"], x["v_suffix"],
                       workspace=ws)
+    elif case == "bwd_16k":
+        # backward of the causal GQA workload at 16384 tokens (Hq 32, Hkv 8, D 128): 3 calls
+        from ring_context_parallelism_gb300.inputs import randn
+        w = small(WORKLOADS[HEADLINE], S=16384)
+        q, k, v = attention_inputs(w, "cuda")
+        o, l = ra.attn(q, k, v, w.n_shards, w.block, True)
+        g = torch.Generator(device="cuda")
+        g.manual_seed(w.seed + 4242)
+        dO = randn(tuple(q.shape), g, q.dtype, "cuda")
+        for _ in range(3):
+            ra.attn_bwd(q, k, v, o, l, dO, w.n_shards, w.block, True)
     elif case == "merge_16k":
         # per-shard partials of a 16384-token, 64-head causal layer (16 shards), then 3 merges
         w = small(WORKLOADS["llama70b_layer_128k_partials"], S=16384)
