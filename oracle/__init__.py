@@ -61,7 +61,7 @@ def _bind(lib):
     vp, i, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
     lib.oracle_attention.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, i, i, vp, i64, vp, vp]
     lib.oracle_attention.restype = i
-    lib.oracle_fanout.argtypes = [vp, vp, i, i, vp, vp, i, vp, vp, i, i, i, i, i, vp, i64, vp, vp]
+    lib.oracle_fanout.argtypes = [vp, vp, i, i, vp, vp, i, vp, vp, i, i, i, i, i, i, vp, i64, vp, vp]
     lib.oracle_fanout.restype = i
     lib.oracle_lse_merge.argtypes = [vp, vp, i, i, i, i, i, vp, vp]
     lib.oracle_lse_merge.restype = i
@@ -194,12 +194,16 @@ def attention_bwd_rows(q, k, v, dout, *, dtype: str, causal: bool, qsel=None, ks
     return dq, dk, dv
 
 
-def fanout(q_rows, offsets, k_prefix, v_prefix, k_suffix, v_suffix, *, dtype: str, sel=None):
+def fanout(q_rows, offsets, k_prefix, v_prefix, k_suffix, v_suffix, *, dtype: str, sel=None,
+           suffix_causal: bool = False):
     """Shared-prefix fan-out attention in fp64.
 
     Follows "AHBM Agentic Runtime Architecture" sections 1.1, 3.2 and 5.2: the
     stacked rows of branch b (rows offsets[b]..offsets[b+1]) see the whole shared
     prefix plus branch b's own private suffix, never another branch's suffix.
+    ``suffix_causal`` (fan-out prefill, section 3.6): the n_b rows of branch b are
+    the last n_b tokens of its suffix; row t sees the suffix keys at positions
+    <= S_suffix - n_b + t.
 
     q_rows [R,Hq,D]; offsets int32 [nb+1]; k/v_prefix [Sp,Hkv,D];
     k/v_suffix [nb,Ss,Hkv,D].  Returns (O [R,Hq,D], lse [Hq,R]) float64, or
@@ -221,7 +225,7 @@ def fanout(q_rows, offsets, k_prefix, v_prefix, k_suffix, v_suffix, *, dtype: st
         lse = np.empty((Hq, R), np.float64)
     rc = _load().oracle_fanout(_ptr(q_rows), _ptr(offsets), nb, R, _ptr(k_prefix), _ptr(v_prefix), Sp,
                                _ptr(k_suffix), _ptr(v_suffix), Ss, Hq, Hkv, D, DTYPES[dtype],
-                               _ptr(sel), 0 if sel is None else sel.size, _ptr(out), _ptr(lse))
+                               int(bool(suffix_causal)), _ptr(sel), 0 if sel is None else sel.size, _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError("oracle_fanout rejected its arguments")
     return out, lse

@@ -210,13 +210,18 @@ int oracle_attention(const void* q, const void* k, const void* v, int dtype,
  *   q_rows [R,Hq,D]; branch b owns stacked rows [off[b], off[b+1]).
  *   k/v_prefix [Sp,Hkv,D] shared by every branch; k/v_suffix [nb,Ss,Hkv,D].
  *   Row r of branch b sees all Sp prefix keys and all Ss keys of suffix b.
+ *   suffix_causal (fan-out prefill, "AHBM Agentic Runtime Architecture" 3.6:
+ *   the branches' new tokens are prefilled together): the n_b new rows of
+ *   branch b are the last n_b tokens of its suffix, so its row t (t = 0 ..
+ *   n_b-1) sits at suffix position Ss - n_b + t and sees the suffix keys at
+ *   positions <= that one (and the whole prefix).
  *   sel ids encode (r,h) as r*Hq + h.  sel == NULL: out [R,Hq,D], lse [Hq,R];
  *   otherwise out [n_sel,D], lse [n_sel].
  */
 int oracle_fanout(const void* q_rows, const int32_t* off, int nb, int R,
                   const void* k_prefix, const void* v_prefix, int Sp,
                   const void* k_suffix, const void* v_suffix, int Ss,
-                  int Hq, int Hkv, int D, int dtype, const int64_t* sel, int64_t n_sel,
+                  int Hq, int Hkv, int D, int dtype, int suffix_causal, const int64_t* sel, int64_t n_sel,
                   double* out, double* lse) {
     if (R < 0 || nb <= 0 || Sp < 0 || Ss < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || D > 512)
         return -1;
@@ -250,7 +255,13 @@ int oracle_fanout(const void* q_rows, const int32_t* off, int nb, int R,
                 keys[n].off = ((int64_t)j * Hkv + hk) * D;
                 ++n;
             }
-            for (int j = 0; j < Ss; ++j) {
+            /* suffix keys this row sees: all, or up to its own suffix position */
+#if ORACLE_MUTANT == 11
+            const int last = suffix_causal ? Ss - (off[b + 1] - off[b]) + (r - off[b]) - 1 : Ss - 1; /* mutant */
+#else
+            const int last = suffix_causal ? Ss - (off[b + 1] - off[b]) + (r - off[b]) : Ss - 1;
+#endif
+            for (int j = 0; j < Ss && j <= last; ++j) {
                 keys[n].k = k_suffix;
                 keys[n].v = v_suffix;
                 keys[n].off = (((int64_t)b * Ss + j) * Hkv + hk) * D;

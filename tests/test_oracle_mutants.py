@@ -19,6 +19,7 @@ PINS = [
     lambda: pins.test_shard_partials_merge_to_unsharded(True),
     pins.test_fanout_equals_per_branch_attention_over_prefix_plus_suffix,
     lambda: layouts.test_oracle_on_stored_layout_equals_sequence_order("zigzag"),
+    pins.test_fanout_prefill_equals_causal_attention_over_prefix_plus_suffix,
     lambda: bwd_pins.test_bwd_finite_differences(True),
     lambda: bwd_pins.test_bwd_matches_torch_float64_autograd(True, 6, 2),
 ]
@@ -34,6 +35,7 @@ MUTANTS = {
     8: "causal mask on the stored order instead of sequence positions",
     9: "backward: softmax Jacobian's row term dropped",
     10: "backward: dK without the softmax scale",
+    11: "fan-out prefill: a row does not see its own suffix token",
 }
 
 

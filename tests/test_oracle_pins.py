@@ -331,6 +331,38 @@ def test_fanout_equals_per_branch_attention_over_prefix_plus_suffix():
     np.testing.assert_allclose(mL[0], lse, rtol=0, atol=1e-13)
 
 
+def test_fanout_prefill_equals_causal_attention_over_prefix_plus_suffix():
+    """Fan-out prefill ("AHBM Agentic Runtime Architecture", section 3.6): the new
+    rows of branch b are the last n_b tokens of its private suffix, so each is the
+    causal attention of the sequence prefix + suffix_b at that token's position."""
+    Sp, Ss, Hq, Hkv, D = 19, 7, 4, 2, 8
+    rows = [3, 7, 0, 1, 5]
+    nb = len(rows)
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    R = int(off[-1])
+    qr = _rand((R, Hq, D), 120)
+    kp, vp = _rand((Sp, Hkv, D), 121), _rand((Sp, Hkv, D), 122)
+    ks, vs = _rand((nb, Ss, Hkv, D), 123), _rand((nb, Ss, Hkv, D), 124)
+    O, lse = oracle.fanout(qr, off, kp, vp, ks, vs, dtype="f64", suffix_causal=True)
+    S = Sp + Ss
+    for b in range(nb):
+        n = rows[b]
+        if n == 0:
+            continue
+        kc = np.concatenate([kp, ks[b]])[None]
+        vc = np.concatenate([vp, vs[b]])[None]
+        qseq = np.zeros((1, S, Hq, D))
+        qseq[0, S - n:] = qr[off[b]: off[b + 1]]
+        ids = np.array([i * Hq + h for i in range(S - n, S) for h in range(Hq)], np.int64)
+        Ob, Lb = oracle.attention(qseq, kc, vc, dtype="f64", causal=True, sel=ids)
+        np.testing.assert_allclose(O[off[b]: off[b + 1]].reshape(-1, D), Ob, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[:, off[b]: off[b + 1]].T.reshape(-1), Lb, rtol=0, atol=1e-13)
+    # the last row of every branch sees its whole suffix: the same as the decode form
+    Od, Ld = oracle.fanout(qr, off, kp, vp, ks, vs, dtype="f64")
+    last = off[1:][np.array(rows) > 0] - 1
+    np.testing.assert_allclose(O[last], Od[last], rtol=0, atol=1e-13)
+
+
 def test_bf16_storage_is_widened_exactly():
     t = torch.randn(1, 16, 2, 8, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
     t = torch.cat([t, torch.tensor([1e-40, -3.0e38, 0.0, -0.0, 1.0, 2.0 ** -133, 65504.0, 3.0],
