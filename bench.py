@@ -39,8 +39,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, valid only while the kernel source hashes to the recorded value.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the timed 32768-token configuration
-    # (bench.py --profile-case prefill_32k, third launch): 403447808 read + 243494656 written
-    "61406eb08888aadf": 646942464,
+    # (bench.py --profile-case prefill_32k, third launch): 402941952 read + 243426560 written
+    "a41c2c2effa09505": 646368512,
 }
 
 
@@ -338,6 +338,29 @@ def run_ours(args, rank, world):
                             "frac_binding_roofline": bound_t / t, "algorithmic_bytes": by, "flops": fl_,
                             "workspace_bytes": ws.numel(), "launches_per_call": 2}
             del x, fo, fl, ws, graph
+
+        # fan-out prefill: 8 branches x 20 new rows, causal inside each 512-token private suffix
+        fw = WORKLOADS["fanout_prefill_8x20"]
+        x = fanout_inputs(fw, "cuda")
+        R = x["R"]
+        fo = torch.empty_like(x["q_rows"])
+        fl = torch.empty(fw.Hq, R, device="cuda", dtype=torch.float32)
+        ws = torch.empty(ra.fanout_workspace_size(R, fw.n_branches, fw.S_prefix, fw.S_suffix, fw.Hq, fw.Hkv, fw.D),
+                         dtype=torch.uint8, device="cuda")
+        pms = timed_steps(lambda: ra.fanout(x["q_rows"], x["offsets"], x["k_prefix"], x["v_prefix"], x["k_suffix"],
+                                            x["v_suffix"], out=fo, lse=fl, workspace=ws, prefill=True), 20, 5, flush)
+        ra.device_status()
+        t = statistics.median(pms) * 1e-3
+        n_b = x["rows"][0]
+        # visible keys per row: the whole prefix plus S_suffix - n_b + t + 1 suffix keys
+        vis = sum(fw.S_prefix + fw.S_suffix - n + tt + 1 for n in x["rows"] for tt in range(n))
+        pf = 4 * fw.D * fw.Hq * vis
+        by = fanout_bytes(R, fw.n_branches, fw.Hq, fw.Hkv, fw.D, fw.S_prefix, fw.S_suffix)
+        result["fanout_prefill_8x20"] = {"R": R, "rows_per_branch": n_b, "us": t * 1e6, "TFLOP_per_s": pf / t / 1e12,
+                                         "frac_bf16_peak": pf / t / 1e12 / pk["bf16_tflops"],
+                                         "GB_per_s": by / t / 1e9, "flops": pf, "algorithmic_bytes": by,
+                                         "launches_per_call": 2}
+        del x, fo, fl, ws
 
         # per-shard partials + LSE merge on the Llama-3-70B-shaped layer
         pw = WORKLOADS["llama70b_layer_128k_partials"]

@@ -222,8 +222,26 @@ ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, i
                                 float* lse, int Hq, int Hkv, int D, ra_dtype dt, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace ra_prefix_fanout_attn needs for these sizes on the current
- * device (0 if the sizes are invalid). */
+/*
+ * Shared-prefix fan-out PREFILL ("AHBM Agentic Runtime Architecture", section
+ * 3.6: the new tokens of all branches -- e.g. 8 sub-agents x 20 tokens -- are
+ * processed together against the shared prefix; section 3.1: each branch's
+ * private pages follow the shared ones).  Same arguments, layouts, workspace
+ * and errors as ra_prefix_fanout_attn; the difference is the mask inside a
+ * private suffix: the n_b new rows of branch b are the last n_b tokens of its
+ * suffix, so its row t (t = 0 .. n_b-1) sits at suffix position
+ * S_suffix - n_b + t and sees the suffix keys at positions <= that one, plus
+ * the whole prefix.  (A branch with n_b > S_suffix has rows that see no suffix
+ * key.)  The last row of each branch gets the ra_prefix_fanout_attn result.
+ */
+ra_status ra_prefix_fanout_prefill(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                                   const void* k_prefix, const void* v_prefix, int S_prefix,
+                                   const void* k_suffix, const void* v_suffix, int S_suffix, void* out,
+                                   float* lse, int Hq, int Hkv, int D, ra_dtype dt, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace ra_prefix_fanout_attn (and ra_prefix_fanout_prefill)
+ * needs for these sizes on the current device (0 if the sizes are invalid). */
 size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int S_suffix, int Hq,
                                        int Hkv, int D, ra_dtype dt);
 

@@ -61,6 +61,7 @@ struct TcParams {
     int split_prefix;   // prefix units hold one row tile: split their KV tiles over both tile slots
     int suffix_slot0;   // partial slot of the suffix (suffix units; only without a prefix)
     int fold;           // suffixes folded into prefix units: branch b into chunk b % n_chunks
+    int suffix_causal;  // fan-out prefill: a branch's rows are the last tokens of its suffix, causal inside it
     int chunk_start[kMaxChunks + 1];  // prefix tile where chunk c starts
     const int* offsets;
     float scale_log2;
@@ -867,6 +868,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lim = min(lim, wi.key_end - 1 - tile_kb);
                 // rows of another branch (a folded suffix) or past the stacked rows
                 if (row < wi.row_lo || row >= wi.row_hi) lim = -1;
+                // prefill: row t of a branch of n rows sits at suffix position S_suffix - n + t
+                if (p.suffix_causal && wi.seg == 1)
+                    lim = min(lim, wi.key_end - (wi.row_hi - wi.row_lo) + (row - wi.row_lo) - tile_kb);
             }
             if (FAN && __all_sync(0xffffffffu, lim < 0)) {
                 // No row of this warp sees a key of this tile: P = 0 (written over
@@ -1241,6 +1245,7 @@ cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
     fanout_slots(a.R, a.Hq, a.Hkv, a.S_prefix > 0 ? a.n_chunks : 0, a.S_prefix, a.S_suffix, &p.split_prefix,
                  &p.suffix_slot0);
     p.fold = (a.S_prefix > 0 && a.S_suffix > 0) ? 1 : 0;
+    p.suffix_causal = a.suffix_causal;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
     p.out = a.part;
     const unsigned long long D = a.D, esz = 2;

@@ -259,10 +259,11 @@ size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int 
     return plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D).total;
 }
 
-ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, int n_branches, int R,
-                                const void* k_prefix, const void* v_prefix, int S_prefix, const void* k_suffix,
-                                const void* v_suffix, int S_suffix, void* out, float* lse, int Hq, int Hkv, int D,
-                                ra_dtype dt, void* workspace, size_t workspace_bytes, void* stream) {
+static ra_status fanout_common(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                               const void* k_prefix, const void* v_prefix, int S_prefix, const void* k_suffix,
+                               const void* v_suffix, int S_suffix, void* out, float* lse, int Hq, int Hkv, int D,
+                               ra_dtype dt, void* workspace, size_t workspace_bytes, void* stream,
+                               int suffix_causal) {
     ra_status st = check_fanout(q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix, k_suffix,
                                 v_suffix, S_suffix, out, Hq, Hkv, D, dt);
     if (st != RA_OK) return st;
@@ -300,6 +301,7 @@ ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, i
     a.part.lse_h = R;
     a.part.lse_part = static_cast<long long>(Hq) * R;
     a.part.o_f32 = 1;
+    a.suffix_causal = suffix_causal;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = ra::launch_fanout_tc(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "fan-out attention launch");
@@ -307,6 +309,22 @@ ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, i
     e = ra::launch_lse_merge(m, s);
     if (e != cudaSuccess) return cuda_fail(e, "fan-out merge launch");
     return ok();
+}
+
+ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                                const void* k_prefix, const void* v_prefix, int S_prefix, const void* k_suffix,
+                                const void* v_suffix, int S_suffix, void* out, float* lse, int Hq, int Hkv, int D,
+                                ra_dtype dt, void* workspace, size_t workspace_bytes, void* stream) {
+    return fanout_common(q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix, k_suffix, v_suffix,
+                         S_suffix, out, lse, Hq, Hkv, D, dt, workspace, workspace_bytes, stream, 0);
+}
+
+ra_status ra_prefix_fanout_prefill(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                                   const void* k_prefix, const void* v_prefix, int S_prefix, const void* k_suffix,
+                                   const void* v_suffix, int S_suffix, void* out, float* lse, int Hq, int Hkv,
+                                   int D, ra_dtype dt, void* workspace, size_t workspace_bytes, void* stream) {
+    return fanout_common(q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix, k_suffix, v_suffix,
+                         S_suffix, out, lse, Hq, Hkv, D, dt, workspace, workspace_bytes, stream, 1);
 }
 
 ra_status ra_prefix_fanout_attn_noalloc(const void* q_rows, const int* branch_offsets, int n_branches, int R,

@@ -42,6 +42,7 @@ struct FanoutTcArgs {
     int n_chunks;               // prefix split
     int chunk_start[65];        // prefix tile where chunk c starts (n_chunks + 1 entries)
     OutDesc part;               // fp32 partials [P][R][Hq][D], lse [P][Hq][R]
+    int suffix_causal = 0;      // prefill: causal inside each branch's suffix
 };
 cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream);
 

@@ -73,6 +73,9 @@ WORKLOADS = {
                                          64, 128, 1005, key_boost_frac=0.01),
     "fanout_decode": FanoutWorkload("fanout_decode", 65536, 512, 16, 1, 16, 64, 8, 128, "bf16", 1004),
     "fanout_decode1": FanoutWorkload("fanout_decode1", 65536, 512, 16, 1, 1, 64, 8, 128, "bf16", 1004),
+    # fan-out prefill: 8 sub-agents x 20 new tokens (M = 160 stacked rows), each the tail of a
+    # 512-token private suffix, against the 65536-token shared prefix
+    "fanout_prefill_8x20": FanoutWorkload("fanout_prefill_8x20", 65536, 512, 8, 20, 20, 64, 8, 128, "bf16", 1006),
 }
 
 

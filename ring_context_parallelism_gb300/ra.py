@@ -38,6 +38,8 @@ SIGNATURES = {
     "ra_lse_merge": (_i, [_vp, _fp, _vp, _fp, _i, _i, _i, _i, _i, _i, _vp]),
     "ra_prefix_fanout_attn": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _fp, _i, _i, _i, _i,
                                    _vp, _sz, _vp]),
+    "ra_prefix_fanout_prefill": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _fp, _i, _i, _i, _i,
+                                      _vp, _sz, _vp]),
     "ra_prefix_fanout_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "ra_prefix_fanout_attn_noalloc": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _fp, _i, _i, _i, _i,
                                            _vp]),
@@ -206,9 +208,10 @@ def fanout_workspace_size(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D, dtype=t
 
 
 def fanout(q_rows, branch_offsets, k_prefix, v_prefix, k_suffix, v_suffix, out=None, lse=None, workspace=None,
-           want_lse: bool = True):
+           want_lse: bool = True, prefill: bool = False):
     """Shared-prefix fan-out attention.  q_rows [R,Hq,D]; branch_offsets int32 [nb+1] (device);
-    k/v_prefix [Sp,Hkv,D]; k/v_suffix [nb,Ss,Hkv,D].  Returns (out [R,Hq,D], lse [Hq,R])."""
+    k/v_prefix [Sp,Hkv,D]; k/v_suffix [nb,Ss,Hkv,D].  Returns (out [R,Hq,D], lse [Hq,R]).
+    prefill=True: a branch's rows are the last tokens of its suffix, causal inside it."""
     R, Hq, D = q_rows.shape
     Sp, Hkv, _ = k_prefix.shape
     nb, Ss = k_suffix.shape[0], k_suffix.shape[1]
@@ -222,9 +225,10 @@ def fanout(q_rows, branch_offsets, k_prefix, v_prefix, k_suffix, v_suffix, out=N
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=q_rows.device, dtype=torch.uint8)
     dev = _cuda(q_rows, branch_offsets, k_prefix, v_prefix, k_suffix, v_suffix, out, lse, workspace)
-    _check(load().ra_prefix_fanout_attn(_ptr(q_rows), _ptr(branch_offsets), nb, R, _ptr(k_prefix), _ptr(v_prefix),
-                                        Sp, _ptr(k_suffix), _ptr(v_suffix), Ss, _ptr(out), _ptr(lse), Hq, Hkv, D,
-                                        _dt(q_rows), _ptr(workspace), workspace.numel(), _stream(dev)))
+    fn = load().ra_prefix_fanout_prefill if prefill else load().ra_prefix_fanout_attn
+    _check(fn(_ptr(q_rows), _ptr(branch_offsets), nb, R, _ptr(k_prefix), _ptr(v_prefix), Sp, _ptr(k_suffix),
+              _ptr(v_suffix), Ss, _ptr(out), _ptr(lse), Hq, Hkv, D, _dt(q_rows), _ptr(workspace), workspace.numel(),
+              _stream(dev)))
     return out, lse
 
 

@@ -300,6 +300,29 @@ def test_fanout_full(Sp, Ss, rows, Hq, Hkv, D):
     _close(L.cpu().double().numpy(), rL, 1e-3, "lse")
 
 
+@pytest.mark.parametrize("Sp,Ss,rows,Hq,Hkv,D", [
+    (1000, 200, [3, 0, 16, 1, 7], 16, 2, 128),     # ragged prefix and suffix tails, an empty branch
+    (8192, 160, [20] * 8, 64, 8, 128),             # 8 agents x 20 rows against 8192 prefix columns
+    (0, 300, [2, 9], 8, 1, 128),                   # no shared prefix: suffix units
+    (640, 128, [33, 5], 8, 2, 64),                 # a branch with more rows than one tile pair
+    (1500, 24, [40, 10, 16], 16, 4, 64),           # more rows than suffix tokens: some rows see none
+    (3000, 256, [16, 16, 16], 64, 8, 128),         # last row pair holds a single row tile
+])
+def test_fanout_prefill_full(Sp, Ss, rows, Hq, Hkv, D):
+    """Fan-out prefill: a branch's rows are the last tokens of its suffix, causal inside it."""
+    w = small(WORKLOADS["fanout_prefill_8x20"], S_prefix=Sp, S_suffix=Ss, n_branches=len(rows), Hq=Hq, Hkv=Hkv,
+              D=D, seed=600 + Sp + Ss)
+    x = fanout_inputs(w, "cpu", rows=rows)
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    O, L = ra.fanout(dev["q_rows"], dev["offsets"], dev["k_prefix"], dev["v_prefix"], dev["k_suffix"],
+                     dev["v_suffix"], prefill=True)
+    ra.device_status()
+    st = [storage(x[k])[0] for k in ("q_rows", "k_prefix", "v_prefix", "k_suffix", "v_suffix")]
+    rO, rL = oracle.fanout(st[0], x["offsets"].numpy(), *st[1:], dtype="bf16", suffix_causal=True)
+    _close(O.float().cpu().double().numpy(), rO, 2e-2, "O")
+    _close(L.cpu().double().numpy(), rL, 1e-3, "lse")
+
+
 # ------------------------------------------------------------------------------------------
 # full-size workloads, sampled outputs
 # ------------------------------------------------------------------------------------------
@@ -351,6 +374,22 @@ def test_fanout_decode1_full_size():
     rO, rL = _oracle_fanout(x)
     _close(O.float().cpu().double().numpy(), rO, 2e-2, "O")
     _close(L.cpu().double().numpy(), rL, 1e-3, "lse")
+
+
+def test_fanout_prefill_8x20_full_size():
+    w = WORKLOADS["fanout_prefill_8x20"]
+    x = fanout_inputs(w, "cuda")
+    O, L = ra.fanout(x["q_rows"], x["offsets"], x["k_prefix"], x["v_prefix"], x["k_suffix"], x["v_suffix"],
+                     prefill=True)
+    ra.device_status()
+    xc = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in x.items()}
+    R, Hq = x["R"], w.Hq
+    ids = torch.unique(torch.cat([torch.randperm(R * Hq, generator=torch.Generator().manual_seed(6))[:320],
+                                  torch.arange(0, Hq), torch.arange((R - 1) * Hq, R * Hq)])).numpy()
+    st = [storage(xc[k])[0] for k in ("q_rows", "k_prefix", "v_prefix", "k_suffix", "v_suffix")]
+    rO, rL = oracle.fanout(st[0], xc["offsets"].numpy(), *st[1:], dtype="bf16", sel=ids, suffix_causal=True)
+    _close(O.reshape(-1, w.D).float().cpu().numpy()[ids], rO, 2e-2, "O (sampled)")
+    _close(L.t().reshape(-1).cpu().numpy()[ids], rL, 1e-3, "lse (sampled)")
 
 
 def test_million_token_stress_sampled():
