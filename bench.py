@@ -339,6 +339,35 @@ def run_ours(args, rank, world):
                             "workspace_bytes": ws.numel(), "launches_per_call": 2}
             del x, fo, fl, ws, graph
 
+        # the R = 16 decode mix over a paged KV cache (16-token pages, shuffled pool)
+        fw = WORKLOADS["fanout_decode1"]
+        x = fanout_inputs(fw, "cuda")
+        R, P = x["R"], 16
+        gp = torch.Generator(device="cpu").manual_seed(fw.seed + 99)
+        npp, nsp = fw.S_prefix // P, fw.S_suffix // P
+        n_pages = npp + fw.n_branches * nsp
+        order = torch.randperm(n_pages, generator=gp).to(torch.int32).cuda()
+        pp, sp = order[:npp].contiguous(), order[npp:].reshape(fw.n_branches, nsp).contiguous()
+        kpool = torch.empty(n_pages, P, fw.Hkv, fw.D, dtype=x["k_prefix"].dtype, device="cuda")
+        vpool = torch.empty_like(kpool)
+        kpool[pp.long()] = x["k_prefix"].reshape(npp, P, fw.Hkv, fw.D)
+        vpool[pp.long()] = x["v_prefix"].reshape(npp, P, fw.Hkv, fw.D)
+        kpool[sp.long().reshape(-1)] = x["k_suffix"].reshape(-1, P, fw.Hkv, fw.D)
+        vpool[sp.long().reshape(-1)] = x["v_suffix"].reshape(-1, P, fw.Hkv, fw.D)
+        fo = torch.empty_like(x["q_rows"])
+        fl = torch.empty(fw.Hq, R, device="cuda", dtype=torch.float32)
+        ws = torch.empty(ra.fanout_workspace_size(R, fw.n_branches, fw.S_prefix, fw.S_suffix, fw.Hq, fw.Hkv, fw.D),
+                         dtype=torch.uint8, device="cuda")
+        gms = timed_steps(lambda: ra.fanout_paged(x["q_rows"], x["offsets"], kpool, vpool, pp, fw.S_prefix, sp,
+                                                  fw.S_suffix, out=fo, lse=fl, workspace=ws), 20, 5, flush)
+        ra.device_status()
+        t = statistics.median(gms) * 1e-3
+        by = fanout_bytes(R, fw.n_branches, fw.Hq, fw.Hkv, fw.D, fw.S_prefix, fw.S_suffix)
+        result["fanout_decode1_paged16"] = {"R": R, "page_size": P, "us": t * 1e6, "GB_per_s": by / t / 1e9,
+                                            "frac_hbm": by / t / 1e9 / pk["hbm_gbs"], "algorithmic_bytes": by,
+                                            "launches_per_call": 2}
+        del x, kpool, vpool, fo, fl, ws
+
         # fan-out prefill: 8 branches x 20 new rows, causal inside each 512-token private suffix
         fw = WORKLOADS["fanout_prefill_8x20"]
         x = fanout_inputs(fw, "cuda")

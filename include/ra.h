@@ -240,8 +240,36 @@ ra_status ra_prefix_fanout_prefill(const void* q_rows, const int* branch_offsets
                                    float* lse, int Hq, int Hkv, int D, ra_dtype dt, void* workspace,
                                    size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace ra_prefix_fanout_attn (and ra_prefix_fanout_prefill)
- * needs for these sizes on the current device (0 if the sizes are invalid). */
+/*
+ * Fan-out over a PAGED KV cache ("AHBM Agentic Runtime Architecture", section
+ * 3.1: the branches' page tables list the shared prefix pages, referenced by
+ * every branch without copying, followed by each branch's private pages).
+ *
+ *   k_pages, v_pages [n_pages, page_size, Hkv, D] dtype dt: the page pools.
+ *   page_size      power of two, 8 <= page_size <= 2^20.
+ *   prefix_pages   int32 device array [ceil(S_prefix / page_size)]: the shared
+ *                  prefix's pages in order (key k is row k % page_size of page
+ *                  prefix_pages[k / page_size]).
+ *   suffix_pages   int32 device array [n_branches][ceil(S_suffix / page_size)]:
+ *                  each branch's private pages in order.
+ *   prefill        0: ra_prefix_fanout_attn semantics; 1: ra_prefix_fanout_prefill.
+ * Page indices are checked on the device: one outside [0, n_pages) records
+ * RA_ERR_INVALID_ARG (reported by ra_device_status) and its keys read as zeros.
+ * The rows of a sequence's last page past S_prefix / S_suffix are read and
+ * given weight zero: they must hold finite values (zeros, or stale keys).
+ * Each prefix tile is still read from HBM once per KV head for all rows.
+ * Other arguments, the workspace (ra_prefix_fanout_workspace_size with the
+ * same R, n_branches, S_prefix, S_suffix) and errors as ra_prefix_fanout_attn.
+ */
+ra_status ra_prefix_fanout_attn_paged(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                                      const void* k_pages, const void* v_pages, int n_pages, int page_size,
+                                      const int* prefix_pages, int S_prefix, const int* suffix_pages,
+                                      int S_suffix, void* out, float* lse, int Hq, int Hkv, int D, ra_dtype dt,
+                                      int prefill, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace ra_prefix_fanout_attn (and ra_prefix_fanout_prefill,
+ * ra_prefix_fanout_attn_paged) needs for these sizes on the current device (0
+ * if the sizes are invalid). */
 size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int S_suffix, int Hq,
                                        int Hkv, int D, ra_dtype dt);
 

@@ -231,6 +231,33 @@ def fanout(q_rows, offsets, k_prefix, v_prefix, k_suffix, v_suffix, *, dtype: st
     return out, lse
 
 
+def fanout_paged(q_rows, offsets, k_pages, v_pages, prefix_pages, S_prefix, suffix_pages, S_suffix, *,
+                 dtype: str, sel=None, suffix_causal: bool = False):
+    """Shared-prefix fan-out over a paged KV cache, fp64.
+
+    Follows "AHBM Agentic Runtime Architecture" section 3.1: a branch's context
+    is its page table, the shared prefix pages (the same pages for every branch)
+    followed by its private pages.  Key k of the prefix is row k % page_size of
+    page prefix_pages[k // page_size]; likewise for branch b's suffix with
+    suffix_pages[b].  The pages are gathered into the prefix and suffix tensors
+    and the result is ``fanout`` of those.
+
+    k_pages, v_pages [n_pages, page_size, Hkv, D]; prefix_pages [n_prefix_pages];
+    suffix_pages [nb, n_suffix_pages] (integer page indices)."""
+    k_pages = _as_storage(k_pages, dtype)
+    v_pages = _as_storage(v_pages, dtype)
+    _, P, Hkv, D = k_pages.shape
+    pre = np.asarray(prefix_pages, np.int64)
+    suf = np.asarray(suffix_pages, np.int64)
+    nb = suf.shape[0]
+    kp = k_pages[pre].reshape(-1, Hkv, D)[:S_prefix]
+    vp = v_pages[pre].reshape(-1, Hkv, D)[:S_prefix]
+    ks = k_pages[suf.reshape(-1)].reshape(nb, -1, Hkv, D)[:, :S_suffix]
+    vs = v_pages[suf.reshape(-1)].reshape(nb, -1, Hkv, D)[:, :S_suffix]
+    return fanout(q_rows, offsets, np.ascontiguousarray(kp), np.ascontiguousarray(vp), np.ascontiguousarray(ks),
+                  np.ascontiguousarray(vs), dtype=dtype, sel=sel, suffix_causal=suffix_causal)
+
+
 def lse_merge(part_O, part_lse):
     """Row-indexed log-sum-exp merge of partial states, fp64.
 

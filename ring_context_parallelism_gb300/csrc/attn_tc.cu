@@ -62,6 +62,12 @@ struct TcParams {
     int suffix_slot0;   // partial slot of the suffix (suffix units; only without a prefix)
     int fold;           // suffixes folded into prefix units: branch b into chunk b % n_chunks
     int suffix_causal;  // fan-out prefill: a branch's rows are the last tokens of its suffix, causal inside it
+    // paged KV: the K/V maps address a page pool [n_pages * page_size, Hkv, D];
+    // key k of the prefix lives in page prefix_pages[k >> page_shift], key k of
+    // branch b's suffix in page suffix_pages[b * n_suffix_pages + (k >> page_shift)]
+    int paged, page_shift, n_pages, n_prefix_pages, n_suffix_pages;
+    const int* prefix_pages;
+    const int* suffix_pages;
     int chunk_start[kMaxChunks + 1];  // prefix tile where chunk c starts
     const int* offsets;
     float scale_log2;
@@ -553,9 +559,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 mbar_arrive_expect_tx(&full[cs.s], C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(map, &full[cs.s], ring + cs.s * C::kTileBytes + c * 16384, c * 64, u.kv_head,
-                                wi.key(), z);
+                if (FAN && p.paged) {
+                    // one box per page (or per 128 rows of a larger page); a 128B-swizzled
+                    // tile is the same bytes whether it lands in one box or several
+                    // (every sub-box starts on a 1024-byte swizzle atom).  Pages past
+                    // the listed ones, and invalid page indices, load zeros from past
+                    // the pool (those keys are masked, or reported).
+                    const int* table = from_suffix ? p.suffix_pages + static_cast<long long>(wi.b) * p.n_suffix_pages
+                                                   : p.prefix_pages;
+                    const int n_listed = from_suffix ? p.n_suffix_pages : p.n_prefix_pages;
+                    const int page_size = 1 << p.page_shift;
+                    const int sub_rows = page_size < kTileN ? page_size : kTileN;
+                    for (int r0 = 0; r0 < kTileN; r0 += sub_rows) {
+                        const int lk = wi.key() + r0;
+                        const int lp = lk >> p.page_shift;
+                        int row = p.n_pages << p.page_shift;
+                        if (lp < n_listed) {
+                            const int pg = table[lp];
+                            if (pg >= 0 && pg < p.n_pages) {
+                                row = (pg << p.page_shift) + (lk - (lp << p.page_shift));
+                            } else {
+                                atomicCAS(&g_tc_status[0], 0u, kDevInvalidArg);
+                                atomicCAS(&g_tc_status[1], 0u, 0x0E000000u | static_cast<unsigned>(lp & 0xFFFFFF));
+                            }
+                        }
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_4d(map, &full[cs.s], ring + cs.s * C::kTileBytes + c * 16384 + r0 * 128, c * 64,
+                                        u.kv_head, row, 0);
+                    }
+                } else {
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_4d(map, &full[cs.s], ring + cs.s * C::kTileBytes + c * 16384, c * 64, u.kv_head,
+                                    wi.key(), z);
+                }
                 cs.next(n_stages);
                 ++issued;
             }
@@ -1246,6 +1282,13 @@ cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
                  &p.suffix_slot0);
     p.fold = (a.S_prefix > 0 && a.S_suffix > 0) ? 1 : 0;
     p.suffix_causal = a.suffix_causal;
+    p.paged = a.paged;
+    p.page_shift = a.page_shift;
+    p.n_pages = a.n_pages;
+    p.n_prefix_pages = a.n_prefix_pages;
+    p.n_suffix_pages = a.n_suffix_pages;
+    p.prefix_pages = a.prefix_pages;
+    p.suffix_pages = a.suffix_pages;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a.D)));
     p.out = a.part;
     const unsigned long long D = a.D, esz = 2;
@@ -1265,17 +1308,27 @@ cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
     const void* vp = a.S_prefix > 0 ? a.v_prefix : a.v_suffix;
     const void* ksf = a.S_suffix > 0 ? a.k_suffix : a.k_prefix;
     const void* vsf = a.S_suffix > 0 ? a.v_suffix : a.v_prefix;
-    if (a.S_prefix > 0) {
+    if (a.paged) {
+        // both segments read the page pool, in boxes of one page (at most 128 rows)
+        const unsigned long long rows = static_cast<unsigned long long>(a.n_pages) << a.page_shift;
+        const unsigned long long pd[4] = {D, (unsigned long long)a.Hkv, rows, 1};
+        const unsigned long long ps[3] = {D * esz, D * esz * a.Hkv, D * esz * a.Hkv * rows};
+        const unsigned pbox[4] = {64, 1, (unsigned)((1 << a.page_shift) < 128 ? (1 << a.page_shift) : 128), 1};
+        if (!make_map(&tk, a.k_prefix, pd, ps, pbox) || !make_map(&tv, a.v_prefix, pd, ps, pbox))
+            return cudaErrorInvalidValue;
+        tk2 = tk;
+        tv2 = tv;
+    } else if (a.S_prefix > 0) {
         if (!make_map(&tk, kp, kd, ks, box) || !make_map(&tv, vp, kd, ks, box)) return cudaErrorInvalidValue;
     }
-    if (a.S_suffix > 0) {
+    if (!a.paged && a.S_suffix > 0) {
         if (!make_map(&tk2, ksf, sd, ss, box) || !make_map(&tv2, vsf, sd, ss, box)) return cudaErrorInvalidValue;
     }
-    if (a.S_prefix == 0) {
+    if (!a.paged && a.S_prefix == 0) {
         tk = tk2;
         tv = tv2;
     }
-    if (a.S_suffix == 0) {
+    if (!a.paged && a.S_suffix == 0) {
         tk2 = tk;
         tv2 = tv;
     }

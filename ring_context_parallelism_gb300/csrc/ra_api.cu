@@ -259,11 +259,18 @@ size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int 
     return plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D).total;
 }
 
+// Paged KV of a fan-out call (all zero: contiguous prefix / suffix tensors).
+struct PagedKv {
+    int paged = 0, page_shift = 0, n_pages = 0;
+    const int* prefix_pages = nullptr;
+    const int* suffix_pages = nullptr;
+};
+
 static ra_status fanout_common(const void* q_rows, const int* branch_offsets, int n_branches, int R,
                                const void* k_prefix, const void* v_prefix, int S_prefix, const void* k_suffix,
                                const void* v_suffix, int S_suffix, void* out, float* lse, int Hq, int Hkv, int D,
                                ra_dtype dt, void* workspace, size_t workspace_bytes, void* stream,
-                               int suffix_causal) {
+                               int suffix_causal, const PagedKv& pg = PagedKv()) {
     ra_status st = check_fanout(q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix, k_suffix,
                                 v_suffix, S_suffix, out, Hq, Hkv, D, dt);
     if (st != RA_OK) return st;
@@ -302,6 +309,16 @@ static ra_status fanout_common(const void* q_rows, const int* branch_offsets, in
     a.part.lse_part = static_cast<long long>(Hq) * R;
     a.part.o_f32 = 1;
     a.suffix_causal = suffix_causal;
+    if (pg.paged) {
+        const int page_size = 1 << pg.page_shift;
+        a.paged = 1;
+        a.page_shift = pg.page_shift;
+        a.n_pages = pg.n_pages;
+        a.n_prefix_pages = (S_prefix + page_size - 1) / page_size;
+        a.n_suffix_pages = (S_suffix + page_size - 1) / page_size;
+        a.prefix_pages = pg.prefix_pages;
+        a.suffix_pages = pg.suffix_pages;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = ra::launch_fanout_tc(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "fan-out attention launch");
@@ -325,6 +342,31 @@ ra_status ra_prefix_fanout_prefill(const void* q_rows, const int* branch_offsets
                                    int D, ra_dtype dt, void* workspace, size_t workspace_bytes, void* stream) {
     return fanout_common(q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix, k_suffix, v_suffix,
                          S_suffix, out, lse, Hq, Hkv, D, dt, workspace, workspace_bytes, stream, 1);
+}
+
+ra_status ra_prefix_fanout_attn_paged(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                                      const void* k_pages, const void* v_pages, int n_pages, int page_size,
+                                      const int* prefix_pages, int S_prefix, const int* suffix_pages, int S_suffix,
+                                      void* out, float* lse, int Hq, int Hkv, int D, ra_dtype dt, int prefill,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+    if (page_size < 8 || (page_size & (page_size - 1)) || page_size > (1 << 20))
+        return fail(RA_ERR_INVALID_ARG, "page_size must be a power of two in [8, 2^20] (got %d)", page_size);
+    if (n_pages < 1 || static_cast<long long>(n_pages) * page_size > (1ll << 31) - 1)
+        return fail(RA_ERR_INVALID_ARG, "n_pages must be >= 1 and n_pages * page_size < 2^31");
+    if (prefill != 0 && prefill != 1) return fail(RA_ERR_INVALID_ARG, "prefill must be 0 or 1");
+    if ((S_prefix > 0 && !prefix_pages) || (S_suffix > 0 && !suffix_pages))
+        return fail(RA_ERR_INVALID_ARG, "null page table");
+    if ((reinterpret_cast<uintptr_t>(prefix_pages) & 3u) || (reinterpret_cast<uintptr_t>(suffix_pages) & 3u))
+        return fail(RA_ERR_INVALID_ARG, "page tables misaligned");
+    PagedKv pg;
+    pg.paged = 1;
+    while ((1 << pg.page_shift) < page_size) ++pg.page_shift;
+    pg.n_pages = n_pages;
+    pg.prefix_pages = prefix_pages;
+    pg.suffix_pages = suffix_pages;
+    // the pools stand in for both the prefix and the suffix tensors
+    return fanout_common(q_rows, branch_offsets, n_branches, R, k_pages, v_pages, S_prefix, k_pages, v_pages,
+                         S_suffix, out, lse, Hq, Hkv, D, dt, workspace, workspace_bytes, stream, prefill, pg);
 }
 
 ra_status ra_prefix_fanout_attn_noalloc(const void* q_rows, const int* branch_offsets, int n_branches, int R,
@@ -486,6 +528,8 @@ ra_status ra_device_status(void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "device status");
     if (code == RA_ERR_DEVICE_TIMEOUT)
         return fail(RA_ERR_DEVICE_TIMEOUT, "%s: bounded device wait ran out (site 0x%08x)", who, where);
+    if (code == RA_ERR_INVALID_ARG && (where >> 24) == 0x0E)
+        return fail(RA_ERR_INVALID_ARG, "%s: page table entry %u is outside the page pool", who, where & 0xFFFFFFu);
     if (code == RA_ERR_INVALID_ARG)
         return fail(RA_ERR_INVALID_ARG, "%s: device-side argument check failed (0x%08x)", who, where);
     if (code) return fail(static_cast<ra_status>(code), "%s: device status %u", who, code);

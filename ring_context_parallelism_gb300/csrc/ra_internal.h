@@ -43,6 +43,10 @@ struct FanoutTcArgs {
     int chunk_start[65];        // prefix tile where chunk c starts (n_chunks + 1 entries)
     OutDesc part;               // fp32 partials [P][R][Hq][D], lse [P][Hq][R]
     int suffix_causal = 0;      // prefill: causal inside each branch's suffix
+    // paged KV (k_prefix / v_prefix then point at the page pools [n_pages, page_size, Hkv, D])
+    int paged = 0, page_shift = 0, n_pages = 0, n_prefix_pages = 0, n_suffix_pages = 0;
+    const int* prefix_pages = nullptr;
+    const int* suffix_pages = nullptr;
 };
 cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream);
 

@@ -40,6 +40,8 @@ SIGNATURES = {
                                    _vp, _sz, _vp]),
     "ra_prefix_fanout_prefill": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _fp, _i, _i, _i, _i,
                                       _vp, _sz, _vp]),
+    "ra_prefix_fanout_attn_paged": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _vp, _fp, _i, _i, _i,
+                                         _i, _i, _vp, _sz, _vp]),
     "ra_prefix_fanout_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "ra_prefix_fanout_attn_noalloc": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _fp, _i, _i, _i, _i,
                                            _vp]),
@@ -229,6 +231,33 @@ def fanout(q_rows, branch_offsets, k_prefix, v_prefix, k_suffix, v_suffix, out=N
     _check(fn(_ptr(q_rows), _ptr(branch_offsets), nb, R, _ptr(k_prefix), _ptr(v_prefix), Sp, _ptr(k_suffix),
               _ptr(v_suffix), Ss, _ptr(out), _ptr(lse), Hq, Hkv, D, _dt(q_rows), _ptr(workspace), workspace.numel(),
               _stream(dev)))
+    return out, lse
+
+
+def fanout_paged(q_rows, branch_offsets, k_pages, v_pages, prefix_pages, S_prefix: int, suffix_pages,
+                 S_suffix: int, out=None, lse=None, workspace=None, want_lse: bool = True, prefill: bool = False):
+    """Shared-prefix fan-out over a paged KV cache.  k/v_pages [n_pages, page_size, Hkv, D];
+    prefix_pages int32 [ceil(S_prefix/page_size)]; suffix_pages int32 [nb, ceil(S_suffix/page_size)]
+    (device).  Returns (out [R,Hq,D], lse [Hq,R])."""
+    R, Hq, D = q_rows.shape
+    n_pages, page_size, Hkv, _ = k_pages.shape
+    nb = branch_offsets.numel() - 1
+    for t in (branch_offsets, prefix_pages, suffix_pages):
+        if t.dtype != torch.int32:
+            raise ValueError("branch_offsets and page tables must be int32")
+    if out is None:
+        out = torch.empty_like(q_rows)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, R), device=q_rows.device, dtype=torch.float32)
+    need = fanout_workspace_size(R, nb, S_prefix, S_suffix, Hq, Hkv, D, q_rows.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q_rows.device, dtype=torch.uint8)
+    dev = _cuda(q_rows, branch_offsets, k_pages, v_pages, prefix_pages, suffix_pages, out, lse, workspace)
+    _check(load().ra_prefix_fanout_attn_paged(_ptr(q_rows), _ptr(branch_offsets), nb, R, _ptr(k_pages),
+                                              _ptr(v_pages), n_pages, page_size, _ptr(prefix_pages), S_prefix,
+                                              _ptr(suffix_pages), S_suffix, _ptr(out), _ptr(lse), Hq, Hkv, D,
+                                              _dt(q_rows), int(bool(prefill)), _ptr(workspace), workspace.numel(),
+                                              _stream(dev)))
     return out, lse
 
 

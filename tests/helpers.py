@@ -115,3 +115,30 @@ def page_positions(S, N, layout):
             pos += [i for i in range(S) if i % N == k]
     return pos
 
+
+def paginate(prefix, suffix, page_size, n_spare, seed):
+    """Scatter a contiguous prefix [Sp, Hkv, D] and per-branch suffixes
+    [nb, Ss, Hkv, D] into a shuffled page pool [n_pages, page_size, Hkv, D]
+    (plus n_spare pages of unrelated finite values); returns (pool,
+    prefix_pages [ceil(Sp/P)], suffix_pages [nb, ceil(Ss/P)]) as torch tensors.
+    Rows of a last page past the sequence hold unrelated finite values."""
+    import torch
+    g = torch.Generator().manual_seed(seed)
+    Sp, Hkv, D = prefix.shape
+    nb, Ss = suffix.shape[0], suffix.shape[1]
+    npp = -(-Sp // page_size)
+    nsp = -(-Ss // page_size)
+    n_pages = npp + nb * nsp + n_spare
+    pool = torch.randn(n_pages, page_size, Hkv, D, generator=g).to(prefix.dtype)
+    order = torch.randperm(n_pages, generator=g)
+    prefix_pages = order[:npp].to(torch.int32)
+    suffix_pages = order[npp:npp + nb * nsp].reshape(nb, nsp).to(torch.int32)
+    for i in range(npp):
+        rows = prefix[i * page_size:(i + 1) * page_size]
+        pool[prefix_pages[i], :rows.shape[0]] = rows
+    for b in range(nb):
+        for i in range(nsp):
+            rows = suffix[b, i * page_size:(i + 1) * page_size]
+            pool[suffix_pages[b, i], :rows.shape[0]] = rows
+    return pool, prefix_pages, suffix_pages
+

@@ -14,7 +14,7 @@ import oracle
 import ring_context_parallelism_gb300 as ra
 from ring_context_parallelism_gb300.inputs import (WORKLOADS, attention_inputs, fanout_inputs, sample_queries,
                                                    small)
-from helpers import storage
+from helpers import paginate, storage
 
 pytestmark = pytest.mark.gpu
 
@@ -321,6 +321,50 @@ def test_fanout_prefill_full(Sp, Ss, rows, Hq, Hkv, D):
     rO, rL = oracle.fanout(st[0], x["offsets"].numpy(), *st[1:], dtype="bf16", suffix_causal=True)
     _close(O.float().cpu().double().numpy(), rO, 2e-2, "O")
     _close(L.cpu().double().numpy(), rL, 1e-3, "lse")
+
+
+@pytest.mark.parametrize("Sp,Ss,rows,Hq,Hkv,D,page,prefill", [
+    (1000, 200, [3, 0, 16, 1, 7], 16, 2, 128, 16, False),   # pages shorter than a tile, ragged tails
+    (1000, 200, [3, 0, 16, 1, 7], 16, 2, 128, 16, True),
+    (4096, 512, [16] * 4, 64, 8, 128, 128, False),           # one page per tile
+    (3000, 256, [16, 16, 16], 64, 8, 128, 256, False),       # pages longer than a tile
+    (0, 300, [2, 9], 8, 1, 128, 32, False),                  # no shared prefix
+    (2048, 0, [4, 4, 4], 16, 4, 64, 64, True),               # no private suffix
+    (640, 128, [33, 5], 8, 2, 64, 8, True),                  # 8-row pages, D = 64
+])
+def test_fanout_paged_full(Sp, Ss, rows, Hq, Hkv, D, page, prefill):
+    """Fan-out over a paged KV cache: the shared prefix pages and each branch's private pages
+    scattered in a shuffled pool (with spare pages of unrelated values)."""
+    w = small(WORKLOADS["fanout_decode"], S_prefix=Sp, S_suffix=Ss, n_branches=len(rows), Hq=Hq, Hkv=Hkv, D=D,
+              seed=900 + Sp + Ss + page)
+    x = fanout_inputs(w, "cpu", rows=rows)
+    kpool, pp, sp = paginate(x["k_prefix"], x["k_suffix"], page, 5, seed=page)
+    vpool, _, _ = paginate(x["v_prefix"], x["v_suffix"], page, 5, seed=page)
+    O, L = ra.fanout_paged(x["q_rows"].cuda(), x["offsets"].cuda(), kpool.cuda(), vpool.cuda(), pp.cuda(), Sp,
+                           sp.cuda(), Ss, prefill=prefill)
+    ra.device_status()
+    rO, rL = oracle.fanout_paged(storage(x["q_rows"])[0], x["offsets"].numpy(), storage(kpool)[0],
+                                 storage(vpool)[0], pp.numpy(), Sp, sp.numpy(), Ss, dtype="bf16",
+                                 suffix_causal=prefill)
+    _close(O.float().cpu().double().numpy(), rO, 2e-2, "O")
+    _close(L.cpu().double().numpy(), rL, 1e-3, "lse")
+
+
+def test_fanout_paged_rejects_a_page_outside_the_pool():
+    """A page index outside the pool is reported by the device check (its keys read as zeros)."""
+    w = small(WORKLOADS["fanout_decode"], S_prefix=512, S_suffix=64, n_branches=2, Hq=8, Hkv=2, D=128, seed=3)
+    x = fanout_inputs(w, "cpu", rows=[2, 3])
+    kpool, pp, sp = paginate(x["k_prefix"], x["k_suffix"], 64, 0, seed=1)
+    vpool, _, _ = paginate(x["v_prefix"], x["v_suffix"], 64, 0, seed=1)
+    bad = pp.clone()
+    bad[3] = kpool.shape[0] + 7
+    ra.fanout_paged(x["q_rows"].cuda(), x["offsets"].cuda(), kpool.cuda(), vpool.cuda(), bad.cuda(), 512,
+                    sp.cuda(), 64)
+    with pytest.raises(ra.RAError, match="page"):
+        ra.device_status()
+    # the status word is cleared: a valid call afterwards reports nothing
+    ra.fanout_paged(x["q_rows"].cuda(), x["offsets"].cuda(), kpool.cuda(), vpool.cuda(), pp.cuda(), 512, sp.cuda(), 64)
+    ra.device_status()
 
 
 # ------------------------------------------------------------------------------------------

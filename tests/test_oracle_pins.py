@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import online_softmax_walk, read_golden, ring_simulator_replay, storage
+from helpers import online_softmax_walk, paginate, read_golden, ring_simulator_replay, storage
 
 
 def _rand(shape, seed):
@@ -361,6 +361,31 @@ def test_fanout_prefill_equals_causal_attention_over_prefix_plus_suffix():
     Od, Ld = oracle.fanout(qr, off, kp, vp, ks, vs, dtype="f64")
     last = off[1:][np.array(rows) > 0] - 1
     np.testing.assert_allclose(O[last], Od[last], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("page_size", [1, 4, 16])
+def test_fanout_paged_equals_contiguous(page_size):
+    """A branch's context read through its page table (shared prefix pages, then
+    its private pages; "AHBM Agentic Runtime Architecture", section 3.1) is the
+    contiguous prefix + suffix, whatever the pages' places in the pool."""
+    Sp, Ss, Hq, Hkv, D = 21, 6, 4, 2, 8
+    rows = [2, 0, 3, 1]
+    nb = len(rows)
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    g = torch.Generator().manual_seed(130)
+    qr = torch.randn(int(off[-1]), Hq, D, generator=g, dtype=torch.float64)
+    kp, vp = torch.randn(Sp, Hkv, D, generator=g, dtype=torch.float64), torch.randn(Sp, Hkv, D, generator=g, dtype=torch.float64)
+    ks = torch.randn(nb, Ss, Hkv, D, generator=g, dtype=torch.float64)
+    vs = torch.randn(nb, Ss, Hkv, D, generator=g, dtype=torch.float64)
+    kpool, pp, sp = paginate(kp, ks, page_size, 3, seed=7)
+    vpool, pp2, sp2 = paginate(vp, vs, page_size, 3, seed=7)
+    assert torch.equal(pp, pp2) and torch.equal(sp, sp2)
+    for causal in (False, True):
+        ref = oracle.fanout(qr.numpy(), off, kp.numpy(), vp.numpy(), ks.numpy(), vs.numpy(), dtype="f64",
+                            suffix_causal=causal)
+        got = oracle.fanout_paged(qr.numpy(), off, kpool.numpy(), vpool.numpy(), pp.numpy(), Sp, sp.numpy(), Ss,
+                                  dtype="f64", suffix_causal=causal)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
 
 
 def test_bf16_storage_is_widened_exactly():
