@@ -525,7 +525,8 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-PROFILE_CASES = ("prefill_32k", "prefill_16k", "fanout_decode", "fanout_decode1", "merge_16k", "bwd_16k")
+PROFILE_CASES = ("prefill_32k", "prefill_16k", "fanout_decode", "fanout_decode1", "merge_16k", "bwd_16k",
+                 "prefill_32k_zigzag", "prefill_32k_striped", "fanout_prefill_8x20", "fanout_decode1_paged16")
 
 
 def run_profile_case(case):
@@ -547,6 +548,37 @@ def run_profile_case(case):
         l = torch.empty(w.B, w.Hq, w.S, device="cuda")
         for _ in range(3):
             ra.attn(q, k, v, w.n_shards, w.block, True, out=o, lse=l)
+    elif case in ("prefill_32k_zigzag", "prefill_32k_striped"):
+        # the headline configuration stored in a zigzag or striped shard layout (same data, same FLOPs)
+        w = WORKLOADS[HEADLINE]
+        q, k, v = attention_inputs(w, "cuda")
+        o = torch.empty_like(q)
+        l = torch.empty(w.B, w.Hq, w.S, device="cuda")
+        for _ in range(3):
+            ra.attn(q, k, v, w.n_shards, w.block, True, out=o, lse=l, layout=case.rsplit("_", 1)[1])
+    elif case == "fanout_prefill_8x20":
+        w = WORKLOADS[case]
+        x = fanout_inputs(w, "cuda")
+        for _ in range(3):
+            ra.fanout(x["q_rows"], x["offsets"], x["k_prefix"], x["v_prefix"], x["k_suffix"], x["v_suffix"],
+                      prefill=True)
+    elif case == "fanout_decode1_paged16":
+        # the R = 16 decode mix with its KV scattered over a shuffled pool of 16-token pages
+        w = WORKLOADS["fanout_decode1"]
+        x = fanout_inputs(w, "cuda")
+        P = 16
+        npp, nsp = w.S_prefix // P, w.S_suffix // P
+        n_pages = npp + w.n_branches * nsp
+        order = torch.randperm(n_pages, generator=torch.Generator().manual_seed(w.seed + 99)).to(torch.int32).cuda()
+        pp, sp = order[:npp].contiguous(), order[npp:].reshape(w.n_branches, nsp).contiguous()
+        kpool = torch.empty(n_pages, P, w.Hkv, w.D, dtype=x["k_prefix"].dtype, device="cuda")
+        vpool = torch.empty_like(kpool)
+        kpool[pp.long()] = x["k_prefix"].reshape(npp, P, w.Hkv, w.D)
+        vpool[pp.long()] = x["v_prefix"].reshape(npp, P, w.Hkv, w.D)
+        kpool[sp.long().reshape(-1)] = x["k_suffix"].reshape(-1, P, w.Hkv, w.D)
+        vpool[sp.long().reshape(-1)] = x["v_suffix"].reshape(-1, P, w.Hkv, w.D)
+        for _ in range(3):
+            ra.fanout_paged(x["q_rows"], x["offsets"], kpool, vpool, pp, w.S_prefix, sp, w.S_suffix)
     elif case in ("fanout_decode", "fanout_decode1"):
         w = WORKLOADS[case]
         x = fanout_inputs(w, "cuda")

@@ -816,6 +816,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // zigzag / striped causal walks: this row's sequence position
         const int shard_len = LAY ? p.S / p.n_shards : 0;
         const int row_pos = LAY ? layout_pos(p.layout, shard_len, p.n_shards, row) : row;
+        // the query tile's first row has its smallest position: the keys of a shard it
+        // sees are seen by every row, so whole tiles of them need no mask
+        const int tile_minpos = LAY ? layout_pos(p.layout, shard_len, p.n_shards, FAN ? 0 : u.q_row0) : 0;
+        int lay_full = 0;  // leading tiles of the current shard every row sees whole
 
         // Normalise the O accumulator and write it as part `part`, once `done`
         // (if given) shows its last PV complete.
@@ -895,10 +899,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!FAN) {
                 // keys of this tile the row sees: a prefix of the tile (positions
                 // increase along a shard), ending where the shard's visible keys end
-                if (LAY)
-                    lim = min(lim, shard_visible(p.layout, shard_len, p.n_shards, wi.ring.j, row_pos) -
-                                       (tile_kb - wi.ring.j * shard_len) - 1);
-                else if (p.causal)
+                if (LAY) {
+                    if (wi.ring.in == 0)
+                        lay_full = shard_visible(p.layout, shard_len, p.n_shards, wi.ring.j, tile_minpos) / kTileN;
+                    if (wi.ring.in >= lay_full)
+                        lim = min(lim, shard_visible(p.layout, shard_len, p.n_shards, wi.ring.j, row_pos) -
+                                           (tile_kb - wi.ring.j * shard_len) - 1);
+                } else if (p.causal)
                     lim = min(lim, row - tile_kb);
             } else {
                 lim = min(lim, wi.key_end - 1 - tile_kb);
