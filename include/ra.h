@@ -342,6 +342,17 @@ int ra_ring_walk_layout(int S, int n_shards, int causal, int layout, int q_row0,
  * RA_ERR_CUDA if the stream reports an error. */
 ra_status ra_device_status(void* stream);
 
+/*
+ * Health check of the device-side failure detection (not a step of the method):
+ * launches one thread that waits, for at most limit_ns nanoseconds of the GPU
+ * timer, on an mbarrier that nothing completes -- the bounded wait that guards
+ * every pipeline stage of the attention kernels.  The wait runs out, the
+ * kernel records RA_ERR_DEVICE_TIMEOUT and returns, so the next
+ * ra_device_status(stream) reports RA_ERR_DEVICE_TIMEOUT and the context stays
+ * usable.  limit_ns in (0, 2e9]; RA_ERR_INVALID_ARG otherwise.
+ */
+ra_status ra_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
 /* Thread-local one-line description of the last non-OK status ("" if none). */
 const char* ra_last_error(void);
 

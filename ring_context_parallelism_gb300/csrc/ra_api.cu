@@ -524,6 +524,10 @@ ra_status ra_device_status(void* stream) {
         code = ra::read_clear_status_bwd(&where);
         who = "attention backward";
     }
+    if (!code) {
+        code = ra::read_clear_status_selftest(&where);
+        who = "wait self-test";
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "device status");
     if (code == RA_ERR_DEVICE_TIMEOUT)
@@ -533,6 +537,13 @@ ra_status ra_device_status(void* stream) {
     if (code == RA_ERR_INVALID_ARG)
         return fail(RA_ERR_INVALID_ARG, "%s: device-side argument check failed (0x%08x)", who, where);
     if (code) return fail(static_cast<ra_status>(code), "%s: device status %u", who, code);
+    return ok();
+}
+
+ra_status ra_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+    if (limit_ns == 0 || limit_ns > 2000000000ull) return fail(RA_ERR_INVALID_ARG, "limit_ns must be in (0, 2e9]");
+    const cudaError_t e = ra::launch_selftest_wait_timeout(limit_ns, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "wait self-test launch");
     return ok();
 }
 

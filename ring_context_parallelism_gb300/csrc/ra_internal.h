@@ -110,5 +110,9 @@ unsigned read_clear_status_tc(unsigned* where);
 unsigned read_clear_status_simt(unsigned* where);
 unsigned read_clear_status_merge(unsigned* where);
 unsigned read_clear_status_bwd(unsigned* where);
+unsigned read_clear_status_selftest(unsigned* where);
+
+// Failure-detection health check: a bounded wait that is never satisfied.
+cudaError_t launch_selftest_wait_timeout(unsigned long long limit_ns, cudaStream_t stream);
 
 }  // namespace ra

@@ -46,6 +46,7 @@ SIGNATURES = {
     "ra_prefix_fanout_attn_noalloc": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _fp, _i, _i, _i, _i,
                                            _vp]),
     "ra_ring_shard_order": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
+    "ra_selftest_wait_timeout": (_i, [ctypes.c_ulonglong, _vp]),
     "ra_device_status": (_i, [_vp]),
     "ra_last_error": (ctypes.c_char_p, []),
 }
@@ -311,6 +312,13 @@ def ring_walk(S: int, n_shards: int, causal: bool, layout, q_row0: int, q_rows: 
     if n < 0:
         raise ValueError("invalid arguments")
     return list(order[:n]), list(keys[:n]), total.value
+
+
+def selftest_wait_timeout(limit_ns: int = 50_000_000, stream=None) -> None:
+    """Launch the failure-detection health check: a bounded wait that runs out
+    (the next device_status() raises RAError with RA_ERR_DEVICE_TIMEOUT)."""
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    _check(load().ra_selftest_wait_timeout(int(limit_ns), s))
 
 
 def device_status(stream=None) -> None:

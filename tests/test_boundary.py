@@ -178,3 +178,8 @@ def test_backward_workspace_size(lib):
     assert n == 2 * 32768 * 32 * 4                   # Delta and lse2, [B, Hq, S] fp32 each
     assert f(1, 100, 3, 64, rab.RA_F32) == 2 * 1280   # each rounded up to 256 bytes
     assert f(1, 1024, 4, 96, rab.RA_BF16) == 0
+
+
+def test_selftest_wait_timeout_validation(lib):
+    assert lib.ra_selftest_wait_timeout(0, None) == rab.RA_ERR_INVALID_ARG
+    assert lib.ra_selftest_wait_timeout(3_000_000_000, None) == rab.RA_ERR_INVALID_ARG
