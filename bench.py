@@ -282,6 +282,14 @@ def run_ours(args, rank, world):
                               "flop_convention": "2.5x the forward's causal-adjusted FLOPs (5 GEMMs); the kernels "
                                                  "execute 7 (dQ recomputes S and dP)",
                               "launches_per_call": 3}
+        # the backward over the zigzag layout (same data in storage order, causal on positions)
+        ra.attn(q, k, v, w.n_shards, w.block, w.causal, out=out, lse=lse, layout="zigzag")
+        zms = timed_steps(lambda: ra.attn_bwd(q, k, v, out, lse, dO, w.n_shards, w.block, w.causal, dq, dk, dv, bws,
+                                              layout="zigzag"), min(args.steps, 10), 3, flush)
+        ra.device_status()
+        tz = statistics.median(zms) * 1e-3
+        result["backward"]["zigzag"] = {"ms": tz * 1e3, "TFLOP_per_s": bflops / tz / 1e12,
+                                        "frac_bf16_peak": bflops / tz / 1e12 / pk["bf16_tflops"]}
         del dO, dq, dk, dv, bws
 
         # e2e through the public API with host buffers

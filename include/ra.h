@@ -171,7 +171,23 @@ ra_status ra_blockwise_attn_bwd(const void* q, const void* k, const void* v, con
                                 int D, int n_shards, int block, int causal, ra_dtype dt, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace ra_blockwise_attn_bwd needs (0 if the sizes are invalid). */
+/*
+ * ra_blockwise_attn_bwd for rows stored in a zigzag or striped shard layout
+ * (ra_layout; the forward is ra_blockwise_attn_fwd_layout).  All tensors are
+ * indexed by storage row; the causal mask compares the rows' sequence
+ * positions.  The dQ walk takes from each KV shard the prefix of its rows a
+ * query tile can see (as the forward); the dK/dV walk takes from each query
+ * shard the suffix of its rows that can see a KV tile (positions increase
+ * along a shard's rows in every layout).  Other arguments, rules and errors
+ * as ra_blockwise_attn_bwd and ra_blockwise_attn_fwd_layout.
+ */
+ra_status ra_blockwise_attn_bwd_layout(const void* q, const void* k, const void* v, const void* out,
+                                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                       int B, int S, int Hq, int Hkv, int D, int n_shards, int block,
+                                       int causal, int layout, ra_dtype dt, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace ra_blockwise_attn_bwd (and _layout) needs (0 if the sizes are invalid). */
 size_t ra_blockwise_attn_bwd_workspace_size(int B, int S, int Hq, int D, ra_dtype dt);
 
 /*

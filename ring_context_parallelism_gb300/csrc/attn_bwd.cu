@@ -37,6 +37,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "ra_device.cuh"
 #include "ra_internal.h"
@@ -75,6 +76,7 @@ struct BwdCfg {
 
 struct BwdParams {
     int B, S, Hq, Hkv, n_shards, causal, G, n_tiles;
+    int layout;        // shard layout of the rows (ra_walk.h); the LAY kernels run causal zigzag / striped
     float scale_log2;  // log2(e) / sqrt(D)
     float scale;       // 1 / sqrt(D)
     const float* delta;
@@ -201,7 +203,7 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int issued, int n_sta
 // ---------------------------------------------------------------------------
 // dQ: query-tile outer, KV tiles in ring order
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool LAY>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -216,7 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qt_rev = rem / p.G;
     const int b = grp / p.Hkv, hk = grp - b * p.Hkv;
     const int h = hk * p.G + (rem - qt_rev * p.G);
-    const int q0 = (p.causal ? p.n_tiles - 1 - qt_rev : qt_rev) * kT;
+    const int q0 = !p.causal ? qt_rev * kT
+                   : LAY     ? heavy_tile_row0(p.layout, p.S, p.n_shards, kT, qt_rev)
+                             : (p.n_tiles - 1 - qt_rev) * kT;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -239,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned* status = g_bwd_status;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const RingWalk w = make_ring_walk(p.S, p.n_shards, kT, p.causal, q0, kT);
+    const RingWalk w = make_ring_walk(p.S, p.n_shards, kT, p.causal, q0, kT, LAY ? p.layout : kLayoutContiguous);
     const int total = w.total;
 
     if (threadIdx.x == 0) {
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load_tile<D>(&tm_q, qd_full, q_smem, h, q0, b);
                 load_tile<D>(&tm_do, qd_full, do_smem, h, q0, b);
             }
-            RingIterT<false> it;
+            RingIterT<LAY> it;
             it.start(w);
             Stage st;
             int issued = 0;
@@ -363,7 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lse2_r = p.lse2[vrow];
         const float delta_r = p.delta[vrow];
         const float sl2 = p.scale_log2;
-        RingIterT<false> it;
+        // zigzag / striped: the row's sequence position; the tile's first row has the
+        // smallest, so whole tiles of the keys it sees need no mask
+        const int shard_len = p.S / p.n_shards;
+        const int row_pos = LAY ? layout_pos(p.layout, shard_len, p.n_shards, row) : row;
+        const int tile_minpos = LAY ? layout_pos(p.layout, shard_len, p.n_shards, q0) : 0;
+        int lay_full = 0;
+        RingIterT<LAY> it;
         it.start(w);
         bool ok = true;
         for (int i = 0; i < total; ++i) {
@@ -371,7 +381,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tS = (i & 1) ? tS1 : tS0;
             if (!(ok = mbar_wait(&s_full[i & 1], (i >> 1) & 1, abort_flag, status, 0x16000000u | i))) break;
             tc_fence_after();
-            const int lim = p.causal ? min(kT - 1, row - it.kb) : kT - 1;  // visible columns c <= lim
+            int lim = kT - 1;  // visible columns c <= lim
+            if (LAY) {
+                if (it.in == 0) lay_full = shard_visible(p.layout, shard_len, p.n_shards, it.j, tile_minpos) / kT;
+                if (it.in >= lay_full)
+                    lim = min(lim, shard_visible(p.layout, shard_len, p.n_shards, it.j, row_pos) -
+                                       (it.kb - it.j * shard_len) - 1);
+            } else if (p.causal) {
+                lim = min(lim, row - it.kb);
+            }
             // P = exp(S - L) for this thread's half of the columns
             float pr[64];
 #pragma unroll
@@ -460,9 +478,73 @@ struct QWalk {
         qt = 0;
         a = (causal && a == j) ? N - 1 : (a == 0 ? N - 1 : a - 1);
     }
+    // first query column of the current tile that key row lane_row sees
+    __device__ __forceinline__ int col_lo(int lane_row, int) const {
+        return (causal && a == j && qt == x0) ? lane_row : 0;
+    }
 };
 
-template <int D>
+// The same walk over causal zigzag or striped shards (ra_walk.h).  Positions
+// increase along a shard's rows, so the query rows of shard a that see the KV
+// tile are a suffix of the shard: those whose position is at least the tile's
+// first key's.  Shards with none are skipped.  Tiles from `full` on see every
+// key of the tile; earlier ones mask per key row.
+struct QWalkL {
+    int N, L, tps, j, G, layout, minpos, maxpos;
+    int t, a, qt, g, full;
+    __device__ __forceinline__ void enter() {
+        qt = shard_visible(layout, L, N, a, minpos - 1) / kT;                // rows before the first seeing row
+        full = (shard_visible(layout, L, N, a, maxpos - 1) + kT - 1) / kT;
+    }
+    __device__ __forceinline__ void skip_empty() {
+        while (qt >= tps && t + 1 < N) {
+            ++t;
+            a = (a == 0) ? N - 1 : a - 1;
+            enter();
+        }
+    }
+    __device__ __forceinline__ void start(int n_shards, int shard_len, int shard, int k0, int group, int lay) {
+        N = n_shards;
+        L = shard_len;
+        tps = L / kT;
+        j = shard;
+        G = group;
+        layout = lay;
+        minpos = layout_pos(lay, L, N, k0);
+        maxpos = layout_pos(lay, L, N, k0 + kT - 1);
+        t = 0;
+        a = j;
+        g = 0;
+        enter();
+        skip_empty();
+    }
+    // units of the walk: O(N); computed by one thread
+    __device__ int total() const {
+        int n = 0;
+        for (int tt = 0; tt < N; ++tt) {
+            const int aa = (j - tt + N) % N;
+            n += tps - min(tps, shard_visible(layout, L, N, aa, minpos - 1) / kT);
+        }
+        return G * n;
+    }
+    __device__ __forceinline__ void next() {
+        if (++g < G) return;
+        g = 0;
+        if (++qt < tps) return;
+        if (t + 1 < N) {
+            ++t;
+            a = (a == 0) ? N - 1 : a - 1;
+            enter();
+            skip_empty();
+        }
+    }
+    __device__ __forceinline__ int col_lo(int, int key_pos) const {
+        if (qt >= full) return 0;
+        return max(0, shard_visible(layout, L, N, a, key_pos - 1) - qt * kT);
+    }
+};
+
+template <int D, bool LAY>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -501,9 +583,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned* status = g_bwd_status;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    QWalk qw;
-    qw.start(p.n_shards, tps, j, x_in, p.G, p.causal);
-    const int total = qw.total();
+    using Walk = typename std::conditional<LAY, QWalkL, QWalk>::type;
+    Walk qw;
+    if constexpr (LAY)
+        qw.start(p.n_shards, L, j, k0, p.G, p.layout);
+    else
+        qw.start(p.n_shards, tps, j, x_in, p.G, p.causal);
+    int* total_smem = reinterpret_cast<int*>(bars + C::kNumBars) + 2;  // after tmem_slot and abort_flag
+    if (threadIdx.x == 0) *total_smem = qw.total();
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -529,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const int total = *total_smem;
     // TMEM columns: S^T [0, 128) (P^T packed over it), dP^T [128, 256) (dS^T
     // packed over it), dV [256, 256 + D), dK [256 + D, 256 + 2D)
 
@@ -548,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load_tile<D>(&tm_k, kv_full, k_smem, hk, k0, b);
                 load_tile<D>(&tm_v, kv_full, v_smem, hk, k0, b);
             }
-            QWalk it = qw;
+            Walk it = qw;
             Stage st;
             int issued = 0;
             for (int u = 0; u < total; ++u, it.next()) {
@@ -627,10 +715,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hw = (warp - 4) >> 2;
         const int lane_row = quad * 32 + lane;
         const int key = k0 + lane_row;
+        const int key_pos = LAY ? layout_pos(p.layout, L, p.n_shards, key) : key;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem_base + lane_off, tdP = tS + 128, tdV = tS + 256, tdK = tS + 256 + D;
         const float sl2 = p.scale_log2;
-        QWalk it = qw;
+        Walk it = qw;
         Stage st;
         bool ok = true;
         for (int u = 0; u < total; ++u, it.next()) {
@@ -638,8 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the stage's lse2 / delta came with its Q tile (already landed: the MMA read it)
             if (!(ok = mbar_wait(&q_full[st.s], st.ph, abort_flag, status, 0x27000000u | u))) break;
             tc_fence_after();
-            // the diagonal query tile shows key row `key` to query columns c >= lane_row
-            const int lo = (p.causal && it.a == j && it.qt == x_in) ? lane_row : 0;
+            // key row `key` is visible to the query columns c >= lo of this tile
+            const int lo = it.col_lo(lane_row, key_pos);
             const float* lse2v = vec + st.s * 256;
             const float* dltv = lse2v + 128;
             // P^T = exp(S^T - L) for this thread's half of the columns, packed over its S^T columns
@@ -719,21 +808,21 @@ cudaError_t set_smem(K kernel, int bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int D>
+template <int D, bool LAY>
 cudaError_t launch_tc(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                       const CUtensorMap& tv, cudaStream_t stream) {
     using C = BwdCfg<D>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = set_smem(bwd_dkdv_kernel<D>, C::kKvSmem);
-        if (attr_err == cudaSuccess) attr_err = set_smem(bwd_dq_kernel<D>, C::kDqSmem);
+        attr_err = set_smem(bwd_dkdv_kernel<D, LAY>, C::kKvSmem);
+        if (attr_err == cudaSuccess) attr_err = set_smem(bwd_dq_kernel<D, LAY>, C::kDqSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    bwd_dkdv_kernel<D><<<p.B * p.Hkv * p.n_tiles, kThreads, C::kKvSmem, stream>>>(tq, tdo, tk, tv, p);
+    bwd_dkdv_kernel<D, LAY><<<p.B * p.Hkv * p.n_tiles, kThreads, C::kKvSmem, stream>>>(tq, tdo, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_dq_kernel<D><<<p.B * p.Hq * p.n_tiles, kThreads, C::kDqSmem, stream>>>(tq, tdo, tk, tv, p);
+    bwd_dq_kernel<D, LAY><<<p.B * p.Hq * p.n_tiles, kThreads, C::kDqSmem, stream>>>(tq, tdo, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -755,6 +844,7 @@ BwdParams make_params(const BwdArgs& a, int out_f32, int tile) {
     p.dk = a.dk;
     p.dv = a.dv;
     p.out_f32 = out_f32;
+    p.layout = a.causal ? a.layout : kLayoutContiguous;
     return p;
 }
 
@@ -790,9 +880,10 @@ __global__ void __launch_bounds__(kSimtRows * (D / 32)) bwd_dq_simt_kernel(const
     const int groups = p.B * p.Hq;
     const int qt_rev = blockIdx.x / groups, rem = blockIdx.x % groups;
     const int b = rem / p.Hq, h = rem % p.Hq, hk = h / p.G;
-    const int r0 = (p.causal ? p.n_tiles - 1 - qt_rev : qt_rev) * kSimtRows;
+    const int r0 = p.causal ? heavy_tile_row0(p.layout, p.S, p.n_shards, kSimtRows, qt_rev) : qt_rev * kSimtRows;
     const int row = r0 + r_local;
     const int L = p.S / p.n_shards;
+    const int row_pos = layout_pos(p.layout, L, p.n_shards, row);  // sequence position (causal mask)
     const long long qoff = ((static_cast<long long>(b) * p.S + row) * p.Hq + h) * D + sub;
     float qr[32], dor[32], dq[32];
 #pragma unroll
@@ -804,11 +895,12 @@ __global__ void __launch_bounds__(kSimtRows * (D / 32)) bwd_dq_simt_kernel(const
     const long long vrow = (static_cast<long long>(b) * p.Hq + h) * p.S + row;
     const float lse2_r = p.lse2[vrow];
     const float delta_r = p.delta[vrow];
-    const RingWalk w = make_ring_walk(p.S, p.n_shards, kSimtRows, p.causal, r0, kSimtRows);
+    const RingWalk w = make_ring_walk(p.S, p.n_shards, kSimtRows, p.causal, r0, kSimtRows, p.layout);
     for (int t = 0; t < w.n_visited; ++t) {
         const int jsh = ring_shard_at(w, t);
         const int key_lo = jsh * L;
-        const int key_hi = key_lo + (p.causal ? shard_visible(kLayoutContiguous, L, p.n_shards, jsh, w.maxpos) : L);
+        // causal: the prefix of the shard the tile's last row can see
+        const int key_hi = key_lo + (p.causal ? shard_visible(p.layout, L, p.n_shards, jsh, w.maxpos) : L);
         for (int c0 = key_lo; c0 < key_hi; c0 += kSimtRows) {
             __syncthreads();
             for (int e = tid; e < kSimtRows * (D / 4); e += blockDim.x) {
@@ -831,7 +923,7 @@ __global__ void __launch_bounds__(kSimtRows * (D / 32)) bwd_dq_simt_kernel(const
                     s += __shfl_xor_sync(0xffffffffu, s, x);
                     dp += __shfl_xor_sync(0xffffffffu, dp, x);
                 }
-                const bool vis = !p.causal || c0 + c <= row;
+                const bool vis = !p.causal || layout_pos(p.layout, L, p.n_shards, c0 + c) <= row_pos;
                 const float pc = vis ? exp2f(s * p.scale_log2 - lse2_r) : 0.f;
                 const float ds = pc * (dp - delta_r);
 #pragma unroll
@@ -861,6 +953,8 @@ __global__ void __launch_bounds__(kSimtRows * (D / 32)) bwd_dkdv_simt_kernel(con
     const int b = rem / p.Hkv, hk = rem % p.Hkv;
     const int k0 = x * kSimtRows, key = k0 + r_local;
     const int L = p.S / p.n_shards, N = p.n_shards, jsh = k0 / L;
+    const int key_pos = layout_pos(p.layout, L, N, key);
+    const int minpos = layout_pos(p.layout, L, N, k0);  // the chunk's first (smallest) key position
     const long long koff = ((static_cast<long long>(b) * p.S + key) * p.Hkv + hk) * D + sub;
     float kr[32], vr[32], dk[32], dv[32];
 #pragma unroll
@@ -871,8 +965,11 @@ __global__ void __launch_bounds__(kSimtRows * (D / 32)) bwd_dkdv_simt_kernel(con
     }
     for (int t = 0; t < N; ++t) {
         const int a = (jsh - t + N) % N;
-        if (p.causal && a < jsh) continue;  // query shards before the key's see nothing
-        const int row_lo = (p.causal && a == jsh) ? k0 : a * L, row_hi = (a + 1) * L;
+        // causal: the rows of shard a whose position is at least the chunk's first key's
+        // (a suffix of the shard), from a 32-row boundary
+        const int row_lo = a * L + (p.causal ? shard_visible(p.layout, L, N, a, minpos - 1) / kSimtRows * kSimtRows : 0);
+        const int row_hi = (a + 1) * L;
+        if (row_lo >= row_hi) continue;
         for (int g = 0; g < p.G; ++g) {
             const int h = hk * p.G + g;
             for (int c0 = row_lo; c0 < row_hi; c0 += kSimtRows) {
@@ -902,7 +999,7 @@ __global__ void __launch_bounds__(kSimtRows * (D / 32)) bwd_dkdv_simt_kernel(con
                         s += __shfl_xor_sync(0xffffffffu, s, xx);
                         dp += __shfl_xor_sync(0xffffffffu, dp, xx);
                     }
-                    const bool vis = !p.causal || c0 + c >= key;
+                    const bool vis = !p.causal || layout_pos(p.layout, L, N, c0 + c) >= key_pos;
                     const float pc = vis ? exp2f(s * p.scale_log2 - lse_s[c]) : 0.f;
                     const float dsc = pc * (dp - dlt_s[c]);
 #pragma unroll
@@ -939,7 +1036,12 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t stream) {
     if (!make_map(&tq, a.q, qd, qs, box) || !make_map(&tdo, a.dout, qd, qs, box) || !make_map(&tk, a.k, kd, ks, box) ||
         !make_map(&tv, a.v, kd, ks, box))
         return cudaErrorInvalidValue;
-    return a.D == 128 ? launch_tc<128>(p, tq, tdo, tk, tv, stream) : launch_tc<64>(p, tq, tdo, tk, tv, stream);
+    // without a causal mask every layout is the same walk
+    if (a.causal && a.layout != kLayoutContiguous)
+        return a.D == 128 ? launch_tc<128, true>(p, tq, tdo, tk, tv, stream)
+                          : launch_tc<64, true>(p, tq, tdo, tk, tv, stream);
+    return a.D == 128 ? launch_tc<128, false>(p, tq, tdo, tk, tv, stream)
+                      : launch_tc<64, false>(p, tq, tdo, tk, tv, stream);
 }
 
 cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t stream) {

@@ -436,11 +436,11 @@ size_t ra_blockwise_attn_bwd_workspace_size(int B, int S, int Hq, int D, ra_dtyp
     return 2 * vec;  // Delta, then lse in log2 units
 }
 
-ra_status ra_blockwise_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
-                                const void* dout, void* dq, void* dk, void* dv, int B, int S, int Hq, int Hkv,
-                                int D, int n_shards, int block, int causal, ra_dtype dt, void* workspace,
-                                size_t workspace_bytes, void* stream) {
-    ra_status st = check_ring(q, k, v, out, B, S, Hq, Hkv, D, n_shards, block, causal, dt, RA_LAYOUT_CONTIGUOUS);
+static ra_status bwd_common(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int B, int S, int Hq, int Hkv, int D,
+                            int n_shards, int block, int causal, int layout, ra_dtype dt, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    ra_status st = check_ring(q, k, v, out, B, S, Hq, Hkv, D, n_shards, block, causal, dt, layout);
     if (st != RA_OK) return st;
     if (!lse || !dout || !dq || !dk || !dv) return fail(RA_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -469,10 +469,28 @@ ra_status ra_blockwise_attn_bwd(const void* q, const void* k, const void* v, con
     a.D = D;
     a.n_shards = n_shards;
     a.causal = causal;
+    a.layout = layout;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t e = dt == RA_BF16 ? ra::launch_bwd_tc(a, s) : ra::launch_bwd_simt(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "attention backward launch");
     return ok();
+}
+
+ra_status ra_blockwise_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                                const void* dout, void* dq, void* dk, void* dv, int B, int S, int Hq, int Hkv,
+                                int D, int n_shards, int block, int causal, ra_dtype dt, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, n_shards, block, causal,
+                      RA_LAYOUT_CONTIGUOUS, dt, workspace, workspace_bytes, stream);
+}
+
+ra_status ra_blockwise_attn_bwd_layout(const void* q, const void* k, const void* v, const void* out,
+                                       const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                                       int S, int Hq, int Hkv, int D, int n_shards, int block, int causal,
+                                       int layout, ra_dtype dt, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+    return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, n_shards, block, causal, layout, dt,
+                      workspace, workspace_bytes, stream);
 }
 
 int ra_layout_positions(int S, int n_shards, int layout, int* pos) {

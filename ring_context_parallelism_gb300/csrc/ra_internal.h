@@ -100,6 +100,7 @@ struct BwdArgs {
     void *dq, *dk, *dv;
     float *ws_delta, *ws_lse2;
     int B, S, Hq, Hkv, D, n_shards, causal;
+    int layout = 0;  // shard layout of the rows (ra_walk.h kLayout*)
 };
 cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t stream);    // bf16
 cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t stream);  // fp32

@@ -31,6 +31,8 @@ SIGNATURES = {
     "ra_ring_partials_fwd_layout": (_i, [_vp, _vp, _vp, _vp, _fp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
     "ra_blockwise_attn_bwd": (_i, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                    _vp, _sz, _vp]),
+    "ra_blockwise_attn_bwd_layout": (_i, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                          _i, _i, _i, _vp, _sz, _vp]),
     "ra_blockwise_attn_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "ra_layout_positions": (_i, [_i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
     "ra_ring_walk_layout": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int),
@@ -146,9 +148,9 @@ def attn(q, k, v, n_shards: int, block: int, causal: bool, out=None, lse=None, w
 
 
 def attn_bwd(q, k, v, out, lse, dout, n_shards: int, block: int, causal: bool, dq=None, dk=None, dv=None,
-             workspace=None):
+             workspace=None, layout="contiguous"):
     """Backward pass: (dq [B,S,Hq,D], dk, dv [B,S,Hkv,D]) for the upstream gradient dout, given the
-    forward's out and lse for the same q, k, v (bf16 or fp32)."""
+    forward's out and lse for the same q, k, v (bf16 or fp32), rows in the given shard layout."""
     B, S, Hq, D = q.shape
     Hkv = k.shape[2]
     if k.shape != (B, S, Hkv, D) or v.shape != k.shape or out.shape != q.shape or dout.shape != q.shape:
@@ -162,9 +164,16 @@ def attn_bwd(q, k, v, out, lse, dout, n_shards: int, block: int, causal: bool, d
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
     dev = _cuda(q, k, v, out, lse, dout, dq, dk, dv, workspace)
-    _check(load().ra_blockwise_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
-                                        _ptr(dk), _ptr(dv), B, S, Hq, Hkv, D, n_shards, block, int(bool(causal)),
-                                        _dt(q), _ptr(workspace), workspace.numel(), _stream(dev)))
+    lay = _layout(layout)
+    if lay == 0:
+        _check(load().ra_blockwise_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                                            _ptr(dk), _ptr(dv), B, S, Hq, Hkv, D, n_shards, block, int(bool(causal)),
+                                            _dt(q), _ptr(workspace), workspace.numel(), _stream(dev)))
+    else:
+        _check(load().ra_blockwise_attn_bwd_layout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                                   _ptr(dq), _ptr(dk), _ptr(dv), B, S, Hq, Hkv, D, n_shards, block,
+                                                   int(bool(causal)), lay, _dt(q), _ptr(workspace),
+                                                   workspace.numel(), _stream(dev)))
     return dq, dk, dv
 
 

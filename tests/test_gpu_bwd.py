@@ -14,7 +14,7 @@ import torch
 import oracle
 import ring_context_parallelism_gb300 as ra
 from ring_context_parallelism_gb300.inputs import WORKLOADS, attention_inputs, randn, sample_queries, small
-from helpers import storage
+from helpers import page_positions, storage
 
 pytestmark = pytest.mark.gpu
 
@@ -138,3 +138,32 @@ def test_gqa_causal_prefill_32k_backward_sampled():
     scale = float(want.abs().max())
     assert float(dk_sum.abs().max()) <= 2e-2 * scale, float(dk_sum.abs().max())
     assert float((dv_sum - want).abs().max()) <= 2e-2 * scale, float((dv_sum - want).abs().max())
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "striped"])
+@pytest.mark.parametrize("dtype,B,S,Hq,Hkv,D,N,block", [
+    ("bf16", 1, 2048, 4, 2, 128, 4, 128),
+    ("bf16", 1, 1024, 2, 1, 64, 2, 128),
+    ("bf16", 2, 3072, 2, 1, 128, 6, 128),    # one tile per zigzag chunk
+    ("f32", 1, 256, 2, 1, 64, 4, 32),
+    ("f32", 1, 384, 3, 3, 128, 3, 64),
+])
+def test_backward_layout_full(layout, dtype, B, S, Hq, Hkv, D, N, block):
+    """Backward over rows stored in a zigzag or striped shard layout (storage row p holds
+    token pos[p]) against the oracle with the causal mask on positions."""
+    base = WORKLOADS["gqa_causal_prefill_32k"] if dtype == "bf16" else WORKLOADS["tiny_exact_f32"]
+    w = small(base, B=B, S=S, Hq=Hq, Hkv=Hkv, D=D, n_shards=N, block=block, causal=True, seed=950 + S + D + N)
+    q, k, v = attention_inputs(w, "cpu")
+    dO = _dout(w)
+    pos = np.array(page_positions(S, N, layout), np.int64)
+    idx = torch.from_numpy(pos)
+    q, k, v, dO = (t[:, idx].contiguous() for t in (q, k, v, dO))
+    qd, kd, vd, dOd = (t.cuda() for t in (q, k, v, dO))
+    O, lse = ra.attn(qd, kd, vd, N, block, True, layout=layout)
+    dq, dk, dv = ra.attn_bwd(qd, kd, vd, O, lse, dOd, N, block, True, layout=layout)
+    ra.device_status()
+    st = [storage(t)[0] for t in (q, k, v, dO)]
+    rq, rk, rv = oracle.attention_bwd(*st, dtype=dtype, causal=True, pos=pos.astype(np.int32))
+    _close(dq.float().cpu().numpy(), rq, dtype, "dQ")
+    _close(dk.float().cpu().numpy(), rk, dtype, "dK")
+    _close(dv.float().cpu().numpy(), rv, dtype, "dV")
