@@ -44,7 +44,7 @@ extern "C" {
 typedef enum {
     RA_OK = 0,
     RA_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment or divisibility */
-    RA_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+    RA_ERR_UNSUPPORTED = 2,    /* valid request the kernels do not implement */
     RA_ERR_CUDA = 3,           /* a CUDA runtime/driver call or launch failed */
     RA_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait ran out */
     RA_ERR_WORKSPACE = 5       /* workspace missing or smaller than required */
