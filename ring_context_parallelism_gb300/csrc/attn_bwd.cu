@@ -439,6 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
     }
+    // Launched as a programmatic dependent of the dK/dV kernel (it reads none of that
+    // kernel's results, so its CTAs may fill SMs the dK/dV tail frees); a CTA does not
+    // finish before that grid has, so work after this launch on the stream sees both.
+    if (threadIdx.x == 0) grid_dependency_wait();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -617,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total = *total_smem;
+    if (threadIdx.x == 0) grid_launch_dependents();  // the dQ kernel may take SMs as this grid drains
     // TMEM columns: S^T [0, 128) (P^T packed over it), dP^T [128, 256) (dS^T
     // packed over it), dV [256, 256 + D), dK [256 + D, 256 + 2D)
 
@@ -822,8 +827,17 @@ cudaError_t launch_tc(const BwdParams& p, const CUtensorMap& tq, const CUtensorM
     bwd_dkdv_kernel<D, LAY><<<p.B * p.Hkv * p.n_tiles, kThreads, C::kKvSmem, stream>>>(tq, tdo, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_dq_kernel<D, LAY><<<p.B * p.Hq * p.n_tiles, kThreads, C::kDqSmem, stream>>>(tq, tdo, tk, tv, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.B * p.Hq * p.n_tiles);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kDqSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D, LAY>, tq, tdo, tk, tv, p);
 }
 
 BwdParams make_params(const BwdArgs& a, int out_f32, int tile) {
