@@ -39,8 +39,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, valid only while the kernel source hashes to the recorded value.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the timed 32768-token configuration
-    # (bench.py --profile-case prefill_32k, third launch): 402941952 read + 243426560 written
-    "a41c2c2effa09505": 646368512,
+    # (bench.py --profile-case prefill_32k, third launch): 403606784 read + 243387648 written
+    "ea3886c34d6dac5a": 646994432,
 }
 
 

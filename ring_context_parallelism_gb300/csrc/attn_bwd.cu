@@ -556,11 +556,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = BwdCfg<D>;
     constexpr int NS = C::kKvS;
     // (batch, KV head) outermost (its CTAs share the group's Q / dO in L2);
-    // within it the key tiles in order, the earliest (most queries) first
+    // within it the key tiles by sequence position, the earliest (seen by the
+    // most queries) first
     const int grp = blockIdx.x / p.n_tiles;
     const int x = blockIdx.x - grp * p.n_tiles;
     const int b = grp / p.Hkv, hk = grp - b * p.Hkv;
-    const int k0 = x * kT;
+    const int k0 = LAY ? heavy_tile_row0(p.layout, p.S, p.n_shards, kT, p.n_tiles - 1 - x) : x * kT;
     const int L = p.S / p.n_shards, tps = L / kT;
     const int j = k0 / L, x_in = (k0 - j * L) / kT;
 
@@ -965,7 +966,9 @@ __global__ void __launch_bounds__(kSimtRows * (D / 32)) bwd_dkdv_simt_kernel(con
     const int groups = p.B * p.Hkv;
     const int x = blockIdx.x / groups, rem = blockIdx.x % groups;
     const int b = rem / p.Hkv, hk = rem % p.Hkv;
-    const int k0 = x * kSimtRows, key = k0 + r_local;
+    // causal: the chunks by sequence position, the earliest (seen by the most queries) first
+    const int k0 = p.causal ? heavy_tile_row0(p.layout, p.S, p.n_shards, kSimtRows, p.n_tiles - 1 - x) : x * kSimtRows;
+    const int key = k0 + r_local;
     const int L = p.S / p.n_shards, N = p.n_shards, jsh = k0 / L;
     const int key_pos = layout_pos(p.layout, L, N, key);
     const int minpos = layout_pos(p.layout, L, N, k0);  // the chunk's first (smallest) key position
