@@ -5,10 +5,14 @@
 One JSON line on rank 0.  The headline step is one ra_blockwise_attn_fwd call
 on the causal GQA prefill workload (B=1, S=32768, Hq=32, Hkv=8, D=128, bf16,
 8 ring shards, 128-key blocks); `value` is its causal-adjusted attention
-TFLOP/s (4*D FLOPs per unmasked query/key pair).  The same line carries the
-other rows of the path measured on their own workloads: shared-prefix fan-out
-decode (HBM GB/s), per-shard partials + LSE merge on the Llama-3-70B-shaped
-layer, and (with --all) the million-token stress case.
+TFLOP/s (4*D FLOPs per unmasked query/key pair), `e2e` the same call with the
+inputs copied from pinned host memory and the results read back every step.
+The same line carries the other rows measured on their own workloads: the
+headline workload in the zigzag and striped shard layouts, its backward pass
+(contiguous and zigzag), shared-prefix fan-out decode (HBM GB/s; contiguous and
+over a paged KV pool), fan-out prefill (8 branches x 20 rows), per-shard
+partials + LSE merge on the Llama-3-70B-shaped layer, and (with --all) the
+million-token stress case.
 
 Under torchrun (--gpus N > 1) every rank runs an independent replica of the
 same workload (the path needs no exchange between GPUs); the barrier and the

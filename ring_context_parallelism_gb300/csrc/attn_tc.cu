@@ -17,11 +17,18 @@
 // 2^8 (in log2 units); otherwise the stale max is kept, which changes no
 // result (O and l share it) and skips the O rescale.
 //
-// Roles (384 threads):  warp 0 lane 0  TMA producer (Q once, then K_i, V_i
-// into a 4-stage smem ring, 8 for D = 64);  warp 1 lane 0  MMA issuer (also allocates TMEM);
-// warps 4-7  softmax + epilogue of tile 0;  warps 8-11  same for tile 1.
-// TMEM: tile t uses columns [256t, 256t+128) for S (P~ overwrites its first
-// half as packed bf16) and [256t+128, 256t+128+D) for O.
+// Roles (384 threads):  warp 0 lane 0  TMA producer of Q (once) and the K ring;
+// warp 2 lane 0  TMA producer of the V ring (up to three stages each for
+// D = 128, four for D = 64; Cfg below);  warp 1 lane 0  MMA issuer (also
+// allocates TMEM);  warps 4-7  softmax + epilogue of tile 0;  warps 8-11  same
+// for tile 1.  TMEM: tile t uses columns [256t, 256t+128) for S (P~ overwrites
+// its first half as packed bf16) and [256t+128, 256t+128+D) for O.
+//
+// Kernel modes: the ring prefill over contiguous shards, the same walk over
+// causal zigzag / striped shards (ra_walk.h), and the fan-out (stacked branch
+// rows against a prefix chunk plus folded private suffixes; decode, prefill with
+// a causal suffix, or a paged KV pool), whose units split their KV tiles over
+// the two softmax slots (one row tile) or pair two row tiles.
 //
 // Every wait is bounded (ra::mbar_wait); a wait that runs out records
 // RA_ERR_DEVICE_TIMEOUT in the status word and the CTA unwinds and returns.
