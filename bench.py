@@ -467,8 +467,24 @@ def run_ours(args, rank, world):
             "merge_ms": tm * 1e3, "merge_GB_per_s": mb / tm / 1e9, "merge_frac_hbm": mb / tm / 1e9 / pk["hbm_gbs"],
             "pipeline_ms": (tp + tm) * 1e3, "pipeline_TFLOP_per_s": pf / (tp + tm) / 1e12, "flops": pf,
             "partials_bytes": pO.numel() * 2 + pL.numel() * 4}
+        # the same layer in one fused pass (ra_blockwise_attn_fwd, no partials)
+        fms = timed_steps(lambda: ra.attn(pq, pkk, pv, pw.n_shards, pw.block, pw.causal, out=mO, lse=mL), 2, 1, flush)
+        ra.device_status()
+        tf = statistics.mean(fms) * 1e-3
+        result["llama70b_layer_128k_partials"].update(
+            {"fused_ms": tf * 1e3, "fused_TFLOP_per_s": pf / tf / 1e12, "fused_frac_bf16_peak": pf / tf / 1e12 / pk["bf16_tflops"]})
         del pq, pkk, pv, pO, pL, mO, mL
         torch.cuda.empty_cache()
+
+        # the tiny exact workload (fp32 inputs, fp32 CUDA-core path; latency-bound, time only)
+        tw = WORKLOADS["tiny_exact_f32"]
+        tq, tk, tv = attention_inputs(tw, "cuda")
+        tms = timed_steps(lambda: ra.attn(tq, tk, tv, tw.n_shards, tw.block, tw.causal), 20, 5)
+        ra.device_status()
+        result["tiny_exact_f32"] = {"ms": statistics.median(tms),
+                                    "TFLOP_per_s": ring_flops(tw.B, tw.S, tw.Hq, tw.D, tw.causal) /
+                                                   (statistics.median(tms) * 1e-3) / 1e12}
+        del tq, tk, tv
 
         if args.all:
             sw = WORKLOADS["million_token_stress"]
