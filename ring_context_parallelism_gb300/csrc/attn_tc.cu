@@ -716,8 +716,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr int kBlk = C::kBlk;
                 constexpr int nKc = C::kMaxKV, nVc = C::kNVPair;
                 uint32_t kflip = 0, vflip = 0;
-                // (ring prefill only: the fan-out variants measured slower with it)
-                for (; RING && ok && i + kBlk <= total; i += kBlk) {
+                // (contiguous ring prefill only: the fan-out and zigzag / striped variants
+                // measured slower with it -- their larger code missed the instruction
+                // cache: 3x the no-instruction stalls of the contiguous mode under ncu)
+                for (; MODE == kModeRing && ok && i + kBlk <= total; i += kBlk) {
                     const uint32_t kb = k_lo0, vb = v_lo0, qa = q0, qb = q1;
 #pragma unroll
                     for (int pos = 0; pos < kBlk; ++pos) {
