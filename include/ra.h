@@ -334,6 +334,18 @@ ra_status ra_prefix_fanout_attn_noalloc(const void* q_rows, const int* branch_of
 int ra_ring_shard_order(int S, int n_shards, int causal, int q_row0, int* shard_order);
 
 /*
+ * Host-side view of how a fan-out call splits the shared prefix (no GPU): for
+ * these sizes on n_sm SMs, writes the n_chunks + 1 prefix-tile boundaries
+ * (128-key tiles; chunk c covers tiles [chunk_start[c], chunk_start[c+1]))
+ * and returns n_chunks (<= 64), or -1 on invalid arguments.  chunk_start
+ * holds 65 ints.  The split is chosen by simulating the block scheduler over
+ * the launch's units (prefix chunk x KV head x row pair) and minimising the
+ * makespan; it may make chunks unequal.
+ */
+int ra_prefix_fanout_plan(int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv, int n_sm,
+                          int* chunk_start);
+
+/*
  * Host-side (no GPU): pos[p] = sequence position of storage row p under
  * `layout` (ra_layout) for S rows in n_shards shards.  pos holds S ints.
  * Returns 0, or -1 on invalid arguments (zigzag needs an even shard length).

@@ -1206,75 +1206,6 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
                       : launch<64, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream);
 }
 
-int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_prefix, int S_suffix, int* split_prefix,
-                 int* suffix_slot0) {
-    const int rows_per_tile = kTileM / (Hq / Hkv);
-    if (split_prefix) *split_prefix = (R <= rows_per_tile) ? 1 : 0;
-    if (suffix_slot0) *suffix_slot0 = 0;
-    // with a prefix the suffixes are folded into prefix units; without one,
-    // suffix units write slot 0
-    return S_prefix > 0 ? n_chunks : (S_suffix > 0 ? 1 : 0);
-}
-
-void fanout_split(int n_chunks, int S_prefix, int S_suffix, int n_branches, int n_mpairs, int* chunk_start) {
-    // Prefix tiles per chunk such that prefix + folded suffix work is even: the
-    // chunk of branch b is b % n_chunks; on average a row pair of a chunk meets
-    // its branches' rows in proportion 1/n_mpairs.
-    const int n_tiles = (S_prefix + kTileN - 1) / kTileN;
-    const double s_tiles = (S_suffix > 0 && S_prefix > 0) ? (S_suffix + kTileN - 1) / kTileN : 0;
-    double want[kMaxChunks];
-    double total = n_tiles + s_tiles * n_branches / n_mpairs;
-    double sum = 0;
-    for (int c = 0; c < n_chunks; ++c) {
-        const int nbr = n_branches / n_chunks + (c < n_branches % n_chunks ? 1 : 0);
-        want[c] = total / n_chunks - s_tiles * nbr / n_mpairs;
-        if (want[c] < 1) want[c] = 1;
-        sum += want[c];
-    }
-    // scale to the prefix tile count, cumulative rounding, at least one tile each
-    int prev = 0;
-    double acc = 0;
-    chunk_start[0] = 0;
-    for (int c = 0; c < n_chunks; ++c) {
-        acc += want[c] * n_tiles / sum;
-        int e = static_cast<int>(acc + 0.5);
-        if (e < prev + 1) e = prev + 1;
-        if (e > n_tiles - (n_chunks - 1 - c)) e = n_tiles - (n_chunks - 1 - c);
-        chunk_start[c + 1] = e;
-        prev = e;
-    }
-    chunk_start[n_chunks] = n_tiles;
-}
-
-void fanout_chunking(int R, int S_prefix, int S_suffix, int n_branches, int Hq, int Hkv, int n_sm, int* n_chunks) {
-    const int G = Hq / Hkv;
-    const int rows_per_tile = kTileM / G;
-    const int n_mpairs = (R + 2 * rows_per_tile - 1) / (2 * rows_per_tile);
-    const int n_tiles = (S_prefix + kTileN - 1) / kTileN;
-    if (n_tiles == 0 || n_mpairs == 0) {
-        *n_chunks = 0;
-        return;
-    }
-    const double s_tiles = S_suffix > 0 ? (S_suffix + kTileN - 1) / kTileN : 0;
-    const double work = n_tiles + s_tiles * n_branches / n_mpairs;  // tiles per (KV head, row pair)
-    // Minimise (waves x tiles per unit) on n_sm SMs; ties: fewer chunks (fewer partials).
-    double best = -1;
-    int best_c = 1;
-    const int max_c = n_tiles < kMaxChunks ? n_tiles : kMaxChunks;
-    for (int c = 1; c <= max_c; ++c) {
-        const long long units = static_cast<long long>(Hkv) * n_mpairs * c;
-        const long long waves = (units + n_sm - 1) / n_sm;
-        // + per-unit fixed cost (first loads from HBM, epilogue, partial written
-        // and merged), measured at about ten tiles of work
-        const double cost = waves * (work / c + 10.0) + 1e-3 * c;
-        if (best < 0 || cost < best) {
-            best = cost;
-            best_c = c;
-        }
-    }
-    *n_chunks = best_c;
-}
-
 cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
     TcParams p{};
     p.fanout = 1;

@@ -1,0 +1,195 @@
+// fanout_plan.cu -- host-side planning of a fan-out launch: how many chunks the
+// shared prefix is split into and where their boundaries lie.
+//
+// The units of a fan-out launch are (prefix chunk, KV head, row pair), launched
+// chunk-major with the row pair fastest; each writes one partial per row, and
+// the merge joins them ("AHBM Agentic Runtime Architecture", sections 3.3-3.4:
+// every sequence shard produces a partial state, merged by row).  A unit costs
+// its prefix tiles, the suffix tiles folded into its chunk (branch b's suffix
+// goes to chunk b % n_chunks) and a fixed cost measured at about ten tiles
+// (first loads from HBM, epilogue, its partial written and merged).
+//
+// The plan is chosen by simulating the block scheduler: units in launch order,
+// each started on the SM that frees first, the makespan minimised.  Besides
+// equal chunks it tries shaped splits (one longer chunk, one shorter), which
+// let a launch whose unit count is not a multiple of the SM count finish its
+// second wave together with the first.  Plans are cached per shape.
+#include <algorithm>
+#include <cmath>
+#include <functional>
+#include <map>
+#include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
+
+#include "ra_internal.h"
+
+namespace ra {
+
+namespace {
+
+constexpr int kTileRows = 128;  // query rows of an M tile / keys of a KV tile
+constexpr int kMaxPlanChunks = 64;
+constexpr double kUnitFixedTiles = 10.0;
+
+struct Shape {
+    int n_tiles;       // prefix KV tiles
+    double s_tiles;    // suffix tiles of one branch
+    int n_branches, n_mpairs, Hkv, n_sm;
+};
+
+// Folded suffix tiles an average unit of chunk c carries.
+double folded(const Shape& sh, int n_chunks, int c) {
+    if (sh.s_tiles == 0) return 0;
+    const int nbr = sh.n_branches / n_chunks + (c < sh.n_branches % n_chunks ? 1 : 0);
+    return sh.s_tiles * nbr / sh.n_mpairs;
+}
+
+// Makespan (in tile units) of the greedy schedule of a plan.
+double simulate(const Shape& sh, const std::vector<int>& prefix_tiles) {
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int i = 0; i < sh.n_sm; ++i) free_at.push(0.0);
+    double makespan = 0;
+    const int n = static_cast<int>(prefix_tiles.size());
+    for (int c = 0; c < n; ++c) {
+        const double cost = prefix_tiles[c] + folded(sh, n, c) + kUnitFixedTiles;
+        for (long long u = 0; u < static_cast<long long>(sh.Hkv) * sh.n_mpairs; ++u) {
+            const double t = free_at.top() + cost;
+            free_at.pop();
+            free_at.push(t);
+            makespan = std::max(makespan, t);
+        }
+    }
+    return makespan;
+}
+
+// Prefix tiles per chunk for target work weights (prefix + folded suffix), at
+// least one tile each, summing to n_tiles (cumulative rounding).
+std::vector<int> split(const Shape& sh, const std::vector<double>& weight) {
+    const int n = static_cast<int>(weight.size());
+    double wsum = 0;
+    for (double w : weight) wsum += w;
+    double total = sh.n_tiles;
+    for (int c = 0; c < n; ++c) total += folded(sh, n, c);
+    std::vector<double> want(n);
+    double sum = 0;
+    for (int c = 0; c < n; ++c) {
+        want[c] = std::max(1.0, total * weight[c] / wsum - folded(sh, n, c));
+        sum += want[c];
+    }
+    std::vector<int> tiles(n);
+    double acc = 0;
+    int prev = 0;
+    for (int c = 0; c < n; ++c) {
+        acc += want[c] * sh.n_tiles / sum;
+        int e = static_cast<int>(acc + 0.5);
+        e = std::max(e, prev + 1);
+        e = std::min(e, sh.n_tiles - (n - 1 - c));
+        if (c == n - 1) e = sh.n_tiles;
+        tiles[c] = e - prev;
+        prev = e;
+    }
+    return tiles;
+}
+
+struct Plan {
+    double cost = -1;
+    std::vector<int> tiles;
+};
+
+Plan search(const Shape& sh) {
+    Plan best;
+    const int max_c = std::min(sh.n_tiles, kMaxPlanChunks);
+    auto consider = [&](const std::vector<int>& tiles, double penalty) {
+        const double cost = simulate(sh, tiles) + penalty + 1e-3 * tiles.size();  // ties: fewer partials
+        if (best.cost < 0 || cost < best.cost) {
+            best.cost = cost;
+            best.tiles = tiles;
+        }
+    };
+    for (int c = 1; c <= max_c; ++c) consider(split(sh, std::vector<double>(c, 1.0)), 0);
+    // shaped splits around the best equal split: chunk 1 (or 0) longer, the last shorter
+    const int c0 = static_cast<int>(best.tiles.size());
+    const long long per_chunk = static_cast<long long>(sh.Hkv) * sh.n_mpairs;
+    for (int c = std::max(2, c0 - 1); c <= std::min(max_c, c0 + 1); ++c) {
+        if ((per_chunk * c) % sh.n_sm == 0) continue;  // whole waves: equal chunks are best
+        for (int big_at = 0; big_at <= 1; ++big_at)
+            for (double fb = 1.0; fb <= 3.01; fb += 0.1)
+                for (double fs = 0.2; fs <= 1.01; fs += 0.1) {
+                    std::vector<double> w(c, 1.0);
+                    w[big_at] = fb;
+                    w[c - 1] = std::min(w[c - 1], fs);
+                    // a shaped plan must beat the equal one clearly: the model is approximate
+                    consider(split(sh, w), 1.0);
+                }
+    }
+    return best;
+}
+
+std::mutex g_plan_mu;
+std::map<std::tuple<int, int, int, int, int, int>, std::vector<int>> g_plans;
+
+}  // namespace
+
+int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_prefix, int S_suffix, int* split_prefix,
+                 int* suffix_slot0) {
+    const int rows_per_tile = kTileRows / (Hq / Hkv);
+    if (split_prefix) *split_prefix = (R <= rows_per_tile) ? 1 : 0;
+    if (suffix_slot0) *suffix_slot0 = 0;
+    // with a prefix the suffixes are folded into prefix units; without one,
+    // suffix units write slot 0
+    return S_prefix > 0 ? n_chunks : (S_suffix > 0 ? 1 : 0);
+}
+
+void fanout_plan(int R, int S_prefix, int S_suffix, int n_branches, int Hq, int Hkv, int n_sm, int* n_chunks,
+                 int* chunk_start) {
+    const int rows_per_tile = kTileRows / (Hq / Hkv);
+    Shape sh;
+    sh.n_mpairs = (R + 2 * rows_per_tile - 1) / (2 * rows_per_tile);
+    sh.n_tiles = (S_prefix + kTileRows - 1) / kTileRows;
+    sh.s_tiles = (S_suffix > 0 && S_prefix > 0) ? (S_suffix + kTileRows - 1) / kTileRows : 0;
+    sh.n_branches = n_branches;
+    sh.Hkv = Hkv;
+    sh.n_sm = n_sm > 0 ? n_sm : 1;
+    if (sh.n_tiles == 0 || sh.n_mpairs == 0) {
+        *n_chunks = 0;
+        if (chunk_start) chunk_start[0] = 0;
+        return;
+    }
+    const auto key = std::make_tuple(sh.n_mpairs, sh.n_tiles, static_cast<int>(sh.s_tiles), n_branches, Hkv, sh.n_sm);
+    std::vector<int> tiles;
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mu);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) tiles = it->second;
+    }
+    if (tiles.empty()) {
+        tiles = search(sh).tiles;
+        std::lock_guard<std::mutex> lock(g_plan_mu);
+        if (g_plans.size() > 4096) g_plans.clear();
+        g_plans[key] = tiles;
+    }
+    *n_chunks = static_cast<int>(tiles.size());
+    if (chunk_start) {
+        chunk_start[0] = 0;
+        for (size_t c = 0; c < tiles.size(); ++c) chunk_start[c + 1] = chunk_start[c] + tiles[c];
+    }
+}
+
+void fanout_split_equal(int n_chunks, int R, int S_prefix, int S_suffix, int n_branches, int Hq, int Hkv,
+                        int* chunk_start) {
+    const int rows_per_tile = kTileRows / (Hq / Hkv);
+    Shape sh;
+    sh.n_mpairs = std::max(1, (R + 2 * rows_per_tile - 1) / (2 * rows_per_tile));
+    sh.n_tiles = (S_prefix + kTileRows - 1) / kTileRows;
+    sh.s_tiles = (S_suffix > 0 && S_prefix > 0) ? (S_suffix + kTileRows - 1) / kTileRows : 0;
+    sh.n_branches = n_branches;
+    sh.Hkv = Hkv;
+    sh.n_sm = 1;
+    const std::vector<int> tiles = split(sh, std::vector<double>(n_chunks, 1.0));
+    chunk_start[0] = 0;
+    for (int c = 0; c < n_chunks; ++c) chunk_start[c + 1] = chunk_start[c] + tiles[c];
+}
+
+}  // namespace ra

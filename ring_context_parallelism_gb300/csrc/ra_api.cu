@@ -114,16 +114,8 @@ struct FanoutPlan {
     size_t part_o_bytes, part_lse_bytes, total;
 };
 
-// Sizes of a plan with a given prefix chunk count.
-FanoutPlan plan_with_chunks(int n_chunks, int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv,
-                            int D) {
-    FanoutPlan f{};
-    f.n_chunks = S_prefix > 0 ? n_chunks : 0;
-    if (f.n_chunks > 0) {
-        const int rows_per_tile = 128 / (Hq / Hkv);
-        const int n_mpairs = (R + 2 * rows_per_tile - 1) / (2 * rows_per_tile);
-        ra::fanout_split(f.n_chunks, S_prefix, S_suffix, n_branches, n_mpairs > 0 ? n_mpairs : 1, f.chunk_start);
-    }
+// Slots and workspace bytes of a plan whose chunk count and boundaries are set.
+FanoutPlan finish_plan(FanoutPlan f, int R, int S_prefix, int S_suffix, int Hq, int Hkv, int D) {
     f.P = ra::fanout_slots(R, Hq, Hkv, f.n_chunks, S_prefix, S_suffix, nullptr, nullptr);
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     f.part_o_bytes = up(static_cast<size_t>(f.P) * R * Hq * D * sizeof(float));
@@ -132,10 +124,21 @@ FanoutPlan plan_with_chunks(int n_chunks, int R, int n_branches, int S_prefix, i
     return f;
 }
 
+// A plan with a given prefix chunk count and equal-work chunks.
+FanoutPlan plan_with_chunks(int n_chunks, int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv,
+                            int D) {
+    FanoutPlan f{};
+    f.n_chunks = S_prefix > 0 ? n_chunks : 0;
+    if (f.n_chunks > 0) ra::fanout_split_equal(f.n_chunks, R, S_prefix, S_suffix, n_branches, Hq, Hkv, f.chunk_start);
+    return finish_plan(f, R, S_prefix, S_suffix, Hq, Hkv, D);
+}
+
+// The planned split (chunk count and boundaries from the scheduler simulation).
 FanoutPlan plan_fanout(int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv, int D) {
-    int n_chunks = 0;
-    ra::fanout_chunking(R, S_prefix, S_suffix, n_branches, Hq, Hkv, sm_count(), &n_chunks);
-    return plan_with_chunks(n_chunks, R, n_branches, S_prefix, S_suffix, Hq, Hkv, D);
+    FanoutPlan f{};
+    f.n_chunks = 0;
+    if (S_prefix > 0) ra::fanout_plan(R, S_prefix, S_suffix, n_branches, Hq, Hkv, sm_count(), &f.n_chunks, f.chunk_start);
+    return finish_plan(f, R, S_prefix, S_suffix, Hq, Hkv, D);
 }
 
 ra_status check_fanout(const void* q_rows, const int* offsets, int n_branches, int R, const void* k_prefix,
@@ -491,6 +494,16 @@ ra_status ra_blockwise_attn_bwd_layout(const void* q, const void* k, const void*
                                        void* stream) {
     return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, S, Hq, Hkv, D, n_shards, block, causal, layout, dt,
                       workspace, workspace_bytes, stream);
+}
+
+int ra_prefix_fanout_plan(int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv, int n_sm,
+                          int* chunk_start) {
+    if (R < 1 || n_branches < 1 || S_prefix < 1 || S_suffix < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
+        128 % (Hq / Hkv) || n_sm < 1 || !chunk_start)
+        return -1;
+    int n = 0;
+    ra::fanout_plan(R, S_prefix, S_suffix, n_branches, Hq, Hkv, n_sm, &n, chunk_start);
+    return n;
 }
 
 int ra_layout_positions(int S, int n_shards, int layout, int* pos) {

@@ -58,13 +58,16 @@ cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream);
 int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_prefix, int S_suffix, int* split_prefix,
                  int* suffix_slot0);
 
-// Number of prefix chunks for a fan-out call (shared by the workspace query),
-// at most 64.
-void fanout_chunking(int R, int S_prefix, int S_suffix, int n_branches, int Hq, int Hkv, int n_sm, int* n_chunks);
+// Prefix split of a fan-out call (fanout_plan.cu): the chunk count (at most
+// 64) and the n_chunks + 1 prefix-tile boundaries, from a simulation of the
+// block scheduler; cached per shape.
+void fanout_plan(int R, int S_prefix, int S_suffix, int n_branches, int Hq, int Hkv, int n_sm, int* n_chunks,
+                 int* chunk_start);
 
-// Chunk boundaries (n_chunks + 1 tile indices) balancing prefix tiles against
-// the folded suffix tiles.
-void fanout_split(int n_chunks, int S_prefix, int S_suffix, int n_branches, int n_mpairs, int* chunk_start);
+// Equal-work boundaries for a given chunk count (the no-alloc entry point's
+// fallback when the planned partials do not fit its scratch).
+void fanout_split_equal(int n_chunks, int R, int S_prefix, int S_suffix, int n_branches, int Hq, int Hkv,
+                        int* chunk_start);
 
 // Exact fp32 path (CUDA-core FMA).
 struct RingSimtArgs {

@@ -35,6 +35,7 @@ SIGNATURES = {
                                           _i, _i, _i, _vp, _sz, _vp]),
     "ra_blockwise_attn_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "ra_layout_positions": (_i, [_i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
+    "ra_prefix_fanout_plan": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
     "ra_ring_walk_layout": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int),
                                  ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "ra_lse_merge": (_i, [_vp, _fp, _vp, _fp, _i, _i, _i, _i, _i, _i, _vp]),
@@ -308,6 +309,15 @@ def layout_positions(S: int, n_shards: int, layout) -> list[int]:
     if load().ra_layout_positions(S, n_shards, _layout(layout), buf) != 0:
         raise ValueError("invalid arguments")
     return list(buf[:S])
+
+
+def fanout_plan(R: int, n_branches: int, S_prefix: int, S_suffix: int, Hq: int, Hkv: int, n_sm: int) -> list[int]:
+    """Prefix-tile boundaries of the fan-out split for these sizes (host-side, no GPU)."""
+    buf = (ctypes.c_int * 65)()
+    n = load().ra_prefix_fanout_plan(R, n_branches, S_prefix, S_suffix, Hq, Hkv, n_sm, buf)
+    if n < 0:
+        raise ValueError("invalid arguments")
+    return list(buf[:n + 1])
 
 
 def ring_walk(S: int, n_shards: int, causal: bool, layout, q_row0: int, q_rows: int, tile: int):

@@ -183,3 +183,42 @@ def test_backward_workspace_size(lib):
 def test_selftest_wait_timeout_validation(lib):
     assert lib.ra_selftest_wait_timeout(0, None) == rab.RA_ERR_INVALID_ARG
     assert lib.ra_selftest_wait_timeout(3_000_000_000, None) == rab.RA_ERR_INVALID_ARG
+
+
+def _greedy_makespan(tiles, Hkv, n_mpairs, n_sm, fold, fixed=10.0):
+    """Units in launch order (chunk, KV head, row pair), each on the SM that frees first."""
+    import heapq
+    heap = [0.0] * n_sm
+    span = 0.0
+    for c, t in enumerate(tiles):
+        for _ in range(Hkv * n_mpairs):
+            end = heapq.heappop(heap) + t + fold[c] + fixed
+            span = max(span, end)
+            heapq.heappush(heap, end)
+    return span
+
+
+@pytest.mark.parametrize("R,nb,Sp,Ss,Hq,Hkv,n_sm", [
+    (147, 16, 65536, 512, 64, 8, 152), (16, 16, 65536, 512, 64, 8, 152), (160, 8, 65536, 512, 64, 8, 152),
+    (98, 17, 2500, 384, 64, 8, 152), (16, 16, 65536, 512, 64, 8, 148), (300, 4, 200000, 0, 32, 8, 132),
+    (5, 2, 129, 7, 16, 2, 8)])
+def test_fanout_plan_is_a_valid_split_no_worse_than_equal_chunks(lib, R, nb, Sp, Ss, Hq, Hkv, n_sm):
+    b = ra.fanout_plan(R, nb, Sp, Ss, Hq, Hkv, n_sm)
+    n_tiles = -(-Sp // 128)
+    assert 1 <= len(b) - 1 <= 64 and b[0] == 0 and b[-1] == n_tiles
+    tiles = [b[i + 1] - b[i] for i in range(len(b) - 1)]
+    assert min(tiles) >= 1
+    n_mpairs = -(-R // (2 * (128 // (Hq // Hkv))))
+    s_tiles = -(-Ss // 128)
+
+    def fold(n):   # suffix tiles an average unit of each chunk carries (branch b -> chunk b % n)
+        return [s_tiles * (nb // n + (c < nb % n)) / n_mpairs for c in range(n)]
+
+    got = _greedy_makespan(tiles, Hkv, n_mpairs, n_sm, fold(len(tiles)))
+    # every equal split (as the planner balances it), the best of them
+    best_equal = None
+    for n in range(1, min(64, n_tiles) + 1):
+        q = [n_tiles // n + (c < n_tiles % n) for c in range(n)]
+        span = _greedy_makespan(q, Hkv, n_mpairs, n_sm, fold(n))
+        best_equal = span if best_equal is None else min(best_equal, span)
+    assert got <= best_equal * 1.03, (tiles, got, best_equal)
