@@ -101,6 +101,7 @@ struct Plan {
 Plan search(const Shape& sh) {
     Plan best;
     const int max_c = std::min(sh.n_tiles, kMaxPlanChunks);
+    const long long per_chunk = static_cast<long long>(sh.Hkv) * sh.n_mpairs;
     auto consider = [&](const std::vector<int>& tiles, double penalty) {
         const double cost = simulate(sh, tiles) + penalty + 1e-3 * tiles.size();  // ties: fewer partials
         if (best.cost < 0 || cost < best.cost) {
@@ -108,18 +109,32 @@ Plan search(const Shape& sh) {
             best.tiles = tiles;
         }
     };
-    for (int c = 1; c <= max_c; ++c) consider(split(sh, std::vector<double>(c, 1.0)), 0);
-    // shaped splits around the best equal split: chunk 1 (or 0) longer, the last shorter
-    const int c0 = static_cast<int>(best.tiles.size());
-    const long long per_chunk = static_cast<long long>(sh.Hkv) * sh.n_mpairs;
-    for (int c = std::max(2, c0 - 1); c <= std::min(max_c, c0 + 1); ++c) {
-        if ((per_chunk * c) % sh.n_sm == 0) continue;  // whole waves: equal chunks are best
+    // equal chunks: with equal units the greedy schedule is whole waves, so the
+    // scan uses that closed form, then simulates the best three counts
+    const double work = sh.n_tiles + sh.s_tiles * sh.n_branches / sh.n_mpairs;  // tiles per (KV head, row pair)
+    int c0 = 1;
+    double c0_cost = -1;
+    for (int c = 1; c <= max_c; ++c) {
+        const long long waves = (per_chunk * c + sh.n_sm - 1) / sh.n_sm;
+        const double cost = waves * (work / c + kUnitFixedTiles) + 1e-3 * c;
+        if (c0_cost < 0 || cost < c0_cost) {
+            c0_cost = cost;
+            c0 = c;
+        }
+    }
+    const int c_lo = std::max(1, c0 - 1), c_hi = std::min(max_c, c0 + 1);
+    for (int c = c_lo; c <= c_hi; ++c) consider(split(sh, std::vector<double>(c, 1.0)), 0);
+    // shaped splits (chunk 0 or 1 longer, the last shorter) where the last wave is
+    // partial and the waves are few enough for it to matter
+    for (int c = std::max(2, c_lo); c <= c_hi; ++c) {
+        const long long units = per_chunk * c;
+        if (units % sh.n_sm == 0 || units > 4LL * sh.n_sm) continue;
         for (int big_at = 0; big_at <= 1; ++big_at)
-            for (double fb = 1.0; fb <= 3.01; fb += 0.1)
-                for (double fs = 0.2; fs <= 1.01; fs += 0.1) {
+            for (int ib = 0; ib <= 10; ++ib)
+                for (int is = 0; is <= 4; ++is) {
                     std::vector<double> w(c, 1.0);
-                    w[big_at] = fb;
-                    w[c - 1] = std::min(w[c - 1], fs);
+                    w[big_at] = 1.0 + 0.2 * ib;
+                    w[c - 1] = std::min(w[c - 1], 0.2 + 0.2 * is);
                     // a shaped plan must beat the equal one clearly: the model is approximate
                     consider(split(sh, w), 1.0);
                 }
