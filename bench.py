@@ -587,7 +587,8 @@ def run_reference(args, rank, world):
 
 
 PROFILE_CASES = ("prefill_32k", "prefill_16k", "fanout_decode", "fanout_decode1", "merge_16k", "bwd_16k",
-                 "prefill_32k_zigzag", "prefill_32k_striped", "fanout_prefill_8x20", "fanout_decode1_paged16")
+                 "prefill_32k_zigzag", "prefill_32k_striped", "fanout_prefill_8x20", "fanout_decode1_paged16",
+                 "bwd_16k_zigzag")
 
 
 def run_profile_case(case):
@@ -648,17 +649,19 @@ def run_profile_case(case):
         for _ in range(3):
             ra.fanout(x["q_rows"], x["offsets"], x["k_prefix"], x["v_prefix"], x["k_suffix"], x["v_suffix"],
                       workspace=ws)
-    elif case == "bwd_16k":
-        # backward of the causal GQA workload at 16384 tokens (Hq 32, Hkv 8, D 128): 3 calls
+    elif case in ("bwd_16k", "bwd_16k_zigzag"):
+        # backward of the causal GQA workload at 16384 tokens (Hq 32, Hkv 8, D 128), contiguous
+        # or with the rows in the zigzag layout: 3 calls
         from ring_context_parallelism_gb300.inputs import randn
+        lay = "zigzag" if case.endswith("zigzag") else "contiguous"
         w = small(WORKLOADS[HEADLINE], S=16384)
         q, k, v = attention_inputs(w, "cuda")
-        o, l = ra.attn(q, k, v, w.n_shards, w.block, True)
+        o, l = ra.attn(q, k, v, w.n_shards, w.block, True, layout=lay)
         g = torch.Generator(device="cuda")
         g.manual_seed(w.seed + 4242)
         dO = randn(tuple(q.shape), g, q.dtype, "cuda")
         for _ in range(3):
-            ra.attn_bwd(q, k, v, o, l, dO, w.n_shards, w.block, True)
+            ra.attn_bwd(q, k, v, o, l, dO, w.n_shards, w.block, True, layout=lay)
     elif case == "merge_16k":
         # per-shard partials of a 16384-token, 64-head causal layer (16 shards), then 3 merges
         w = small(WORKLOADS["llama70b_layer_128k_partials"], S=16384)
