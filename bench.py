@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, valid only while the kernel source hashes to the recorded value.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the timed 32768-token configuration
-    # (bench.py --profile-case prefill_32k, third launch): 403160064 read + 243380224 written
-    "289fe85b80a466a7": 646540288,
+    # (bench.py --profile-case prefill_32k, third launch): 403492608 read + 243308288 written
+    "0b8a635732b8d159": 646800896,
 }
 
 
