@@ -66,7 +66,8 @@ struct BwdCfg {
     // lse2 and delta of its 128 rows
     static constexpr int kKvS = D == 128 ? 2 : 4;
     static constexpr int kVecOff = (2 + 2 * kKvS) * kTileBytes;
-    static constexpr int kKvBarOff = kVecOff + kKvS * 1024;
+    static constexpr int kInfoOff = kVecOff + kKvS * 1024;  // [kKvS] int2 per Q stage (layout walk)
+    static constexpr int kKvBarOff = kInfoOff + 64;
     static constexpr int kNumBars = 24;
     static constexpr int kDqSmem = kDqBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
     static constexpr int kKvSmem = kKvBarOff + kNumBars * 8 + 16 + 1024;
@@ -542,10 +543,10 @@ struct QWalkL {
             skip_empty();
         }
     }
-    __device__ __forceinline__ int col_lo(int, int key_pos) const {
-        if (qt >= full) return 0;
-        return max(0, shard_visible(layout, L, N, a, key_pos - 1) - qt * kT);
-    }
+    // The query shard of a tile that masks per key row, or -1 where the tile sees
+    // every key: key row at position kp sees the tile's columns from
+    // max(0, shard_visible(.., shard, kp - 1) - qt * kT) on.
+    __device__ __forceinline__ int col_lo_shard() const { return qt >= full ? -1 : a; }
 };
 
 template <int D, bool LAY>
@@ -572,6 +573,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* q_smem = smem + 2 * C::kTileBytes;
     uint8_t* do_smem = q_smem + NS * C::kTileBytes;
     float* vec = reinterpret_cast<float*>(smem + C::kVecOff);  // [NS][lse2 128 | delta 128]
+    // LAY: per Q stage (query shard, first row of the tile), or shard -1 where the
+    // tile sees every key; written by the Q producer before the stage's arrive
+    int2* stage_info = reinterpret_cast<int2*>(smem + C::kInfoOff);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kKvBarOff);
     uint64_t* kv_full = bars;
     uint64_t* q_full = bars + 1;
@@ -649,6 +653,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&empty[st.s], st.ph ^ 1, abort_flag, status, 0x21000000u | (2 * u + (is_q ? 0 : 1))))
                     break;
                 const int q0 = it.a * L + it.qt * kT, h = hk * p.G + it.g;
+                if constexpr (LAY) {
+                    if (is_q) stage_info[st.s] = make_int2(it.col_lo_shard(), it.qt * kT);
+                }
                 mbar_arrive_expect_tx(&full[st.s], C::kTileBytes + (is_q ? 1024 : 0));
                 load_tile<D>(map, &full[st.s], ring + st.s * C::kTileBytes, h, q0, b);
                 if (is_q) {
@@ -725,16 +732,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS = tmem_base + lane_off, tdP = tS + 128, tdV = tS + 256, tdK = tS + 256 + D;
         const float sl2 = p.scale_log2;
+        // the layout kernels read the walk's position from the stage (stage_info);
+        // only the contiguous walk is stepped here
         Walk it = qw;
         Stage st;
         bool ok = true;
-        for (int u = 0; u < total; ++u, it.next()) {
+        for (int u = 0; u < total; ++u) {
             if (!(ok = mbar_wait(s_full, u & 1, abort_flag, status, 0x26000000u | u))) break;
             // the stage's lse2 / delta came with its Q tile (already landed: the MMA read it)
             if (!(ok = mbar_wait(&q_full[st.s], st.ph, abort_flag, status, 0x27000000u | u))) break;
             tc_fence_after();
             // key row `key` is visible to the query columns c >= lo of this tile
-            const int lo = it.col_lo(lane_row, key_pos);
+            int lo;
+            if constexpr (LAY) {
+                const int2 si = stage_info[st.s];
+                lo = si.x < 0 ? 0 : max(0, shard_visible(p.layout, L, p.n_shards, si.x, key_pos - 1) - si.y);
+            } else {
+                lo = it.col_lo(lane_row, key_pos);
+                it.next();
+            }
             const float* lse2v = vec + st.s * 256;
             const float* dltv = lse2v + 128;
             // P^T = exp(S^T - L) for this thread's half of the columns, packed over its S^T columns
