@@ -404,8 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float y0, y1;
                     ffma2(y0, y1, __uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]), sl2, sl2, -lse2_r,
                           -lse2_r);
-                    pr[c * 32 + 2 * j] = col0 + 2 * j <= lim ? ex2_approx(y0) : 0.f;
-                    pr[c * 32 + 2 * j + 1] = col0 + 2 * j + 1 <= lim ? ex2_approx(y1) : 0.f;
+                    pr[c * 32 + 2 * j] = ex2_approx(y0);
+                    pr[c * 32 + 2 * j + 1] = ex2_approx(y1);
+                }
+                // masked columns (diagonal / partly visible tiles only) are zeroed
+                // after the fact, so full tiles run no compare (values past lim may
+                // be inf: they are replaced, never used)
+                if (lim < col0 + 31) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (col0 + j > lim) pr[c * 32 + j] = 0.f;
                 }
             }
             // dS = P (dP - Delta), packed bf16 over this half's own S columns
@@ -768,12 +776,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float y0, y1;
                     ffma2(y0, y1, __uint_as_float(sv[2 * jj]), __uint_as_float(sv[2 * jj + 1]), sl2, sl2, -L2.x,
                           -L2.y);
-                    const float p0 = cc >= lo ? ex2_approx(y0) : 0.f;
-                    const float p1 = cc + 1 >= lo ? ex2_approx(y1) : 0.f;
-                    pr[c * 32 + 2 * jj] = p0;
-                    pr[c * 32 + 2 * jj + 1] = p1;
-                    pp[jj] = pack_bf16x2(p0, p1);
+                    pr[c * 32 + 2 * jj] = ex2_approx(y0);
+                    pr[c * 32 + 2 * jj + 1] = ex2_approx(y1);
                 }
+                // masked columns (diagonal / partly visible tiles only) are zeroed
+                // after the fact, so full tiles run no compare
+                if (lo > col0) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (col0 + e < lo) pr[c * 32 + e] = 0.f;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) pp[jj] = pack_bf16x2(pr[c * 32 + 2 * jj], pr[c * 32 + 2 * jj + 1]);
                 tmem_st16(tS + hw * 64 + c * 16, pp);
             }
             tmem_wait_st();
