@@ -426,9 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tdP + col0, dp);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    pk[j] = pack_bf16x2(pr[c * 32 + 2 * j] * (__uint_as_float(dp[2 * j]) - delta_r),
-                                        pr[c * 32 + 2 * j + 1] * (__uint_as_float(dp[2 * j + 1]) - delta_r));
+                for (int j = 0; j < 16; ++j) {
+                    float d0 = __uint_as_float(dp[2 * j]), d1 = __uint_as_float(dp[2 * j + 1]);
+                    fadd2(d0, d1, -delta_r, -delta_r);
+                    fmul2(d0, d1, pr[c * 32 + 2 * j], pr[c * 32 + 2 * j + 1]);
+                    pk[j] = pack_bf16x2(d0, d1);
+                }
                 tmem_st16(tS + hw * 64 + c * 16, pk);
             }
             tmem_wait_st();
@@ -770,14 +773,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tS + col0, sv);
                 tmem_wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int cc = col0 + 2 * jj;
-                    const float2 L2 = *reinterpret_cast<const float2*>(lse2v + cc);
-                    float y0, y1;
-                    ffma2(y0, y1, __uint_as_float(sv[2 * jj]), __uint_as_float(sv[2 * jj + 1]), sl2, sl2, -L2.x,
-                          -L2.y);
-                    pr[c * 32 + 2 * jj] = ex2_approx(y0);
-                    pr[c * 32 + 2 * jj + 1] = ex2_approx(y1);
+                for (int jq = 0; jq < 8; ++jq) {
+                    const int e = 4 * jq;
+                    const float4 L4 = *reinterpret_cast<const float4*>(lse2v + col0 + e);
+                    float y0, y1, y2, y3;
+                    ffma2(y0, y1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sl2, sl2, -L4.x, -L4.y);
+                    ffma2(y2, y3, __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]), sl2, sl2, -L4.z, -L4.w);
+                    pr[c * 32 + e] = ex2_approx(y0);
+                    pr[c * 32 + e + 1] = ex2_approx(y1);
+                    pr[c * 32 + e + 2] = ex2_approx(y2);
+                    pr[c * 32 + e + 3] = ex2_approx(y3);
                 }
                 // masked columns (diagonal / partly visible tiles only) are zeroed
                 // after the fact, so full tiles run no compare
@@ -803,11 +808,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tdP + col0, dp);
                 tmem_wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int cc = col0 + 2 * jj;
-                    const float2 DL = *reinterpret_cast<const float2*>(dltv + cc);
-                    pd[jj] = pack_bf16x2(pr[c * 32 + 2 * jj] * (__uint_as_float(dp[2 * jj]) - DL.x),
-                                         pr[c * 32 + 2 * jj + 1] * (__uint_as_float(dp[2 * jj + 1]) - DL.y));
+                for (int jq = 0; jq < 8; ++jq) {
+                    const int e = 4 * jq;
+                    const float4 D4 = *reinterpret_cast<const float4*>(dltv + col0 + e);
+                    float d0 = __uint_as_float(dp[e]), d1 = __uint_as_float(dp[e + 1]);
+                    float d2 = __uint_as_float(dp[e + 2]), d3 = __uint_as_float(dp[e + 3]);
+                    fadd2(d0, d1, -D4.x, -D4.y);
+                    fadd2(d2, d3, -D4.z, -D4.w);
+                    fmul2(d0, d1, pr[c * 32 + e], pr[c * 32 + e + 1]);
+                    fmul2(d2, d3, pr[c * 32 + e + 2], pr[c * 32 + e + 3]);
+                    pd[2 * jq] = pack_bf16x2(d0, d1);
+                    pd[2 * jq + 1] = pack_bf16x2(d2, d3);
                 }
                 tmem_st16(tdP + hw * 64 + c * 16, pd);
             }
