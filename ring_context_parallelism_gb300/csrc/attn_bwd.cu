@@ -119,6 +119,15 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* out, const T* do
     }
 }
 
+// (a0, a1) *= (b0, b1), one packed fp32x2 multiply.
+__device__ __forceinline__ void fmul2(float& a0, float& a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
 // ---------------------------------------------------------------------------
 // MMA issue helpers
 // ---------------------------------------------------------------------------

@@ -284,15 +284,6 @@ __device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) 
         : "f"(b0), "f"(b1));
 }
 
-// (a0, a1) *= (b0, b1), one packed fp32x2 multiply.
-__device__ __forceinline__ void fmul2(float& a0, float& a1, float b0, float b1) {
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
-        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(b0), "f"(b1));
-}
-
 // max(a, b, c) in one three-input instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
