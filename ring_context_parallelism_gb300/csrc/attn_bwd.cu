@@ -401,18 +401,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lim = min(lim, row - it.kb);
             }
             // P = exp(S - L) for this thread's half of the columns
+            // both 32-column chunks are loaded before one wait (one TMEM round trip)
             float pr[64];
+            uint32_t sv[64];
+            tmem_ld32(tS + hw * 64, sv);
+            tmem_ld32(tS + hw * 64 + 32, sv + 32);
+            tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int col0 = hw * 64 + c * 32;
-                uint32_t sv[32];
-                tmem_ld32(tS + col0, sv);
-                tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     float y0, y1;
-                    ffma2(y0, y1, __uint_as_float(sv[2 * j]), __uint_as_float(sv[2 * j + 1]), sl2, sl2, -lse2_r,
-                          -lse2_r);
+                    ffma2(y0, y1, __uint_as_float(sv[c * 32 + 2 * j]), __uint_as_float(sv[c * 32 + 2 * j + 1]), sl2,
+                          sl2, -lse2_r, -lse2_r);
                     pr[c * 32 + 2 * j] = ex2_approx(y0);
                     pr[c * 32 + 2 * j + 1] = ex2_approx(y1);
                 }
@@ -774,20 +776,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* lse2v = vec + st.s * 256;
             const float* dltv = lse2v + 128;
             // P^T = exp(S^T - L) for this thread's half of the columns, packed over its S^T columns
+            // both 32-column chunks are loaded before one wait (one TMEM round trip),
+            // the first chunk's lse2 read from shared memory meanwhile
             float pr[64];
+            uint32_t sv[64];
+            tmem_ld32(tS + hw * 64, sv);
+            tmem_ld32(tS + hw * 64 + 32, sv + 32);
+            float4 L0[8];
+#pragma unroll
+            for (int jq = 0; jq < 8; ++jq) L0[jq] = *reinterpret_cast<const float4*>(lse2v + hw * 64 + 4 * jq);
+            tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int col0 = hw * 64 + c * 32;
-                uint32_t sv[32], pp[16];
-                tmem_ld32(tS + col0, sv);
-                tmem_wait_ld();
+                uint32_t pp[16];
 #pragma unroll
                 for (int jq = 0; jq < 8; ++jq) {
                     const int e = 4 * jq;
-                    const float4 L4 = *reinterpret_cast<const float4*>(lse2v + col0 + e);
+                    const float4 L4 = c == 0 ? L0[jq] : *reinterpret_cast<const float4*>(lse2v + col0 + e);
                     float y0, y1, y2, y3;
-                    ffma2(y0, y1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sl2, sl2, -L4.x, -L4.y);
-                    ffma2(y2, y3, __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]), sl2, sl2, -L4.z, -L4.w);
+                    ffma2(y0, y1, __uint_as_float(sv[c * 32 + e]), __uint_as_float(sv[c * 32 + e + 1]), sl2, sl2,
+                          -L4.x, -L4.y);
+                    ffma2(y2, y3, __uint_as_float(sv[c * 32 + e + 2]), __uint_as_float(sv[c * 32 + e + 3]), sl2, sl2,
+                          -L4.z, -L4.w);
                     pr[c * 32 + e] = ex2_approx(y0);
                     pr[c * 32 + e + 1] = ex2_approx(y1);
                     pr[c * 32 + e + 2] = ex2_approx(y2);
