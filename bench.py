@@ -62,6 +62,14 @@ def fanout_flops(R, Hq, D, S_prefix, S_suffix):
     return 4 * D * Hq * R * (S_prefix + S_suffix)
 
 
+def fanout_prefill_flops(rows, Hq, D, S_prefix, S_suffix):
+    """Fan-out prefill with a causal suffix: row t of a branch with n new rows is
+    suffix token S_suffix - n + t and sees the whole prefix plus suffix keys up to
+    itself."""
+    vis = sum(S_prefix + S_suffix - n + t + 1 for n in rows for t in range(n))
+    return 4 * D * Hq * vis
+
+
 def fanout_bytes(R, n_branches, Hq, Hkv, D, S_prefix, S_suffix, esz=2):
     """Prefix K+V once, every suffix K+V once, Q in, O out, lse out."""
     kv = 2 * esz * Hkv * D * (S_prefix + n_branches * S_suffix)
@@ -426,9 +434,7 @@ def run_ours(args, rank, world):
         ra.device_status()
         t = statistics.median(pms) * 1e-3
         n_b = x["rows"][0]
-        # visible keys per row: the whole prefix plus S_suffix - n_b + t + 1 suffix keys
-        vis = sum(fw.S_prefix + fw.S_suffix - n + tt + 1 for n in x["rows"] for tt in range(n))
-        pf = 4 * fw.D * fw.Hq * vis
+        pf = fanout_prefill_flops(x["rows"], fw.Hq, fw.D, fw.S_prefix, fw.S_suffix)
         by = fanout_bytes(R, fw.n_branches, fw.Hq, fw.Hkv, fw.D, fw.S_prefix, fw.S_suffix)
         result["fanout_prefill_8x20"] = {"R": R, "rows_per_branch": n_b, "us": t * 1e6, "TFLOP_per_s": pf / t / 1e12,
                                          "frac_bf16_peak": pf / t / 1e12 / pk["bf16_tflops"],
