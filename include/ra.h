@@ -353,6 +353,20 @@ int ra_prefix_fanout_plan(int R, int n_branches, int S_prefix, int S_suffix, int
 int ra_layout_positions(int S, int n_shards, int layout, int* pos);
 
 /*
+ * Host-side (no GPU): the order in which the causal kernels launch the tiles of
+ * `tile_rows` storage rows.  Under the causal mask a query's work grows with its
+ * position (the load imbalance of "RingAttention and Context Parallelism:
+ * Mathematical Foundations ...", section 5); the kernels launch the tiles
+ * heaviest first, which keeps the last wave of the grid short.  row0[r] = first
+ * storage row of the r-th query tile launched; the
+ * backward's key tiles are launched in the reverse order (a key's work shrinks
+ * with its position).  row0 holds S / tile_rows ints.  Returns 0, or -1 on
+ * invalid arguments (S % n_shards, the shard length -- half of it for zigzag --
+ * % tile_rows, zigzag with an odd shard length).
+ */
+int ra_tile_launch_order(int S, int n_shards, int layout, int tile_rows, int* row0);
+
+/*
  * Host-side view of the walk of one query tile under a layout: the query rows
  * [q_row0, q_row0 + q_rows) (inside one shard; for zigzag inside one half of
  * it), KV tiles of `tile` keys.  Writes, for each visited shard in ring order,

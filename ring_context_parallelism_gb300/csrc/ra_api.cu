@@ -515,6 +515,16 @@ int ra_layout_positions(int S, int n_shards, int layout, int* pos) {
     return 0;
 }
 
+int ra_tile_launch_order(int S, int n_shards, int layout, int tile_rows, int* row0) {
+    if (S < 1 || n_shards < 1 || S % n_shards || tile_rows < 1 || !row0) return -1;
+    if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIPED) return -1;
+    const int L = S / n_shards;
+    const int span = layout == RA_LAYOUT_ZIGZAG ? L / 2 : L;  // a tile stays inside one span
+    if ((layout == RA_LAYOUT_ZIGZAG && L % 2) || span % tile_rows) return -1;
+    for (int r = 0; r < S / tile_rows; ++r) row0[r] = ra::heavy_tile_row0(layout, S, n_shards, tile_rows, r);
+    return 0;
+}
+
 int ra_ring_walk_layout(int S, int n_shards, int causal, int layout, int q_row0, int q_rows, int tile,
                         int* shard_order, int* visible_keys, int* total_tiles) {
     if (S < 1 || n_shards < 1 || S % n_shards || !shard_order || !visible_keys || !total_tiles) return -1;

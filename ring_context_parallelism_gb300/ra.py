@@ -35,6 +35,7 @@ SIGNATURES = {
                                           _i, _i, _i, _vp, _sz, _vp]),
     "ra_blockwise_attn_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "ra_layout_positions": (_i, [_i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
+    "ra_tile_launch_order": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
     "ra_prefix_fanout_plan": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
     "ra_ring_walk_layout": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int),
                                  ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
@@ -309,6 +310,15 @@ def layout_positions(S: int, n_shards: int, layout) -> list[int]:
     if load().ra_layout_positions(S, n_shards, _layout(layout), buf) != 0:
         raise ValueError("invalid arguments")
     return list(buf[:S])
+
+
+def tile_launch_order(S: int, n_shards: int, layout, tile_rows: int) -> list[int]:
+    """First storage row of each query tile in the causal kernels' launch order, heaviest first
+    (host-side, no GPU)."""
+    buf = (ctypes.c_int * max(S // max(tile_rows, 1), 1))()
+    if load().ra_tile_launch_order(S, n_shards, _layout(layout), tile_rows, buf) != 0:
+        raise ValueError("invalid arguments")
+    return list(buf[:S // tile_rows])
 
 
 def fanout_plan(R: int, n_branches: int, S_prefix: int, S_suffix: int, Hq: int, Hkv: int, n_sm: int) -> list[int]:

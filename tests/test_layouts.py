@@ -186,3 +186,33 @@ def test_oracle_on_stored_layout_equals_sequence_order(layout):
     mO, mL = oracle.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
     assert np.abs(mO - Os).max() <= 1e-12
     assert np.abs(mL - lses).max() <= 1e-12
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("S,N,tile", [(1024, 4, 128), (2048, 8, 32), (4096, 2, 128), (1024, 8, 64), (768, 3, 32)])
+def test_tile_launch_order_is_a_heaviest_first_permutation(lib, layout, S, N, tile):
+    """The causal kernels (forward tensor-core and fp32, both backward kernels)
+    take their tiles in this order, so it must visit every tile once; under the
+    causal mask a tile's work is the keys its rows see, and the order must not
+    increase it."""
+    span = S // N // 2 if layout == "zigzag" else S // N
+    if span % tile:
+        with pytest.raises(ValueError):
+            ra.tile_launch_order(S, N, layout, tile)
+        return
+    order = ra.tile_launch_order(S, N, layout, tile)
+    assert sorted(order) == list(range(0, S, tile))
+    pos = page_positions(S, N, layout)
+    # causal work of a tile: each row at position p sees p + 1 keys
+    work = [sum(pos[r] + 1 for r in range(r0, r0 + tile)) for r0 in order]
+    assert all(a >= b for a, b in zip(work, work[1:]))
+    # the rows of a tile stay inside one contiguous run of the layout (positions increase)
+    for r0 in order:
+        assert all(pos[r] < pos[r + 1] for r in range(r0, r0 + tile - 1))
+
+
+def test_tile_launch_order_rejects_invalid_arguments(lib):
+    for args in [(1000, 3, "contiguous", 128), (1024, 4, "zigzag", 256), (1024, 0, "striped", 32),
+                 (1024, 4, "contiguous", 0), (1026, 2, "zigzag", 1)]:
+        with pytest.raises(ValueError):
+            ra.tile_launch_order(*args)
