@@ -2,6 +2,7 @@
 check that the pins catch every one of them."""
 import os
 
+import numpy as np
 import pytest
 
 import oracle
@@ -53,3 +54,56 @@ def test_pins_catch_planted_mistake(mutant, tmp_path):
     finally:
         oracle.use_library(None)
     assert caught, f"no pin caught mutant {mutant}: {MUTANTS[mutant]}"
+
+
+# The paged fan-out oracle gathers the pages in Python before the C oracle runs,
+# so its mistakes are planted by swapping in a variant of that gather.
+PAGED_MUTANTS = {
+    "prefix pages in reverse order": dict(reverse_prefix=True),
+    "every branch reads branch 0's private pages": dict(branch0=True),
+    "last prefix page not cut at S_prefix": dict(no_cut=True),
+    "V read through the K pool": dict(v_from_k=True),
+}
+
+
+def _paged_variant(reverse_prefix=False, branch0=False, no_cut=False, v_from_k=False):
+    def fanout_paged(q_rows, offsets, k_pages, v_pages, prefix_pages, S_prefix, suffix_pages, S_suffix, *, dtype,
+                     sel=None, suffix_causal=False):
+        kpool = np.ascontiguousarray(k_pages)
+        vpool = kpool if v_from_k else np.ascontiguousarray(v_pages)
+        _, _, Hkv, D = kpool.shape
+        pre = np.asarray(prefix_pages, np.int64)
+        suf = np.asarray(suffix_pages, np.int64)
+        if reverse_prefix:
+            pre = pre[::-1]
+        if branch0:
+            suf = np.repeat(suf[:1], len(suf), axis=0)
+        nb = suf.shape[0]
+        n_pre = None if no_cut else S_prefix
+        kp = kpool[pre].reshape(-1, Hkv, D)[:n_pre]
+        vp = vpool[pre].reshape(-1, Hkv, D)[:n_pre]
+        ks = kpool[suf.reshape(-1)].reshape(nb, -1, Hkv, D)[:, :S_suffix]
+        vs = vpool[suf.reshape(-1)].reshape(nb, -1, Hkv, D)[:, :S_suffix]
+        return oracle.fanout(q_rows, offsets, np.ascontiguousarray(kp), np.ascontiguousarray(vp),
+                             np.ascontiguousarray(ks), np.ascontiguousarray(vs), dtype=dtype, sel=sel,
+                             suffix_causal=suffix_causal)
+    return fanout_paged
+
+
+def test_paged_gather_variant_without_mistake_passes(monkeypatch):
+    """The harness itself: the variant with nothing planted passes the pin."""
+    monkeypatch.setattr(oracle, "fanout_paged", _paged_variant())
+    for page_size in (1, 4, 16):
+        pins.test_fanout_paged_equals_contiguous(page_size)
+
+
+@pytest.mark.parametrize("mutant", sorted(PAGED_MUTANTS))
+def test_paged_pin_catches_planted_mistake(mutant, monkeypatch):
+    monkeypatch.setattr(oracle, "fanout_paged", _paged_variant(**PAGED_MUTANTS[mutant]))
+    caught = 0
+    for page_size in (1, 4, 16):
+        try:
+            pins.test_fanout_paged_equals_contiguous(page_size)
+        except (AssertionError, ValueError):
+            caught += 1
+    assert caught, f"the paged pin did not catch: {mutant}"
