@@ -25,7 +25,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "attn_oracle.c")
+SOURCE = _SRC = os.path.join(_HERE, "attn_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -33,18 +33,17 @@ _lib = None
 DTYPES = {"f32": 0, "bf16": 1, "f64": 2}
 
 
-def build(force: bool = False, mutant: int = 0, out: str | None = None) -> str:
+def build(force: bool = False, src: str | None = None, out: str | None = None) -> str:
     """Compile attn_oracle.c into liboracle.so (gcc, -O2, OpenMP).
 
-    ``mutant`` > 0 builds a copy with one deliberately planted mistake (for the
-    test that checks the pins catch it) into ``out``."""
+    ``src`` / ``out`` compile another source file into another library (the
+    test that plants mistakes in a patched copy of the oracle uses them)."""
     path = out or _LIB_PATH
-    if (not force and not mutant and os.path.exists(path)
+    if (not force and src is None and os.path.exists(path)
             and os.path.getmtime(path) >= os.path.getmtime(_SRC)):
         return path
     tmp = path + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11", f"-DORACLE_MUTANT={int(mutant)}",
-           _SRC, "-o", tmp, "-lm"]
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11", src or _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, path)
     return path

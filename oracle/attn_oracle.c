@@ -49,12 +49,6 @@
 
 enum { OR_F32 = 0, OR_BF16 = 1, OR_F64 = 2 };
 
-/* ORACLE_MUTANT plants one deliberate mistake, so that a test can check that
- * the pins catch it.  The default build (no macro) is the oracle. */
-#ifndef ORACLE_MUTANT
-#define ORACLE_MUTANT 0
-#endif
-
 /* Widen one stored element to double.  bf16 is the upper half of an IEEE
  * binary32, so the widening is exact. */
 static double load_elem(const void* base, int dtype, int64_t idx) {
@@ -96,17 +90,10 @@ static double softmax_row(const double* q_row, const key_ref* keys, int64_t n, i
                           int dtype, double scale, double* s, double* out) {
     for (int d = 0; d < D; ++d) out[d] = 0.0;
     if (n == 0) return -INFINITY;
-#if ORACLE_MUTANT == 6
-    if (n > 1) --n; /* mutant: drop the last visible key */
-#endif
     double m = -INFINITY;
     for (int64_t j = 0; j < n; ++j) {
         double acc = 0.0;
-#if ORACLE_MUTANT == 5
-        for (int d = 0; d < D; ++d) acc += q_row[d] * load_elem(keys[j].v, dtype, keys[j].off + d);
-#else
         for (int d = 0; d < D; ++d) acc += q_row[d] * load_elem(keys[j].k, dtype, keys[j].off + d);
-#endif
         s[j] = acc * scale;
         if (s[j] > m) m = s[j];
     }
@@ -117,11 +104,7 @@ static double softmax_row(const double* q_row, const key_ref* keys, int64_t n, i
         for (int d = 0; d < D; ++d) out[d] += p * load_elem(keys[j].v, dtype, keys[j].off + d);
     }
     for (int d = 0; d < D; ++d) out[d] /= l;
-#if ORACLE_MUTANT == 3
-    return m + log2(l); /* mutant: wrong log base */
-#else
     return m + log(l);
-#endif
 }
 
 /*
@@ -142,11 +125,7 @@ int oracle_attention(const void* q, const void* k, const void* v, int dtype,
     if (kv_begin < 0 || kv_end > S || kv_begin > kv_end) return -1;
     const int64_t n_q = sel ? n_sel : (int64_t)B * S * Hq;
     const int group = Hq / Hkv;
-#if ORACLE_MUTANT == 1
-    const double scale = 1.0 / (double)D; /* mutant: wrong softmax scale */
-#else
     const double scale = 1.0 / sqrt((double)D);
-#endif
     int bad = 0;
 #pragma omp parallel
     {
@@ -162,26 +141,13 @@ int oracle_attention(const void* q, const void* k, const void* v, int dtype,
             const int64_t bi = id / Hq;
             const int i = (int)(bi % S);
             const int b = (int)(bi / S);
-#if ORACLE_MUTANT == 4
-            const int hk = h % Hkv; /* mutant: interleaved instead of grouped GQA heads */
-#else
             const int hk = h / group;
-#endif
             for (int d = 0; d < D; ++d) q_row[d] = load_elem(q, dtype, id * D + d);
             int64_t n = 0;
             int hi = kv_end;
-#if ORACLE_MUTANT == 2
-            if (causal && i < hi) hi = i; /* mutant: causal mask drops the diagonal */
-            if (hi < kv_begin) hi = kv_begin;
-#else
             if (causal && i + 1 < hi) hi = i + 1;
-#endif
             for (int j = kv_begin; j < (pos ? kv_end : hi); ++j) {
-#if ORACLE_MUTANT == 8
-                if (pos && causal && j > i) continue; /* mutant: mask on stored order, not positions */
-#else
                 if (pos && causal && pos[j] > pos[i]) continue;
-#endif
                 keys[n].k = k;
                 keys[n].v = v;
                 keys[n].off = (((int64_t)b * S + j) * Hkv + hk) * D;
@@ -256,11 +222,7 @@ int oracle_fanout(const void* q_rows, const int32_t* off, int nb, int R,
                 ++n;
             }
             /* suffix keys this row sees: all, or up to its own suffix position */
-#if ORACLE_MUTANT == 11
-            const int last = suffix_causal ? Ss - (off[b + 1] - off[b]) + (r - off[b]) - 1 : Ss - 1; /* mutant */
-#else
             const int last = suffix_causal ? Ss - (off[b + 1] - off[b]) + (r - off[b]) : Ss - 1;
-#endif
             for (int j = 0; j < Ss && j <= last; ++j) {
                 keys[n].k = k_suffix;
                 keys[n].v = v_suffix;
@@ -320,9 +282,7 @@ int oracle_lse_merge(const double* part_O, const double* part_lse, int P, int B,
             wsum += w;
             for (int d = 0; d < D; ++d) o[d] += w * part_O[p * o_stride + id * D + d];
         }
-#if ORACLE_MUTANT != 7
-        for (int d = 0; d < D; ++d) o[d] /= wsum; /* mutant 7 forgets the normaliser */
-#endif
+        for (int d = 0; d < D; ++d) o[d] /= wsum;
         out_lse[lidx] = M + log(wsum);
     }
     return 0;
@@ -372,11 +332,7 @@ static void backward_row(const double* q_row, const double* do_row, const key_re
         delta += P[j] * dp;
     }
     for (int64_t j = 0; j < n; ++j) {
-#if ORACLE_MUTANT == 9
-        dS[j] = P[j] * dS[j]; /* mutant: the softmax Jacobian's row term dropped */
-#else
         dS[j] = P[j] * (dS[j] - delta);
-#endif
     }
 }
 
@@ -432,11 +388,7 @@ int oracle_attention_bwd(const void* q, const void* k, const void* v, const void
                         const int64_t koff = keys[jj].off;  /* the key's row in k, v, dk, dv */
                         for (int d = 0; d < D; ++d) {
                             dqi[d] += scale * dS[jj] * load_elem(k, dtype, koff + d);
-#if ORACLE_MUTANT == 10
-                            dk[koff + d] += dS[jj] * q_row[d]; /* mutant: dK without the softmax scale */
-#else
                             dk[koff + d] += scale * dS[jj] * q_row[d];
-#endif
                             dv[koff + d] += P[jj] * do_row[d];
                         }
                     }

@@ -171,13 +171,8 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         // pages ([S, Hkv, D] layout).
         mp = idx % p.n_mpairs;
         const int rest = idx / p.n_mpairs;
-#ifndef RA_FANOUT_CHUNK_FASTEST
         u.kv_head = rest % p.Hkv;
         const int chunk = rest / p.Hkv;
-#else
-        const int chunk = rest % p.n_chunks;
-        u.kv_head = rest / p.n_chunks;
-#endif
         u.kv_z = 0;
         u.kv_lo = p.chunk_start[chunk] * kTileN;
         u.kv_hi = min(p.S_prefix, p.chunk_start[chunk + 1] * kTileN);

@@ -1,5 +1,10 @@
-"""Plant one mistake at a time in the oracle (a CPU rebuild of its C source) and
-check that the pins catch every one of them."""
+"""Plant one mistake at a time in the oracle and check that the pins catch
+every one of them.
+
+The oracle's C source carries no planted mistakes: each mutant here is a text
+patch (a line of the definition and its wrong replacement) applied to a
+temporary copy of ``oracle/attn_oracle.c``, which is then compiled on the CPU
+and swapped in for the duration of the pins."""
 import os
 
 import numpy as np
@@ -25,24 +30,68 @@ PINS = [
     lambda: bwd_pins.test_bwd_matches_torch_float64_autograd(True, 6, 2),
 ]
 
+# description -> (text of the oracle, its wrong replacement); each text occurs
+# exactly once in the source.
 MUTANTS = {
-    1: "softmax scale 1/d instead of 1/sqrt(d)",
-    2: "causal mask drops the diagonal",
-    3: "lse in log2 instead of ln",
-    4: "interleaved GQA head map",
-    5: "scores against V instead of K",
-    6: "last visible key dropped",
-    7: "merge forgets to normalise",
-    8: "causal mask on the stored order instead of sequence positions",
-    9: "backward: softmax Jacobian's row term dropped",
-    10: "backward: dK without the softmax scale",
-    11: "fan-out prefill: a row does not see its own suffix token",
+    1: ("softmax scale 1/d instead of 1/sqrt(d)",
+        "(int64_t)B * S * Hq;\n    const int group = Hq / Hkv;\n    const double scale = 1.0 / sqrt((double)D);",
+        "(int64_t)B * S * Hq;\n    const int group = Hq / Hkv;\n    const double scale = 1.0 / (double)D;"),
+    2: ("causal mask drops the diagonal",
+        "if (causal && i + 1 < hi) hi = i + 1;",
+        "if (causal && i < hi) hi = i;\n            if (hi < kv_begin) hi = kv_begin;"),
+    3: ("lse in log2 instead of ln",
+        "return m + log(l);",
+        "return m + log2(l);"),
+    4: ("interleaved GQA head map",
+        "const int hk = h / group;\n            for (int d = 0; d < D; ++d) q_row[d] = load_elem(q, dtype",
+        "const int hk = h % Hkv;\n            for (int d = 0; d < D; ++d) q_row[d] = load_elem(q, dtype"),
+    5: ("scores against V instead of K",
+        "acc += q_row[d] * load_elem(keys[j].k, dtype, keys[j].off + d);\n        s[j] = acc * scale;",
+        "acc += q_row[d] * load_elem(keys[j].v, dtype, keys[j].off + d);\n        s[j] = acc * scale;"),
+    6: ("last visible key dropped",
+        "if (n == 0) return -INFINITY;\n",
+        "if (n == 0) return -INFINITY;\n    if (n > 1) --n;\n"),
+    7: ("merge forgets to normalise",
+        "for (int d = 0; d < D; ++d) o[d] /= wsum;",
+        ""),
+    8: ("causal mask on the stored order instead of sequence positions",
+        "if (pos && causal && pos[j] > pos[i]) continue;",
+        "if (pos && causal && j > i) continue;"),
+    9: ("backward: softmax Jacobian's row term dropped",
+        "dS[j] = P[j] * (dS[j] - delta);",
+        "dS[j] = P[j] * dS[j];"),
+    10: ("backward: dK without the softmax scale",
+         "dk[koff + d] += scale * dS[jj] * q_row[d];",
+         "dk[koff + d] += dS[jj] * q_row[d];"),
+    11: ("fan-out prefill: a row does not see its own suffix token",
+         "+ (r - off[b]) : Ss - 1;",
+         "+ (r - off[b]) - 1 : Ss - 1;"),
 }
+
+
+def mutant_source(mutant):
+    """The oracle's source with mutant ``mutant``'s text patch applied."""
+    src = open(oracle.SOURCE).read()
+    _, good, bad = MUTANTS[mutant]
+    assert src.count(good) == 1, f"mutant {mutant}: its text must occur exactly once in the oracle"
+    return src.replace(good, bad)
+
+
+def test_oracle_source_carries_no_planted_mistake():
+    """Every mutant's correct text is in the oracle, none of the wrong ones."""
+    src = open(oracle.SOURCE).read()
+    for n, (what, good, bad) in MUTANTS.items():
+        assert src.count(good) == 1, what
+        if bad:
+            assert bad not in src, what
 
 
 @pytest.mark.parametrize("mutant", sorted(MUTANTS))
 def test_pins_catch_planted_mistake(mutant, tmp_path):
-    path = oracle.build(mutant=mutant, out=os.path.join(tmp_path, f"liboracle_m{mutant}.so"))
+    src = os.path.join(tmp_path, f"attn_oracle_m{mutant}.c")
+    with open(src, "w") as f:
+        f.write(mutant_source(mutant))
+    path = oracle.build(src=src, out=os.path.join(tmp_path, f"liboracle_m{mutant}.so"))
     caught = []
     oracle.use_library(path)
     try:
@@ -53,7 +102,7 @@ def test_pins_catch_planted_mistake(mutant, tmp_path):
                 caught.append(pin)
     finally:
         oracle.use_library(None)
-    assert caught, f"no pin caught mutant {mutant}: {MUTANTS[mutant]}"
+    assert caught, f"no pin caught mutant {mutant}: {MUTANTS[mutant][0]}"
 
 
 # The paged fan-out oracle gathers the pages in Python before the C oracle runs,
