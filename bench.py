@@ -1,6 +1,6 @@
 """Benchmark of the blockwise ring-attention hot path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--all]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One JSON line on rank 0.  The headline step is one ra_blockwise_attn_fwd call
 on the causal GQA prefill workload (B=1, S=32768, Hq=32, Hkv=8, D=128, bf16,
@@ -11,8 +11,8 @@ The same line carries the other rows measured on their own workloads: the
 headline workload in the zigzag and striped shard layouts, its backward pass
 (contiguous and zigzag), shared-prefix fan-out decode (HBM GB/s; contiguous and
 over a paged KV pool), fan-out prefill (8 branches x 20 rows), per-shard
-partials + LSE merge on the Llama-3-70B-shaped layer, and (with --all) the
-million-token stress case.
+partials + LSE merge on the Llama-3-70B-shaped layer, and the million-token
+stress case.
 
 Under torchrun (--gpus N > 1) every rank runs an independent replica of the
 same workload (the path needs no exchange between GPUs); the barrier and the
@@ -104,6 +104,41 @@ def max_over_ranks(x: float, world: int, device) -> float:
 def job_throughput(units_per_step: float, steps: int, total_ms: float, world: int) -> float:
     """Whole-job rate: the units all ranks processed over the slowest rank's time (x 1e-12, per s)."""
     return world * units_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
+def gpu_local_cpus(device_index: int):
+    """Host CPUs on the GPU's own NUMA node (from sysfs), or None if unknown.
+
+    Pinned host buffers are placed on the node of the CPU that first touches
+    them; allocating them from these CPUs keeps host<->device copies off the
+    link between host sockets."""
+    try:
+        bus = subprocess.run(["nvidia-smi", "-i", str(device_index), "--query-gpu=pci.bus_id",
+                              "--format=csv,noheader"], capture_output=True, text=True, timeout=20).stdout.strip()
+        dom, rest = bus.split(":", 1)
+        path = f"/sys/bus/pci/devices/{(dom[-4:] + ':' + rest).lower()}"
+        cpus = set()
+        for part in open(os.path.join(path, "local_cpulist")).read().strip().split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        node = int(open(os.path.join(path, "numa_node")).read().strip())
+        return (cpus or None), node
+    except Exception:
+        return None, None
+
+
+def pinned_on_gpu_node(device_index: int, make):
+    """Runs make() (which allocates and fills pinned host tensors) on the GPU's
+    NUMA-local CPUs, then restores the thread's CPU affinity."""
+    cpus, node = gpu_local_cpus(device_index)
+    old = os.sched_getaffinity(0)
+    if cpus:
+        os.sched_setaffinity(0, cpus)
+    try:
+        return make(), node, len(cpus) if cpus else None
+    finally:
+        os.sched_setaffinity(0, old)
 
 
 def peaks():
@@ -308,13 +343,25 @@ def run_ours(args, rank, world):
         # host memory and reads its O and lse back; steps are pipelined over three streams (the
         # next step's inputs in, this step's kernel, the previous step's results out) with two
         # device buffer sets, as a serving loop would.  Timed from the first copy to the last read.
-        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        dev_index = torch.cuda.current_device()
+
+        def host_buffers():
+            hin = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q, k, v)]
+            for h, t in zip(hin, (q, k, v)):
+                h.copy_(t)                                      # first touch on the GPU's node
+            hout = [dict(oh=torch.empty(out.shape, dtype=out.dtype, pin_memory=True),
+                         lh=torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)) for _ in range(2)]
+            for ho in hout:
+                ho["oh"].zero_()
+                ho["lh"].zero_()
+            return hin, hout
+
+        (hin, hout), numa_node, numa_cpus = pinned_on_gpu_node(dev_index, host_buffers)
+        qh, kh, vh = hin
         slots = []
-        for _ in range(2):
+        for i in range(2):
             slots.append(dict(q=torch.empty_like(q), k=torch.empty_like(k), v=torch.empty_like(v),
-                              o=torch.empty_like(out), l=torch.empty_like(lse),
-                              oh=torch.empty(out.shape, dtype=out.dtype, pin_memory=True),
-                              lh=torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True),
+                              o=torch.empty_like(out), l=torch.empty_like(lse), oh=hout[i]["oh"], lh=hout[i]["lh"],
                               in_done=torch.cuda.Event(), run_done=torch.cuda.Event(), out_done=torch.cuda.Event()))
         s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
@@ -340,8 +387,27 @@ def run_ours(args, rank, world):
                     sl["lh"].copy_(sl["l"], non_blocking=True)
                     sl["out_done"].record(s_out)
 
-        n_e2e = max(3, min(args.steps, 10))
-        e2e_steps(2)                                           # warm-up
+        h2d_bytes = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+        d2h_bytes = slots[0]["oh"].numel() * slots[0]["oh"].element_size() + \
+            slots[0]["lh"].numel() * slots[0]["lh"].element_size()
+
+        def leg_gbs(copy, nbytes, reps=5):
+            """One copy leg alone (host wall clock over reps copies): its own bandwidth."""
+            copy()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                copy()
+            torch.cuda.synchronize()
+            return nbytes * reps / (time.perf_counter() - t0) / 1e9
+
+        sl0 = slots[0]
+        h2d_gbs = leg_gbs(lambda: [d.copy_(h, non_blocking=True) for d, h in ((sl0["q"], qh), (sl0["k"], kh),
+                                                                              (sl0["v"], vh))], h2d_bytes)
+        d2h_gbs = leg_gbs(lambda: [h.copy_(d, non_blocking=True) for h, d in ((sl0["oh"], sl0["o"]),
+                                                                              (sl0["lh"], sl0["l"]))], d2h_bytes)
+        n_e2e = max(30, args.steps)
+        e2e_steps(3)                                           # warm-up
         torch.cuda.synchronize()
         flush()
         torch.cuda.synchronize()
@@ -351,13 +417,16 @@ def run_ours(args, rank, world):
         e2e_total_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, "cuda")
         ra.device_status()
         assert torch.equal(slots[0]["oh"], slots[1]["oh"])    # every step read back the same result
+        e2e_ms = e2e_total_ms / n_e2e
+        copy_ms = max(h2d_bytes / (h2d_gbs * 1e9), d2h_bytes / (d2h_gbs * 1e9)) * 1e3
         e2e = {"value": job_throughput(flops, n_e2e, e2e_total_ms, world), "unit": "TFLOP/s",
-               "ms_per_step": e2e_total_ms / n_e2e, "steps": n_e2e,
+               "ms_per_step": e2e_ms, "steps": n_e2e,
                "pipelining": "3 streams (h2d, kernel, d2h), 2 device buffer sets; wall clock over all steps",
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (qh, kh, vh)),
-               "d2h_bytes_per_step": slots[0]["oh"].numel() * slots[0]["oh"].element_size() +
-                                     slots[0]["lh"].numel() * slots[0]["lh"].element_size()}
-        del qh, kh, vh, slots
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+               "h2d_GB_per_s_alone": h2d_gbs, "d2h_GB_per_s_alone": d2h_gbs,
+               "bound": "copies" if copy_ms > ms_step else "kernel",
+               "host_numa_node": numa_node, "pinned_alloc_cpus": numa_cpus}
+        del qh, kh, vh, slots, hin, hout
 
         # fan-out decode (config 4) and its R=16 sub-case
         for name in ("fanout_decode", "fanout_decode1"):
@@ -492,17 +561,21 @@ def run_ours(args, rank, world):
                                                    (statistics.median(tms) * 1e-3) / 1e12}
         del tq, tk, tv
 
-        if args.all:
-            sw = WORKLOADS["million_token_stress"]
-            sq, sk, sv = attention_inputs(sw, "cuda")
-            so = torch.empty_like(sq)
-            sl = torch.empty(sw.B, sw.Hq, sw.S, device="cuda", dtype=torch.float32)
-            sms = timed_steps(lambda: ra.attn(sq, sk, sv, sw.n_shards, sw.block, True, out=so, lse=sl), 1, 1)
-            ra.device_status()
-            sf = ring_flops(sw.B, sw.S, sw.Hq, sw.D, True)
-            result["million_token_stress"] = {"s": sms[0] / 1e3, "TFLOP_per_s": sf / (sms[0] * 1e-3) / 1e12,
-                                              "frac_bf16_peak": sf / (sms[0] * 1e-3) / 1e12 / pk["bf16_tflops"]}
-            del sq, sk, sv, so, sl
+        # the million-token stress workload (1% of keys x8): one untimed call, then two timed ones
+        sw = WORKLOADS["million_token_stress"]
+        sq, sk, sv = attention_inputs(sw, "cuda")
+        so = torch.empty_like(sq)
+        sl = torch.empty(sw.B, sw.Hq, sw.S, device="cuda", dtype=torch.float32)
+        sms = timed_steps(lambda: ra.attn(sq, sk, sv, sw.n_shards, sw.block, True, out=so, lse=sl), 2, 1)
+        ra.device_status()
+        sf = ring_flops(sw.B, sw.S, sw.Hq, sw.D, True)
+        ts = statistics.mean(sms) * 1e-3
+        result["million_token_stress"] = {"s": ts, "s_per_call": sms, "TFLOP_per_s": sf / ts / 1e12,
+                                          "frac_bf16_peak": sf / ts / 1e12 / pk["bf16_tflops"],
+                                          "frac_of_sustained": sf / ts / 1e12 / pk["bf16_tflops_sustained"],
+                                          "flops": sf, "S": sw.S, "n_shards": sw.n_shards}
+        del sq, sk, sv, so, sl
+        torch.cuda.empty_cache()
 
     clocks = clk.summary()
     achieved = flops / (ms_step * 1e-3) / 1e12
@@ -686,7 +759,6 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--all", action="store_true", help="also time the million-token stress workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", choices=PROFILE_CASES,
                     help="run three calls of one kernel family on a small case (for ncu captures) and exit")

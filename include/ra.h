@@ -314,7 +314,9 @@ size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int 
  *
  * The first call on a device (with that device current) looks up the array's
  * device address with cudaGetSymbolAddress; make that first call before any
- * stream capture.  Every call, on every stream, shares the one array, and it
+ * stream capture.  The address is kept per device and context: after a device
+ * reset (cudaDeviceReset) the next call looks it up again in the new context,
+ * so that call, too, belongs before any capture.  Every call, on every stream, shares the one array, and it
  * keeps the previous call's contents (nothing in it needs to start at zero):
  * calls that can overlap on the GPU race on it, so serialise them, e.g. on
  * one stream.

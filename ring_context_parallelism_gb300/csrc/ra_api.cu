@@ -1,6 +1,8 @@
 // ra_api.cu -- the C ABI declared in include/ra.h: host-side validation,
 // output layout descriptors, dispatch to the kernels, device status.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdarg>
 #include <cstdint>
@@ -172,23 +174,55 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+    unsigned long long ctx_id;  // context the address belongs to (0: not looked up)
+    void* addr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_fanout_scratch on the current device, looked up once per
-// device (host code only sees a stand-in for the array's name).
+// Unique id of the calling thread's current context (0 if it cannot be read).
+// A device reset gives the device a new primary context, where the module and
+// its scratch array are loaded again, possibly at another address.
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_fanout_scratch on the current device (host code only
+// sees a stand-in for the array's name).  Looked up once per device and
+// context: again after a device reset has replaced the context.
 ra_status scratch_address(void** addr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(RA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    const unsigned long long ctx = current_context_id();  // 0 before the device's first runtime call
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddr& c = g_scratch_addr[dev];
+    if (!c.addr || ctx == 0 || c.ctx_id != ctx) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_fanout_scratch);
+        e = cudaGetSymbolAddress(&p, g_fanout_scratch);  // sets up the device's context if needed
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fan-out scratch)");
-        g_scratch_addr[dev] = p;
+        c.addr = p;
+        c.ctx_id = current_context_id();
     }
-    *addr = g_scratch_addr[dev];
+    *addr = c.addr;
     return RA_OK;
 }
 
@@ -269,24 +303,15 @@ struct PagedKv {
     const int* suffix_pages = nullptr;
 };
 
-static ra_status fanout_common(const void* q_rows, const int* branch_offsets, int n_branches, int R,
-                               const void* k_prefix, const void* v_prefix, int S_prefix, const void* k_suffix,
-                               const void* v_suffix, int S_suffix, void* out, float* lse, int Hq, int Hkv, int D,
-                               ra_dtype dt, void* workspace, size_t workspace_bytes, void* stream,
-                               int suffix_causal, const PagedKv& pg = PagedKv()) {
-    ra_status st = check_fanout(q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix, k_suffix,
-                                v_suffix, S_suffix, out, Hq, Hkv, D, dt);
-    if (st != RA_OK) return st;
-    if (lse && !aligned16(lse)) return fail(RA_ERR_INVALID_ARG, "lse must be 16-byte aligned");
-    if (R == 0) return ok();
-    const FanoutPlan f = plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D);
-    if (!workspace || workspace_bytes < f.total)
-        return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", f.total, workspace_bytes);
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
-        return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    float* part_o = static_cast<float*>(workspace);
-    float* part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + f.part_o_bytes);
-
+// Launches a fan-out call on a checked plan: the attention kernel writes the
+// plan's chunk partials to part_o / part_lse (laid out as finish_plan sizes
+// them), the merge joins them into out / lse.  Both the workspace entry points
+// and the no-allocation one go through here.
+static ra_status launch_fanout(const FanoutPlan& f, float* part_o, float* part_lse, const void* q_rows,
+                               const int* branch_offsets, int n_branches, int R, const void* k_prefix,
+                               const void* v_prefix, int S_prefix, const void* k_suffix, const void* v_suffix,
+                               int S_suffix, void* out, float* lse, int Hq, int Hkv, int D, void* stream,
+                               int suffix_causal, const PagedKv& pg) {
     ra::FanoutTcArgs a{};
     a.q_rows = q_rows;
     a.offsets = branch_offsets;
@@ -329,6 +354,27 @@ static ra_status fanout_common(const void* q_rows, const int* branch_offsets, in
     e = ra::launch_lse_merge(m, s);
     if (e != cudaSuccess) return cuda_fail(e, "fan-out merge launch");
     return ok();
+}
+
+static ra_status fanout_common(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                               const void* k_prefix, const void* v_prefix, int S_prefix, const void* k_suffix,
+                               const void* v_suffix, int S_suffix, void* out, float* lse, int Hq, int Hkv, int D,
+                               ra_dtype dt, void* workspace, size_t workspace_bytes, void* stream,
+                               int suffix_causal, const PagedKv& pg = PagedKv()) {
+    ra_status st = check_fanout(q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix, k_suffix,
+                                v_suffix, S_suffix, out, Hq, Hkv, D, dt);
+    if (st != RA_OK) return st;
+    if (lse && !aligned16(lse)) return fail(RA_ERR_INVALID_ARG, "lse must be 16-byte aligned");
+    if (R == 0) return ok();
+    const FanoutPlan f = plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D);
+    if (!workspace || workspace_bytes < f.total)
+        return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", f.total, workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(RA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    float* part_o = static_cast<float*>(workspace);
+    float* part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + f.part_o_bytes);
+    return launch_fanout(f, part_o, part_lse, q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix,
+                         k_suffix, v_suffix, S_suffix, out, lse, Hq, Hkv, D, stream, suffix_causal, pg);
 }
 
 ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, int n_branches, int R,
@@ -392,38 +438,8 @@ ra_status ra_prefix_fanout_attn_noalloc(const void* q_rows, const int* branch_of
     if (st != RA_OK) return st;
     float* part_o = static_cast<float*>(scratch);
     float* part_lse = reinterpret_cast<float*>(static_cast<char*>(scratch) + f.part_o_bytes);
-
-    ra::FanoutTcArgs a{};
-    a.q_rows = q_rows;
-    a.offsets = branch_offsets;
-    a.n_branches = n_branches;
-    a.R = R;
-    a.k_prefix = k_prefix;
-    a.v_prefix = v_prefix;
-    a.S_prefix = S_prefix;
-    a.k_suffix = k_suffix;
-    a.v_suffix = v_suffix;
-    a.S_suffix = S_suffix;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.D = D;
-    a.n_chunks = f.n_chunks;
-    for (int c = 0; c <= f.n_chunks; ++c) a.chunk_start[c] = f.chunk_start[c];
-    a.part.o = part_o;
-    a.part.lse = part_lse;
-    a.part.o_row = static_cast<long long>(Hq) * D;
-    a.part.o_h = D;
-    a.part.o_part = static_cast<long long>(R) * Hq * D;
-    a.part.lse_h = R;
-    a.part.lse_part = static_cast<long long>(Hq) * R;
-    a.part.o_f32 = 1;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = ra::launch_fanout_tc(a, s);
-    if (e != cudaSuccess) return cuda_fail(e, "fan-out attention launch");
-    ra::MergeArgs m{part_o, part_lse, out, lse, f.P, 1, R, Hq, D, 1, 0};
-    e = ra::launch_lse_merge(m, s);
-    if (e != cudaSuccess) return cuda_fail(e, "fan-out merge launch");
-    return ok();
+    return launch_fanout(f, part_o, part_lse, q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix,
+                         k_suffix, v_suffix, S_suffix, out, lse, Hq, Hkv, D, stream, 0, PagedKv());
 }
 
 int ra_ring_shard_order(int S, int n_shards, int causal, int q_row0, int* shard_order) {

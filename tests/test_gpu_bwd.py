@@ -2,11 +2,15 @@
 fp64 backward oracle on the same seeded inputs.
 
 Tolerance.  fp32 inputs: 1e-4 max abs error (the fp32 bar of the forward).
-bf16 inputs: the forward's O bar (2e-2 for outputs of magnitude <= 1) scaled to
-each gradient tensor's own magnitude: max abs error <= 2e-2 * max(1, max |ref|).
-The kernels round P and dS to bf16 before the dV, dK and dQ products (relative
-error 2^-9 per term) and round the results to bf16 (2^-9 of their magnitude),
-so the error grows with the gradient's size, not with 1."""
+bf16 inputs, two criteria per gradient tensor, both required:
+  * absolute: max abs error <= 2e-2 * max(1, max |ref|), the forward's O bar
+    scaled to the gradient's own magnitude;
+  * relative: max abs error / max |ref| <= 8e-3.  On its way to a stored
+    gradient element a product term passes two bf16 roundings: its P or dS
+    operand (rounded before the dV, dK, dQ products) and the stored result
+    itself, each at most 2^-8 (bf16's unit roundoff) relative, so 2 * 2^-8 of
+    the tensor's largest magnitude bounds the error a correct kernel makes.
+The error therefore grows with the gradient's size, not with 1."""
 import numpy as np
 import pytest
 import torch
@@ -28,8 +32,14 @@ def _lib():
     ra.load()
 
 
+BF16_REL = 8e-3  # 2 x 2^-8: two bf16 roundings on the way to a stored gradient element
+
+
 def _tol(ref, dtype):
-    return 1e-4 if dtype == "f32" else 2e-2 * max(1.0, float(np.abs(ref).max()))
+    if dtype == "f32":
+        return 1e-4
+    big = float(np.abs(ref).max()) if ref.size else 0.0
+    return min(2e-2 * max(1.0, big), BF16_REL * big) if big > 0 else 2e-2
 
 
 def _close(got, ref, dtype, what):
@@ -37,7 +47,7 @@ def _close(got, ref, dtype, what):
     err = float(np.abs(got - ref).max()) if ref.size else 0.0
     tol = _tol(ref, dtype)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
-    assert err <= tol, f"{what}: max abs err {err:.3e} > {tol:.2e}"
+    assert err <= tol, f"{what}: max abs err {err:.3e} > {tol:.2e} (max |ref| {float(np.abs(ref).max()):.3g})"
     return err
 
 
