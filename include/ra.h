@@ -342,7 +342,11 @@ int ra_ring_shard_order(int S, int n_shards, int causal, int q_row0, int* shard_
  * and returns n_chunks (<= 64), or -1 on invalid arguments.  chunk_start
  * holds 65 ints.  The split is chosen by simulating the block scheduler over
  * the launch's units (prefix chunk x KV head x row pair) and minimising the
- * makespan; it may make chunks unequal.
+ * makespan; it may make chunks unequal.  Calls whose stacked rows fit one
+ * 128-row tile per KV head are bound by HBM bandwidth: their units take at
+ * most 4/5 of the SMs (fewer chunks, fewer partials to merge).  This is the
+ * split of the contiguous entry points; ra_prefix_fanout_attn_paged spreads
+ * such units over every SM.
  */
 int ra_prefix_fanout_plan(int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv, int n_sm,
                           int* chunk_start);

@@ -430,8 +430,19 @@ __device__ __forceinline__ void reg_inc() {
 // their KV tiles over the two tile slots (one row tile), all pair two row
 // tiles, or mix both (suffix units without a prefix).  The uniform fan-out
 // variants compile only their own issue and softmax paths.
-// kModeRingLayout: a causal ring walk over zigzag or striped shards.
-enum KernelMode : int { kModeRing = 0, kModeFanMixed = 1, kModeFanSplit = 2, kModeFanPaired = 3, kModeRingLayout = 4 };
+// kModeRingLayout: a causal ring walk over zigzag or striped shards.  The
+// fan-out modes over a paged KV pool (kModeFan*Paged) are the same three
+// fan-out variants with the producers' page-table path compiled in.
+enum KernelMode : int {
+    kModeRing = 0,
+    kModeFanMixed = 1,
+    kModeFanSplit = 2,
+    kModeFanPaired = 3,
+    kModeRingLayout = 4,
+    kModeFanMixedPaged = 5,
+    kModeFanSplitPaged = 6,
+    kModeFanPairedPaged = 7
+};
 
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -442,9 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool RING = MODE == kModeRing || MODE == kModeRingLayout;
     constexpr bool FAN = !RING;
     constexpr bool LAY = MODE == kModeRingLayout;
+    constexpr bool PG = MODE >= kModeFanMixedPaged;              // paged KV pool
+    constexpr int FMODE = PG ? MODE - kModeFanMixedPaged + kModeFanMixed : MODE;  // its unpaged fan-out mode
     const Unit u = decode_unit<FAN, LAY>(p);
     if (!u.valid) return;
-    const bool split = MODE == kModeFanSplit ? true : (RING || MODE == kModeFanPaired) ? false : u.split != 0;
+    const bool split = FMODE == kModeFanSplit ? true : (RING || FMODE == kModeFanPaired) ? false : u.split != 0;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -520,9 +533,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ producers
         // Lane 0 of warp 0 loads Q and streams the K ring, lane 0 of warp 2 the
         // V ring: one issuing thread alone cannot keep both rings filled at the
-        // rate the MMAs (or HBM, for the fan-out) consume them.
+        // rate the MMAs (or HBM, for the fan-out) consume them.  A paged fan-out
+        // tile arrives in one small box per page and column chunk (16 for
+        // 16-token pages), and the TMA unit takes small boxes slowly from a
+        // single issuing thread: there every lane of the warp walks the tiles,
+        // lane 0 sets the stage's expected bytes and each lane issues one box.
         reg_dec<FAN>();
-        if (lane == 0) {
+        constexpr bool warp_issue = PG;
+        if (lane == 0 || warp_issue) {
+            const bool lead = lane == 0;
             const bool is_k = (warp == 0);
             uint64_t* full = is_k ? k_full : v_full;
             uint64_t* empty = is_k ? k_empty : v_empty;
@@ -530,9 +549,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n_stages = is_k ? nK : nV;
             const CUtensorMap* map1 = is_k ? &tm_k : &tm_v;
             const CUtensorMap* map2 = is_k ? &tm_k2 : &tm_v2;
-            tma_prefetch_desc(map1);
-            if (FAN) tma_prefetch_desc(map2);
-            if (is_k) {
+            if (lead) {
+                tma_prefetch_desc(map1);
+                if (FAN) tma_prefetch_desc(map2);
+            }
+            if (is_k && lead) {
                 tma_prefetch_desc(&tm_q);
                 mbar_arrive_expect_tx(q_full, u.n_q * C::kTileBytes);
                 for (int t = 0; t < u.n_q; ++t)
@@ -559,9 +580,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int j = is_k ? i - n_stages : i - n_stages + 1;
                     ok = mbar_wait(&iter_done[j % C::kIterRing], (j / C::kIterRing) & 1, abort_flag, status, where);
                 }
+                if (warp_issue) ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                mbar_arrive_expect_tx(&full[cs.s], C::kTileBytes);
-                if (FAN && p.paged) {
+                if (lead) mbar_arrive_expect_tx(&full[cs.s], C::kTileBytes);
+                if (PG) {
+                    __syncwarp();  // the expected bytes are set before any box of the stage can land
                     // one box per page (or per 128 rows of a larger page); a 128B-swizzled
                     // tile is the same bytes whether it lands in one box or several
                     // (every sub-box starts on a 1024-byte swizzle atom).  Pages past
@@ -572,7 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int n_listed = from_suffix ? p.n_suffix_pages : p.n_prefix_pages;
                     const int page_size = 1 << p.page_shift;
                     const int sub_rows = page_size < kTileN ? page_size : kTileN;
-                    for (int r0 = 0; r0 < kTileN; r0 += sub_rows) {
+                    const int n_boxes = (kTileN / sub_rows) * C::kChunks;  // at most 16 x 2 (8-token pages)
+                    for (int b = lane; b < n_boxes; b += 32) {
+                        const int r0 = (b / C::kChunks) * sub_rows;
+                        const int c = b % C::kChunks;
                         const int lk = wi.key() + r0;
                         const int lp = lk >> p.page_shift;
                         int row = p.n_pages << p.page_shift;
@@ -585,9 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 atomicCAS(&g_tc_status[1], 0u, 0x0E000000u | static_cast<unsigned>(lp & 0xFFFFFF));
                             }
                         }
-                        for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_4d(map, &full[cs.s], ring + cs.s * C::kTileBytes + c * 16384 + r0 * 128, c * 64,
-                                        u.kv_head, row, 0);
+                        tma_load_4d(map, &full[cs.s], ring + cs.s * C::kTileBytes + c * 16384 + r0 * 128, c * 64,
+                                    u.kv_head, row, 0);
                     }
                 } else {
                     for (int c = 0; c < C::kChunks; ++c)
@@ -597,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cs.next(n_stages);
                 ++issued;
             }
-            if (*abort_flag) {
+            if (lead && *abort_flag) {
                 // let copies already in flight land before the CTA exits: the
                 // last n_stages loads of this ring (and Q)
                 StageCtr ls;
@@ -1277,6 +1302,16 @@ cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
     const int n_suffix_units = (a.S_suffix > 0 && !p.fold) ? a.n_branches * a.Hkv * p.suffix_mpairs : 0;
     const int grid = p.n_prefix_units + n_suffix_units;
     // uniform launches (prefix units only) get the variant compiled for their mode
+    if (a.paged) {
+        if (n_suffix_units == 0 && p.split_prefix)
+            return a.D == 128 ? launch<128, kModeFanSplitPaged>(p, grid, tq, tk, tv, tk2, tv2, stream)
+                              : launch<64, kModeFanSplitPaged>(p, grid, tq, tk, tv, tk2, tv2, stream);
+        if (n_suffix_units == 0)
+            return a.D == 128 ? launch<128, kModeFanPairedPaged>(p, grid, tq, tk, tv, tk2, tv2, stream)
+                              : launch<64, kModeFanPairedPaged>(p, grid, tq, tk, tv, tk2, tv2, stream);
+        return a.D == 128 ? launch<128, kModeFanMixedPaged>(p, grid, tq, tk, tv, tk2, tv2, stream)
+                          : launch<64, kModeFanMixedPaged>(p, grid, tq, tk, tv, tk2, tv2, stream);
+    }
     if (n_suffix_units == 0 && p.split_prefix)
         return a.D == 128 ? launch<128, kModeFanSplit>(p, grid, tq, tk, tv, tk2, tv2, stream)
                           : launch<64, kModeFanSplit>(p, grid, tq, tk, tv, tk2, tv2, stream);

@@ -14,6 +14,17 @@
 // equal chunks it tries shaped splits (one longer chunk, one shorter), which
 // let a launch whose unit count is not a multiple of the SM count finish its
 // second wave together with the first.  Plans are cached per shape.
+//
+// Units that hold a single row tile (all stacked rows of a KV head in one
+// 128-row tile: few rows, a decode) are bound by HBM bandwidth, not by their
+// SM: the prefix bytes leave HBM at the same rate whether 112 or 152 CTAs
+// read them, while every extra chunk adds a partial to write and merge and a
+// unit's fixed cost.  Their chunk count is capped so that the units take at
+// most 4/5 of the SMs (measured on GB300, 65536-token prefix, 8 KV heads,
+// 16 rows: 14-15 chunks 59.9 us, 16 chunks 61.9 us, 19 chunks 64.0 us, the
+// launch and its merge).  Not over a paged KV cache: small pages arrive in
+// small TMA boxes, which bound each SM's read rate, so a paged launch wants
+// every SM (16-token pages: 74 us with 19 chunks, 88 us with 15).
 #include <algorithm>
 #include <cmath>
 #include <functional>
@@ -37,7 +48,15 @@ struct Shape {
     int n_tiles;       // prefix KV tiles
     double s_tiles;    // suffix tiles of one branch
     int n_branches, n_mpairs, Hkv, n_sm;
+    bool one_tile;     // the stacked rows fit one row tile (bandwidth-bound units)
 };
+
+// Largest chunk count the plan may use.
+int max_chunks(const Shape& sh) {
+    int c = std::min(sh.n_tiles, kMaxPlanChunks);
+    if (sh.one_tile) c = std::min(c, std::max(1, 4 * sh.n_sm / (5 * sh.Hkv * sh.n_mpairs)));
+    return c;
+}
 
 // Folded suffix tiles an average unit of chunk c carries.
 double folded(const Shape& sh, int n_chunks, int c) {
@@ -100,7 +119,7 @@ struct Plan {
 
 Plan search(const Shape& sh) {
     Plan best;
-    const int max_c = std::min(sh.n_tiles, kMaxPlanChunks);
+    const int max_c = max_chunks(sh);
     const long long per_chunk = static_cast<long long>(sh.Hkv) * sh.n_mpairs;
     auto consider = [&](const std::vector<int>& tiles, double penalty) {
         const double cost = simulate(sh, tiles) + penalty + 1e-3 * tiles.size();  // ties: fewer partials
@@ -158,7 +177,7 @@ int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_prefix, int S_suffi
 }
 
 void fanout_plan(int R, int S_prefix, int S_suffix, int n_branches, int Hq, int Hkv, int n_sm, int* n_chunks,
-                 int* chunk_start) {
+                 int* chunk_start, bool paged) {
     const int rows_per_tile = kTileRows / (Hq / Hkv);
     Shape sh;
     sh.n_mpairs = (R + 2 * rows_per_tile - 1) / (2 * rows_per_tile);
@@ -167,12 +186,14 @@ void fanout_plan(int R, int S_prefix, int S_suffix, int n_branches, int Hq, int 
     sh.n_branches = n_branches;
     sh.Hkv = Hkv;
     sh.n_sm = n_sm > 0 ? n_sm : 1;
+    sh.one_tile = R <= rows_per_tile && !paged;
     if (sh.n_tiles == 0 || sh.n_mpairs == 0) {
         *n_chunks = 0;
         if (chunk_start) chunk_start[0] = 0;
         return;
     }
-    const auto key = std::make_tuple(sh.n_mpairs, sh.n_tiles, static_cast<int>(sh.s_tiles), n_branches, Hkv, sh.n_sm);
+    const auto key = std::make_tuple(sh.n_mpairs, sh.n_tiles, static_cast<int>(sh.s_tiles), n_branches, Hkv,
+                                     sh.n_sm * 2 + (sh.one_tile ? 1 : 0));
     std::vector<int> tiles;
     {
         std::lock_guard<std::mutex> lock(g_plan_mu);
@@ -202,6 +223,7 @@ void fanout_split_equal(int n_chunks, int R, int S_prefix, int S_suffix, int n_b
     sh.n_branches = n_branches;
     sh.Hkv = Hkv;
     sh.n_sm = 1;
+    sh.one_tile = R <= rows_per_tile;
     const std::vector<int> tiles = split(sh, std::vector<double>(n_chunks, 1.0));
     chunk_start[0] = 0;
     for (int c = 0; c < n_chunks; ++c) chunk_start[c + 1] = chunk_start[c] + tiles[c];

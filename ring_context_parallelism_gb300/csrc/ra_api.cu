@@ -136,10 +136,12 @@ FanoutPlan plan_with_chunks(int n_chunks, int R, int n_branches, int S_prefix, i
 }
 
 // The planned split (chunk count and boundaries from the scheduler simulation).
-FanoutPlan plan_fanout(int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv, int D) {
+FanoutPlan plan_fanout(int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv, int D,
+                       bool paged = false) {
     FanoutPlan f{};
     f.n_chunks = 0;
-    if (S_prefix > 0) ra::fanout_plan(R, S_prefix, S_suffix, n_branches, Hq, Hkv, sm_count(), &f.n_chunks, f.chunk_start);
+    if (S_prefix > 0)
+        ra::fanout_plan(R, S_prefix, S_suffix, n_branches, Hq, Hkv, sm_count(), &f.n_chunks, f.chunk_start, paged);
     return finish_plan(f, R, S_prefix, S_suffix, Hq, Hkv, D);
 }
 
@@ -293,7 +295,10 @@ size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int 
     if (R < 0 || n_branches < 1 || S_prefix < 0 || S_suffix < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
         (D != 64 && D != 128) || dt != RA_BF16 || 128 % (Hq / Hkv) || S_prefix + S_suffix < 1)
         return 0;
-    return plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D).total;
+    // one size for the contiguous and the paged entry points (their splits may differ)
+    const size_t a = plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D, false).total;
+    const size_t b = plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D, true).total;
+    return a > b ? a : b;
 }
 
 // Paged KV of a fan-out call (all zero: contiguous prefix / suffix tensors).
@@ -366,7 +371,7 @@ static ra_status fanout_common(const void* q_rows, const int* branch_offsets, in
     if (st != RA_OK) return st;
     if (lse && !aligned16(lse)) return fail(RA_ERR_INVALID_ARG, "lse must be 16-byte aligned");
     if (R == 0) return ok();
-    const FanoutPlan f = plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D);
+    const FanoutPlan f = plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D, pg.paged != 0);
     if (!workspace || workspace_bytes < f.total)
         return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", f.total, workspace_bytes);
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)

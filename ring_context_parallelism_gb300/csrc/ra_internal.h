@@ -60,9 +60,10 @@ int fanout_slots(int R, int Hq, int Hkv, int n_chunks, int S_prefix, int S_suffi
 
 // Prefix split of a fan-out call (fanout_plan.cu): the chunk count (at most
 // 64) and the n_chunks + 1 prefix-tile boundaries, from a simulation of the
-// block scheduler; cached per shape.
+// block scheduler; cached per shape.  `paged`: the KV comes from a page pool
+// (rows in one row tile then still spread over every SM).
 void fanout_plan(int R, int S_prefix, int S_suffix, int n_branches, int Hq, int Hkv, int n_sm, int* n_chunks,
-                 int* chunk_start);
+                 int* chunk_start, bool paged = false);
 
 // Equal-work boundaries for a given chunk count (the no-alloc entry point's
 // fallback when the planned partials do not fit its scratch).

@@ -215,9 +215,14 @@ def test_fanout_plan_is_a_valid_split_no_worse_than_equal_chunks(lib, R, nb, Sp,
         return [s_tiles * (nb // n + (c < nb % n)) / n_mpairs for c in range(n)]
 
     got = _greedy_makespan(tiles, Hkv, n_mpairs, n_sm, fold(len(tiles)))
-    # every equal split (as the planner balances it), the best of them
+    # rows in one row tile: bandwidth-bound units, spread over at most 4/5 of the SMs
+    cap = min(64, n_tiles)
+    if R <= 128 // (Hq // Hkv):
+        cap = min(cap, max(1, 4 * n_sm // (5 * Hkv * n_mpairs)))
+        assert len(tiles) <= cap and Hkv * n_mpairs * len(tiles) * 5 <= 4 * n_sm or len(tiles) == 1
+    # every equal split (as the planner balances it) the plan may take, the best of them
     best_equal = None
-    for n in range(1, min(64, n_tiles) + 1):
+    for n in range(1, cap + 1):
         q = [n_tiles // n + (c < n_tiles % n) for c in range(n)]
         span = _greedy_makespan(q, Hkv, n_mpairs, n_sm, fold(n))
         best_equal = span if best_equal is None else min(best_equal, span)
