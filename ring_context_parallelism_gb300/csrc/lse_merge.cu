@@ -16,7 +16,9 @@
 // for many rows and up to 256 partials (coalesced lse reads, weights in shared
 // memory); for fewer rows, bulk copies of up to 32 partials' rows into shared
 // memory (every byte a CTA needs in flight at once), a block per row for more
-// partials than that, and a looping warp per row otherwise.
+// partials than that, and a looping warp per row otherwise.  With heads in
+// multiples of 8 and up to 32 partials, the many-row merge takes blocks of 8
+// heads x 32 positions, whose per-position segments are contiguous.
 #include <cmath>
 
 #include "ra_device.cuh"
@@ -376,6 +378,140 @@ __global__ void __launch_bounds__(kWarps * 32) lse_merge_tiled_kernel(const void
     }
 }
 
+// Head-block variant (H % 8 == 0, P <= 32, many rows): a block owns 8
+// consecutive heads x 32 consecutive positions of one batch.  For a fixed
+// position the 8 heads' rows of a partial are one contiguous segment (8 * D
+// elements, 1 or 2 KB for bf16), so every load instruction of a warp reads 512
+// contiguous bytes, where a block of one head reads D-element rows that lie
+// H * D elements apart.  Phase 1: warp w reads lse of head h0 + w for the 32
+// positions (lane = position, coalesced) for every partial and leaves the
+// weights, the normalisers and a mask of the partials that are non-empty
+// anywhere in the block in shared memory.  Phase 2: warp w merges positions
+// w, w + 8, w + 16, w + 24; lane l holds the 16 bytes at l * 16 + j * 512 of
+// the position's segment (j < kLoads), and the non-empty partials are walked
+// a group at a time with the group's 16 loads per lane in flight.  A partial empty for a
+// whole block (a causal shard after the rows' own) is never read.
+constexpr int kHeadBlock = 8;
+constexpr int kHeadBlockMaxP = 32;
+
+template <int D, bool PART_F32, bool OUT_F32>
+__global__ void __launch_bounds__(kWarps * 32, 2) lse_merge_headblock_kernel(const void* __restrict__ part_O,
+                                                                          const float* __restrict__ part_lse,
+                                                                          void* __restrict__ out,
+                                                                          float* __restrict__ out_lse, int P,
+                                                                          int B, int S, int H) {
+    constexpr int esz = PART_F32 ? 4 : 2;
+    constexpr int kSegBytes = kHeadBlock * D * esz;      // one position's 8-head segment of a partial
+    constexpr int kLoads = kSegBytes / 512;              // 16-byte loads per lane per segment
+    constexpr int kPer = 16 / esz;                       // elements per 16-byte load
+    constexpr int kGroup = 16 / kLoads;                  // partials in flight per step (16 loads per lane)
+    static_assert(kSegBytes % 512 == 0, "segment is a whole number of warp loads");
+    __shared__ float wts[kHeadBlockMaxP][kHeadBlock][32];  // weight of partial p for (head, position)
+    __shared__ float inv_sum[kHeadBlock][32];
+    __shared__ unsigned live_mask;
+    grid_dependency_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_stiles = (S + 31) / 32;
+    const int n_htiles = H / kHeadBlock;
+    const int s_tile = blockIdx.x % n_stiles;
+    const int rest = blockIdx.x / n_stiles;
+    const int h0 = (rest % n_htiles) * kHeadBlock;
+    const long long b = rest / n_htiles;
+    const int s0 = s_tile * 32;
+    const long long rows = static_cast<long long>(B) * S * H;  // rows of one partial
+    if (threadIdx.x == 0) live_mask = 0u;
+    __syncthreads();
+
+    // phase 1: weights of head h0 + warp at positions s0 + lane
+    {
+        const int h = h0 + warp;
+        const bool in_range = s0 + lane < S;
+        const float* lp = part_lse + (b * H + h) * S + s0 + lane;
+        float L[kHeadBlockMaxP];
+        float M = -INFINITY;
+#pragma unroll
+        for (int p = 0; p < kHeadBlockMaxP; ++p) {
+            L[p] = (p < P && in_range) ? lp[p * rows] : -INFINITY;
+            M = fmaxf(M, L[p]);
+        }
+        float sum = 0.f;
+        unsigned mine = 0u;
+#pragma unroll
+        for (int p = 0; p < kHeadBlockMaxP; ++p) {
+            const float wgt = (L[p] == -INFINITY) ? 0.f : expf(L[p] - M);  // empty partial: weight 0
+            if (p < P) wts[p][warp][lane] = wgt;
+            sum += wgt;
+            if (wgt != 0.f) mine |= 1u << p;
+        }
+        inv_sum[warp][lane] = sum > 0.f ? 1.f / sum : 0.f;
+        if (out_lse && in_range) out_lse[(b * H + h) * S + s0 + lane] = sum > 0.f ? M + logf(sum) : -INFINITY;
+        mine = __reduce_or_sync(0xffffffffu, mine);
+        if (lane == 0) atomicOr(&live_mask, mine);
+    }
+    __syncthreads();
+
+    // phase 2: the non-empty partials, four at a time, for each of this warp's positions
+    const unsigned live = live_mask;
+    int hsel[kLoads], dsel[kLoads];  // head (within the block) and first dim of load j
+#pragma unroll
+    for (int j = 0; j < kLoads; ++j) {
+        const int off = (j * 512 + lane * 16) / esz;  // element offset in the segment
+        hsel[j] = off / D;
+        dsel[j] = off % D;
+    }
+    const size_t p_stride = static_cast<size_t>(rows) * D * esz;  // bytes between partials
+    for (int pos = warp; pos < 32; pos += kWarps) {
+        const int s = s0 + pos;
+        if (s >= S) break;
+        const size_t seg = ((static_cast<size_t>(b) * S + s) * H + h0) * D * esz;
+        const char* base = static_cast<const char*>(part_O) + seg + lane * 16;
+        float acc[kLoads][kPer];
+#pragma unroll
+        for (int j = 0; j < kLoads; ++j)
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) acc[j][e] = 0.f;
+        unsigned todo = live;
+        while (todo) {
+            int pp[kGroup];
+#pragma unroll
+            for (int g = 0; g < kGroup; ++g) {
+                pp[g] = todo ? __ffs(todo) - 1 : -1;
+                if (todo) todo &= todo - 1;
+            }
+            // raw 16-byte words in flight (unpacked when accumulated)
+            uint4 raw[kGroup][kLoads];
+#pragma unroll
+            for (int g = 0; g < kGroup; ++g)
+#pragma unroll
+                for (int j = 0; j < kLoads; ++j)
+                    raw[g][j] = pp[g] >= 0 ? *reinterpret_cast<const uint4*>(base + pp[g] * p_stride + j * 512)
+                                           : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int g = 0; g < kGroup; ++g) {
+                if (pp[g] < 0) continue;
+#pragma unroll
+                for (int j = 0; j < kLoads; ++j) {
+                    // a row of a non-empty partial may itself be empty: weight 0, O dropped
+                    const float w = wts[pp[g]][hsel[j]][pos];
+                    float x[kPer];
+                    load_elems<kPer, PART_F32>(&raw[g][j], x);
+#pragma unroll
+                    for (int e = 0; e < kPer; ++e) acc[j][e] = w != 0.f ? fmaf(w, x[e], acc[j][e]) : acc[j][e];
+                }
+            }
+        }
+        char* dst = static_cast<char*>(out) + ((static_cast<size_t>(b) * S + s) * H + h0) * D * (OUT_F32 ? 4 : 2);
+#pragma unroll
+        for (int j = 0; j < kLoads; ++j) {
+            const float inv = inv_sum[hsel[j]][pos];
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) acc[j][e] *= inv;
+            store_elems<kPer, OUT_F32>(dst + (static_cast<size_t>(hsel[j]) * D + dsel[j]) * (OUT_F32 ? 4 : 2),
+                                       acc[j]);
+        }
+    }
+}
+
 // Split-partials variant, for few rows with many partials (the fan-out join):
 // one block per row; warp w accumulates partials w, w + 8, ... and the eight
 // warps' sums are combined in shared memory, so all of a row's partial loads
@@ -497,6 +633,11 @@ template <int D, bool PF, bool OF>
 cudaError_t run(const MergeArgs& a, long long rows, cudaStream_t stream) {
     const long long tiled_blocks = static_cast<long long>(a.B) * a.H * ((a.S + 31) / 32);
     const long long n_sm = sm_count_cached();
+    if (a.H % kHeadBlock == 0 && a.P <= kHeadBlockMaxP && tiled_blocks / kHeadBlock >= 4 * n_sm) {
+        const long long blocks = tiled_blocks / kHeadBlock;
+        return launch_pdl(lse_merge_headblock_kernel<D, PF, OF>, static_cast<unsigned>(blocks), kWarps * 32, 0,
+                          stream, a.part_O, a.part_lse, a.out, a.out_lse, a.P, a.B, a.S, a.H);
+    }
     if (a.P <= kMaxTiledP && tiled_blocks >= 4 * n_sm) {
         const long long blocks = tiled_blocks;
         const size_t smem = static_cast<size_t>(a.P) * 32 * sizeof(float);

@@ -249,6 +249,29 @@ def test_lse_merge_few_rows_many_partials(P, B, S, H, D):
     _close(mL.cpu().double().numpy(), rL, 1e-5, "merged lse")
 
 
+@pytest.mark.parametrize("dt,D,B,S,H,P", [(torch.bfloat16, 128, 1, 2496, 64, 3), (torch.float32, 64, 2, 2500, 32, 5),
+                                         (torch.bfloat16, 64, 1, 8190, 24, 6), (torch.float32, 128, 1, 2500, 64, 2)])
+def test_lse_merge_head_blocks(dt, D, B, S, H, P):
+    """Many rows, heads in multiples of 8: blocks of 8 heads x 32 positions.  Partial p is empty
+    for the positions before p * S / P (a causal shard layout: whole blocks skip it), a few rows
+    are empty inside non-empty partials, empty partials hold NaN, S is not a multiple of 32."""
+    g = torch.Generator().manual_seed(S + D + P)
+    pO = torch.randn(P, B, S, H, D, generator=g).to(dt)
+    pL = torch.randn(P, B, H, S, generator=g) * 3
+    for p_ in range(P):
+        pL[p_, :, :, : p_ * S // P] = -float("inf")
+        pO[p_, :, : p_ * S // P] = float("nan")
+    pL[P - 1, 0, 3, S - 5] = -float("inf")                  # an empty row inside a non-empty partial
+    pL[:, 0, 1, 0] = -float("inf")                          # a row with no partial at all
+    mO, mL = ra.lse_merge(pO.cuda(), pL.cuda())
+    ra.device_status()
+    rO, rL = oracle.lse_merge(torch.nan_to_num(pO.double()).numpy(), pL.double().numpy())
+    assert torch.isfinite(mO.float()).all()
+    tol = 2e-2 if dt == torch.bfloat16 else 1e-5
+    _close(mO.float().cpu().double().numpy(), rO, tol, "merged O")
+    _close(mL.cpu().double().numpy(), rL, 1e-5, "merged lse")
+
+
 def test_lse_merge_many_partials():
     """More partials than the tiled merge kernel holds in shared memory."""
     P, B, S, H, D = 300, 1, 5, 2, 64
