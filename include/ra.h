@@ -227,10 +227,15 @@ ra_status ra_lse_merge(const void* partials_O, const float* partials_lse, void* 
  *   out            [R, Hq, D] dtype dt;   lse [Hq, R] fp32 (may be NULL).
  *   workspace      device scratch of at least
  *                  ra_prefix_fanout_workspace_size(...) bytes, 256-byte aligned,
- *                  owned by the caller; contents on entry are ignored.
- *   Only dt = RA_BF16 is implemented; D = 64 or 128; Hq % Hkv == 0 and
- *   128 % (Hq / Hkv) == 0; S_prefix >= 0, S_suffix >= 0, R >= 0.
- * Errors: RA_ERR_WORKSPACE if workspace is NULL or too small, otherwise as above.
+ *                  owned by the caller; contents on entry are ignored.  Not
+ *                  used (may be NULL) for dt = RA_F32.
+ *   dt = RA_BF16: tensor cores, prefix split into chunks joined by the merge.
+ *   dt = RA_F32: exact fp32 on the CUDA cores (FFMA, expf), each branch's rows
+ *   walking the whole prefix and their suffix; no partials.
+ *   D = 64 or 128; Hq % Hkv == 0 and 128 % (Hq / Hkv) == 0; S_prefix >= 0,
+ *   S_suffix >= 0, R >= 0.
+ * Errors: RA_ERR_WORKSPACE if a bf16 call's workspace is NULL or too small,
+ * otherwise as above.
  */
 ra_status ra_prefix_fanout_attn(const void* q_rows, const int* branch_offsets, int n_branches, int R,
                                 const void* k_prefix, const void* v_prefix, int S_prefix,
@@ -285,7 +290,7 @@ ra_status ra_prefix_fanout_attn_paged(const void* q_rows, const int* branch_offs
 
 /* Bytes of workspace ra_prefix_fanout_attn (and ra_prefix_fanout_prefill,
  * ra_prefix_fanout_attn_paged) needs for these sizes on the current device (0
- * if the sizes are invalid). */
+ * if the sizes are invalid, and for dt = RA_F32, which needs none). */
 size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int S_suffix, int Hq,
                                        int Hkv, int D, ra_dtype dt);
 

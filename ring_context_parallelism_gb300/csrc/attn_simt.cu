@@ -145,7 +145,180 @@ __global__ void __launch_bounds__(kRows * (D / 32)) attn_simt_kernel(const SimtP
     }
 }
 
+// Shared-prefix fan-out in exact fp32 ("AHBM Agentic Runtime Architecture",
+// sections 1.3 and 3.2: the stacked query rows of all branches against one
+// shared prefix; section 5.2: a branch never sees another branch's private
+// KV).  A CTA owns up to 32 stacked (row, query head) pairs of one branch b and
+// one KV head: the rows of b times the query heads of the KV head's group.  It
+// walks the whole prefix, then b's suffix, with the ring kernel's online
+// softmax, and writes O and lse directly (no partials, no merge).  The branch
+// offsets live in device memory, so the grid covers every (branch, KV head)
+// with as many row tiles as R allows; tiles past a branch's rows exit.
+struct SimtFanParams {
+    const float *q, *kp, *vp, *ks, *vs;  // q_rows [R,Hq,D]; prefix [Sp,Hkv,D]; suffix [nb,Ss,Hkv,D] (or page pools)
+    const int* offsets;
+    int R, nb, Sp, Ss, Hq, Hkv, G, tiles, suffix_causal;
+    int paged, page_shift, n_pages, n_prefix_pages, n_suffix_pages;
+    const int* prefix_pages;
+    const int* suffix_pages;
+    float scale;
+    float* out;  // [R, Hq, D]
+    float* lse;  // [Hq, R] (may be null)
+};
+
+template <int D>
+__global__ void __launch_bounds__(kRows * (D / 32)) attn_simt_fanout_kernel(const SimtFanParams p) {
+    constexpr int TPR = D / 32;
+    __shared__ __align__(16) float ks[kChunk][D];
+    __shared__ __align__(16) float vs[kChunk][D];
+    const int tid = threadIdx.x;
+    const int r_local = tid / TPR;
+    const int sub = tid % TPR;
+    const int tile = blockIdx.x % p.tiles;
+    const int rest = blockIdx.x / p.tiles;
+    const int hk = rest % p.Hkv;
+    const int b = rest / p.Hkv;
+    const int lo = p.offsets[b], hi = p.offsets[b + 1];
+    if (lo < 0 || hi < lo || hi > p.R || (b == 0 && lo != 0) || (b == p.nb - 1 && hi != p.R)) {
+        if (tid == 0) {
+            atomicCAS(&g_simt_status[0], 0u, kDevInvalidArg);
+            atomicCAS(&g_simt_status[1], 0u, 0x0F000000u | static_cast<unsigned>(b));
+        }
+        return;
+    }
+    const int n_rows = (hi - lo) * p.G;  // stacked (row, head) pairs of this branch and KV head
+    if (tile * kRows >= n_rows) return;
+    const int stacked = tile * kRows + r_local;
+    const bool active = stacked < n_rows;
+    const int row = lo + (active ? stacked / p.G : 0);
+    const int h = hk * p.G + (active ? stacked % p.G : 0);
+    // prefill: the branch's rows are the last tokens of its suffix, causal inside it
+    const int last = p.suffix_causal ? p.Ss - (hi - lo) + (row - lo) : p.Ss - 1;
+
+    float q[32], o[32];
+    const float* qp = p.q + (static_cast<long long>(row) * p.Hq + h) * D + sub;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        q[j] = active ? qp[j * TPR] : 0.f;
+        o[j] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    const int page_mask = (1 << p.page_shift) - 1;
+
+    for (int seg = 0; seg < 2; ++seg) {
+        const int n_keys = seg == 0 ? p.Sp : p.Ss;
+        const float* kb = seg == 0 ? p.kp : p.ks;
+        const float* vb = seg == 0 ? p.vp : p.vs;
+        const int* table = seg == 0 ? p.prefix_pages : p.suffix_pages + static_cast<long long>(b) * p.n_suffix_pages;
+        const int n_listed = seg == 0 ? p.n_prefix_pages : p.n_suffix_pages;
+        for (int c0 = 0; c0 < n_keys; c0 += kChunk) {
+            const int n = min(kChunk, n_keys - c0);
+            __syncthreads();
+            for (int e = tid; e < kChunk * (D / 4); e += blockDim.x) {
+                const int kr = e / (D / 4);
+                const int kc = (e % (D / 4)) * 4;
+                float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
+                if (kr < n) {
+                    const int key = c0 + kr;
+                    long long r = -1;  // key's row in its tensor (or page pool)
+                    if (p.paged) {
+                        const int lp = key >> p.page_shift;
+                        const int pg = lp < n_listed ? table[lp] : -1;
+                        if (pg >= 0 && pg < p.n_pages) {
+                            r = (static_cast<long long>(pg) << p.page_shift) + (key & page_mask);
+                        } else {
+                            atomicCAS(&g_simt_status[0], 0u, kDevInvalidArg);
+                            atomicCAS(&g_simt_status[1], 0u, 0x0E000000u | static_cast<unsigned>(lp & 0xFFFFFF));
+                        }
+                    } else {
+                        r = seg == 0 ? key : static_cast<long long>(b) * p.Ss + key;
+                    }
+                    if (r >= 0) {
+                        const long long off = (r * p.Hkv + hk) * D + kc;
+                        kv4 = *reinterpret_cast<const float4*>(kb + off);
+                        vv4 = *reinterpret_cast<const float4*>(vb + off);
+                    }
+                }
+                *reinterpret_cast<float4*>(&ks[kr][kc]) = kv4;
+                *reinterpret_cast<float4*>(&vs[kr][kc]) = vv4;
+            }
+            __syncthreads();
+            float s[kChunk];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kChunk; ++c) {
+                float acc = 0.f;
+#pragma unroll
+                for (int d = 0; d < 32; ++d) acc = fmaf(q[d], ks[c][d * TPR + sub], acc);
+#pragma unroll
+                for (int x = 1; x < TPR; x <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
+                const bool vis = c < n && (seg == 0 || c0 + c <= last);
+                s[c] = vis ? acc * p.scale : -INFINITY;
+                mx = fmaxf(mx, s[c]);
+            }
+            const float m_new = fmaxf(m, mx);
+            if (m_new == -INFINITY) continue;  // nothing visible yet for this row
+            const float alpha = (m == -INFINITY) ? 0.f : expf(m - m_new);
+            float rs = 0.f;
+#pragma unroll
+            for (int d = 0; d < 32; ++d) o[d] *= alpha;
+#pragma unroll
+            for (int c = 0; c < kChunk; ++c) {
+                const float pc = expf(s[c] - m_new);
+                rs += pc;
+#pragma unroll
+                for (int d = 0; d < 32; ++d) o[d] = fmaf(pc, vs[c][d * TPR + sub], o[d]);
+            }
+            l = l * alpha + rs;
+            m = m_new;
+        }
+    }
+    if (!active) return;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    float* dst = p.out + (static_cast<long long>(row) * p.Hq + h) * D + sub;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) dst[j * TPR] = o[j] * inv;
+    if (sub == 0 && p.lse) p.lse[static_cast<long long>(h) * p.R + row] = l > 0.f ? m + logf(l) : -INFINITY;
+}
+
 }  // namespace
+
+cudaError_t launch_fanout_simt(const FanoutSimtArgs& a, cudaStream_t stream) {
+    if (a.R == 0) return cudaSuccess;
+    SimtFanParams p{};
+    p.q = a.q_rows;
+    p.kp = a.k_prefix;
+    p.vp = a.v_prefix;
+    p.ks = a.k_suffix;
+    p.vs = a.v_suffix;
+    p.offsets = a.offsets;
+    p.R = a.R;
+    p.nb = a.n_branches;
+    p.Sp = a.S_prefix;
+    p.Ss = a.S_suffix;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = a.Hq / a.Hkv;
+    p.tiles = (a.R * p.G + kRows - 1) / kRows;  // at most every stacked row in one branch
+    p.suffix_causal = a.suffix_causal;
+    p.paged = a.paged;
+    p.page_shift = a.page_shift;
+    p.n_pages = a.n_pages;
+    p.n_prefix_pages = a.n_prefix_pages;
+    p.n_suffix_pages = a.n_suffix_pages;
+    p.prefix_pages = a.prefix_pages;
+    p.suffix_pages = a.suffix_pages;
+    p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(a.D)));
+    p.out = a.out;
+    p.lse = a.lse;
+    const long long grid = static_cast<long long>(a.n_branches) * a.Hkv * p.tiles;
+    if (grid > 0x7fffffffll) return cudaErrorInvalidValue;
+    if (a.D == 128)
+        attn_simt_fanout_kernel<128><<<static_cast<unsigned>(grid), kRows * 4, 0, stream>>>(p);
+    else
+        attn_simt_fanout_kernel<64><<<static_cast<unsigned>(grid), kRows * 2, 0, stream>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_ring_simt(const RingSimtArgs& a, cudaStream_t stream) {
     SimtParams p;

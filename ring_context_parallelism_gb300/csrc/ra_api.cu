@@ -149,7 +149,6 @@ ra_status check_fanout(const void* q_rows, const int* offsets, int n_branches, i
                        const void* v_prefix, int S_prefix, const void* k_suffix, const void* v_suffix, int S_suffix,
                        const void* out, int Hq, int Hkv, int D, ra_dtype dt) {
     if (dt != RA_BF16 && dt != RA_F32) return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dt));
-    if (dt != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "fan-out is implemented for bf16 only");
     if (R < 0 || n_branches < 1 || S_prefix < 0 || S_suffix < 0)
         return fail(RA_ERR_INVALID_ARG, "R >= 0, n_branches >= 1, S_prefix >= 0, S_suffix >= 0 required");
     if (Hq < 1 || Hkv < 1 || Hq % Hkv) return fail(RA_ERR_INVALID_ARG, "Hq must be a positive multiple of Hkv");
@@ -293,8 +292,9 @@ ra_status ra_lse_merge(const void* partials_O, const float* partials_lse, void* 
 size_t ra_prefix_fanout_workspace_size(int R, int n_branches, int S_prefix, int S_suffix, int Hq, int Hkv, int D,
                                        ra_dtype dt) {
     if (R < 0 || n_branches < 1 || S_prefix < 0 || S_suffix < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv ||
-        (D != 64 && D != 128) || dt != RA_BF16 || 128 % (Hq / Hkv) || S_prefix + S_suffix < 1)
+        (D != 64 && D != 128) || (dt != RA_BF16 && dt != RA_F32) || 128 % (Hq / Hkv) || S_prefix + S_suffix < 1)
         return 0;
+    if (dt == RA_F32) return 0;  // the fp32 path writes its rows directly
     // one size for the contiguous and the paged entry points (their splits may differ)
     const size_t a = plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D, false).total;
     const size_t b = plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D, true).total;
@@ -361,6 +361,43 @@ static ra_status launch_fanout(const FanoutPlan& f, float* part_o, float* part_l
     return ok();
 }
 
+// fp32 fan-out: the CUDA-core kernel writes O and lse itself (no workspace).
+static ra_status launch_fanout_f32(const void* q_rows, const int* branch_offsets, int n_branches, int R,
+                                   const void* k_prefix, const void* v_prefix, int S_prefix, const void* k_suffix,
+                                   const void* v_suffix, int S_suffix, void* out, float* lse, int Hq, int Hkv, int D,
+                                   void* stream, int suffix_causal, const PagedKv& pg) {
+    ra::FanoutSimtArgs a{};
+    a.q_rows = static_cast<const float*>(q_rows);
+    a.offsets = branch_offsets;
+    a.n_branches = n_branches;
+    a.R = R;
+    a.k_prefix = static_cast<const float*>(k_prefix);
+    a.v_prefix = static_cast<const float*>(v_prefix);
+    a.S_prefix = S_prefix;
+    a.k_suffix = static_cast<const float*>(k_suffix);
+    a.v_suffix = static_cast<const float*>(v_suffix);
+    a.S_suffix = S_suffix;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.out = static_cast<float*>(out);
+    a.lse = lse;
+    a.suffix_causal = suffix_causal;
+    if (pg.paged) {
+        const int page_size = 1 << pg.page_shift;
+        a.paged = 1;
+        a.page_shift = pg.page_shift;
+        a.n_pages = pg.n_pages;
+        a.n_prefix_pages = (S_prefix + page_size - 1) / page_size;
+        a.n_suffix_pages = (S_suffix + page_size - 1) / page_size;
+        a.prefix_pages = pg.prefix_pages;
+        a.suffix_pages = pg.suffix_pages;
+    }
+    const cudaError_t e = ra::launch_fanout_simt(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fp32 fan-out launch");
+    return ok();
+}
+
 static ra_status fanout_common(const void* q_rows, const int* branch_offsets, int n_branches, int R,
                                const void* k_prefix, const void* v_prefix, int S_prefix, const void* k_suffix,
                                const void* v_suffix, int S_suffix, void* out, float* lse, int Hq, int Hkv, int D,
@@ -371,6 +408,9 @@ static ra_status fanout_common(const void* q_rows, const int* branch_offsets, in
     if (st != RA_OK) return st;
     if (lse && !aligned16(lse)) return fail(RA_ERR_INVALID_ARG, "lse must be 16-byte aligned");
     if (R == 0) return ok();
+    if (dt == RA_F32)
+        return launch_fanout_f32(q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix, k_suffix,
+                                 v_suffix, S_suffix, out, lse, Hq, Hkv, D, stream, suffix_causal, pg);
     const FanoutPlan f = plan_fanout(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D, pg.paged != 0);
     if (!workspace || workspace_bytes < f.total)
         return fail(RA_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", f.total, workspace_bytes);
@@ -432,6 +472,9 @@ ra_status ra_prefix_fanout_attn_noalloc(const void* q_rows, const int* branch_of
     if (st != RA_OK) return st;
     if (lse && !aligned16(lse)) return fail(RA_ERR_INVALID_ARG, "lse must be 16-byte aligned");
     if (R == 0) return ok();
+    if (dt == RA_F32)  // the fp32 path has no partials: the scratch array is not used
+        return launch_fanout_f32(q_rows, branch_offsets, n_branches, R, k_prefix, v_prefix, S_prefix, k_suffix,
+                                 v_suffix, S_suffix, out, lse, Hq, Hkv, D, stream, 0, PagedKv());
     const size_t cap = RA_NOALLOC_SCRATCH_BYTES;
     const FanoutPlan f = plan_fanout_bounded(R, n_branches, S_prefix, S_suffix, Hq, Hkv, D, cap);
     if (f.total == 0)

@@ -79,6 +79,26 @@ struct RingSimtArgs {
 };
 cudaError_t launch_ring_simt(const RingSimtArgs& a, cudaStream_t stream);
 
+// Shared-prefix fan-out in exact fp32 on the CUDA cores: O [R, Hq, D] and lse
+// [Hq, R] written directly (no partials, no workspace).
+struct FanoutSimtArgs {
+    const float* q_rows;
+    const int* offsets;
+    int n_branches, R;
+    const float *k_prefix, *v_prefix;
+    int S_prefix;
+    const float *k_suffix, *v_suffix;
+    int S_suffix;
+    int Hq, Hkv, D;
+    float* out;
+    float* lse;
+    int suffix_causal = 0;
+    int paged = 0, page_shift = 0, n_pages = 0, n_prefix_pages = 0, n_suffix_pages = 0;
+    const int* prefix_pages = nullptr;
+    const int* suffix_pages = nullptr;
+};
+cudaError_t launch_fanout_simt(const FanoutSimtArgs& a, cudaStream_t stream);
+
 // Row-indexed LSE merge.  part_f32 / out_f32 select fp32 or bf16 storage.
 struct MergeArgs {
     const void* part_O;

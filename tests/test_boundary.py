@@ -92,7 +92,7 @@ def test_fanout_argument_validation(lib):
         for k, v in kw.items():
             a[idx[k]] = v
         return f(*a)
-    assert call(dt=rab.RA_F32) == rab.RA_ERR_UNSUPPORTED
+    assert call(dt=7) == rab.RA_ERR_INVALID_ARG        # unknown dtype
     assert call(Hq=24, Hkv=8) == rab.RA_ERR_UNSUPPORTED
     assert call(Hq=15, Hkv=2) == rab.RA_ERR_INVALID_ARG
     assert call(nb=0) == rab.RA_ERR_INVALID_ARG
@@ -104,6 +104,12 @@ def test_fanout_argument_validation(lib):
     assert call(wsb=64) == rab.RA_ERR_WORKSPACE
     assert call(ws=272) == rab.RA_ERR_INVALID_ARG     # not 256-byte aligned
     assert call(R=0) == rab.RA_OK                      # nothing to do, nothing launched
+
+
+def test_fp32_fanout_needs_no_workspace(lib):
+    """The fp32 fan-out writes its rows directly: its workspace size is 0."""
+    assert lib.ra_prefix_fanout_workspace_size(16, 4, 4096, 256, 64, 8, 128, rab.RA_F32) == 0
+    assert lib.ra_prefix_fanout_workspace_size(16, 4, 4096, 256, 64, 8, 128, rab.RA_BF16) > 0
 
 
 def test_workspace_size_query(lib):

@@ -373,6 +373,39 @@ def test_fanout_paged_full(Sp, Ss, rows, Hq, Hkv, D, page, prefill):
     _close(L.cpu().double().numpy(), rL, 1e-3, "lse")
 
 
+@pytest.mark.parametrize("Sp,Ss,rows,Hq,Hkv,D,mode", [
+    (1000, 200, [3, 0, 16, 1, 7], 16, 2, 128, "decode"),    # ragged tails, an empty branch
+    (640, 128, [33, 5], 8, 2, 64, "decode"),                 # a branch with more rows than one tile
+    (0, 300, [2, 9], 8, 1, 128, "decode"),                   # no shared prefix
+    (2048, 0, [4, 4, 4], 16, 4, 64, "decode"),               # no private suffix
+    (1500, 24, [40, 10, 16], 16, 4, 64, "prefill"),          # causal in each suffix, rows past its tokens
+    (1000, 200, [3, 0, 16, 1, 7], 16, 2, 128, "paged"),      # 16-token pages
+    (700, 90, [5, 2], 32, 8, 64, "noalloc"),
+])
+def test_fanout_f32_full(Sp, Ss, rows, Hq, Hkv, D, mode):
+    """fp32 inputs: the exact CUDA-core fan-out, all rows against the oracle at the fp32 bar."""
+    w = small(WORKLOADS["fanout_decode"], S_prefix=Sp, S_suffix=Ss, n_branches=len(rows), Hq=Hq, Hkv=Hkv, D=D,
+              dtype="f32", seed=1300 + Sp + Ss + D)
+    x = fanout_inputs(w, "cpu", rows=rows)
+    assert x["q_rows"].dtype == torch.float32
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    args = [dev[k] for k in ("q_rows", "offsets", "k_prefix", "v_prefix", "k_suffix", "v_suffix")]
+    if mode == "paged":
+        kpool, pp, sp = paginate(x["k_prefix"], x["k_suffix"], 16, 3, seed=2)
+        vpool, _, _ = paginate(x["v_prefix"], x["v_suffix"], 16, 3, seed=2)
+        O, L = ra.fanout_paged(dev["q_rows"], dev["offsets"], kpool.cuda(), vpool.cuda(), pp.cuda(), Sp, sp.cuda(), Ss)
+    elif mode == "noalloc":
+        O, L = ra.fanout_noalloc(*args)
+    else:
+        O, L = ra.fanout(*args, prefill=(mode == "prefill"))
+    ra.device_status()
+    rO, rL = oracle.fanout(x["q_rows"].numpy(), x["offsets"].numpy(), x["k_prefix"].numpy(), x["v_prefix"].numpy(),
+                           x["k_suffix"].numpy(), x["v_suffix"].numpy(), dtype="f32",
+                           suffix_causal=(mode == "prefill"))
+    _close(O.cpu().double().numpy(), rO, 1e-4, "O")
+    _close(L.cpu().double().numpy(), rL, 1e-4, "lse")
+
+
 def test_fanout_paged_rejects_a_page_outside_the_pool():
     """A page index outside the pool is reported by the device check (its keys read as zeros)."""
     w = small(WORKLOADS["fanout_decode"], S_prefix=512, S_suffix=64, n_branches=2, Hq=8, Hkv=2, D=128, seed=3)
