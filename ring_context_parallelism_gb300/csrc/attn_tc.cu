@@ -53,6 +53,7 @@ constexpr int kThreads = 384;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kTmemCols = 512;
 constexpr int kMaxChunks = 64;
+constexpr int kLaunchRegs = 168;  // registers per thread at launch: 65536 / 384, rounded down to a multiple of 8
 
 struct TcParams {
     int fanout;     // 0 ring prefill, 1 fan-out
@@ -407,25 +408,6 @@ struct StageCtr {
     }
 };
 
-// Register split per warpgroup (at most the launch's 384 x 168 = 64512): ring
-// mode 128 x 48 + 2 x 128 x 224 (the MMA issuer's loop fits without spills);
-// fan-out mode, whose producers also walk the folded suffixes, 128 x 56 +
-// 2 x 128 x 224.
-template <bool FAN>
-__device__ __forceinline__ void reg_dec() {
-    if (FAN)
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
-    else
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 48;" ::: "memory");
-}
-template <bool FAN>
-__device__ __forceinline__ void reg_inc() {
-    if (FAN)
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
-    else
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
-}
-
 // Kernel variants: ring prefill, and fan-out launches whose units all split
 // their KV tiles over the two tile slots (one row tile), all pair two row
 // tiles, or mix both (suffix units without a prefix).  The uniform fan-out
@@ -443,6 +425,40 @@ enum KernelMode : int {
     kModeFanSplitPaged = 6,
     kModeFanPairedPaged = 7
 };
+
+// Register split per warpgroup: the producer / MMA warpgroup's registers per
+// thread (dec) and the two softmax warpgroups' (inc), at most the launch's
+// 384 x 168 = 64512 in all.  Chosen per kernel variant as the split with the
+// fewest spilled bytes in ptxas's report, which also measured fastest: the
+// contiguous ring prefill 64 / 216 (its unrolled MMA loop spilled at 48), the
+// fan-out split and paired variants 40 / 232 and 80 / 208 (3% faster than
+// 56 / 224 on the R = 147 decode and the 8 x 20 prefill), the mixed and paged
+// mixed variants 80 / 208 and 72 / 216; the rest 48 or 56 / 224.
+template <int MODE>
+struct RegSplit {
+    static constexpr int dec = MODE == kModeRing           ? 64
+                               : MODE == kModeFanMixed      ? 80
+                               : MODE == kModeFanSplit      ? 40
+                               : MODE == kModeFanPaired     ? 80
+                               : MODE == kModeRingLayout    ? 48
+                               : MODE == kModeFanMixedPaged ? 72
+                                                            : 56;
+    static constexpr int inc = MODE == kModeRing           ? 216
+                               : MODE == kModeFanMixed      ? 208
+                               : MODE == kModeFanSplit      ? 232
+                               : MODE == kModeFanPaired     ? 208
+                               : MODE == kModeFanMixedPaged ? 216
+                                                            : 224;
+    static_assert(128 * dec + 256 * inc <= kThreads * kLaunchRegs, "register split exceeds the launch's registers");
+};
+template <int MODE>
+__device__ __forceinline__ void reg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RegSplit<MODE>::dec) : "memory");
+}
+template <int MODE>
+__device__ __forceinline__ void reg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RegSplit<MODE>::inc) : "memory");
+}
 
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -538,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 16-token pages), and the TMA unit takes small boxes slowly from a
         // single issuing thread: there every lane of the warp walks the tiles,
         // lane 0 sets the stage's expected bytes and each lane issues one box.
-        reg_dec<FAN>();
+        reg_dec<MODE>();
         constexpr bool warp_issue = PG;
         if (lane == 0 || warp_issue) {
             const bool lead = lane == 0;
@@ -635,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        reg_dec<FAN>();
+        reg_dec<MODE>();
         if (lane == 0) {
             const uint32_t q_addr = smem_u32(q_smem);
             // low descriptor words: Q tiles, K stages (LBO 16 B), V stages (LBO 16 KB)
@@ -811,10 +827,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(drain, 0, abort_flag, status, 0);
         }
     } else if (warp == 3) {
-        reg_dec<FAN>();
+        reg_dec<MODE>();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        reg_inc<FAN>();
+        reg_inc<MODE>();
         const int t = (warp - 4) >> 2;
         if (t < T) {
         const int quad = warp & 3;
@@ -1153,6 +1169,11 @@ cudaError_t launch(const TcParams& p, int grid, const CUtensorMap& q, const CUte
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(attn_tc_kernel<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        // the softmax warpgroups' register increase draws on the launch's registers:
+        // a build that launched with fewer would wait for them forever
+        cudaFuncAttributes fa;
+        if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, attn_tc_kernel<D, MODE>);
+        if (attr_err == cudaSuccess && fa.numRegs < kLaunchRegs) attr_err = cudaErrorLaunchOutOfResources;
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (grid <= 0) return cudaSuccess;
