@@ -57,7 +57,6 @@ constexpr int kLaunchRegs = 168;  // registers per thread at launch: 65536 / 384
 
 struct TcParams {
     int fanout;     // 0 ring prefill, 1 fan-out
-    int partials;   // ring: one partial per KV shard
     int causal;
     int layout;     // ring: shard layout (ra_walk.h), used when causal
     int T2;         // ring: two heads per CTA (GQA group size even)
@@ -414,7 +413,10 @@ struct StageCtr {
 // variants compile only their own issue and softmax paths.
 // kModeRingLayout: a causal ring walk over zigzag or striped shards.  The
 // fan-out modes over a paged KV pool (kModeFan*Paged) are the same three
-// fan-out variants with the producers' page-table path compiled in.
+// fan-out variants with the producers' page-table path compiled in.  The ring
+// walks that write one partial per KV shard (kModeRing*Partials) are compiled
+// apart from the single-output ones: the flush inside the tile loop made the
+// contiguous prefill 7% slower (5.30 against 4.95 ms) where it is never taken.
 enum KernelMode : int {
     kModeRing = 0,
     kModeFanMixed = 1,
@@ -423,32 +425,39 @@ enum KernelMode : int {
     kModeRingLayout = 4,
     kModeFanMixedPaged = 5,
     kModeFanSplitPaged = 6,
-    kModeFanPairedPaged = 7
+    kModeFanPairedPaged = 7,
+    kModeRingPartials = 8,
+    kModeRingLayoutPartials = 9
 };
 
 // Register split per warpgroup: the producer / MMA warpgroup's registers per
 // thread (dec) and the two softmax warpgroups' (inc), at most the launch's
-// 384 x 168 = 64512 in all.  Chosen per kernel variant as the split with the
-// fewest spilled bytes in ptxas's report, which also measured fastest: the
-// contiguous ring prefill 64 / 216 (its unrolled MMA loop spilled at 48), the
-// fan-out split and paired variants 40 / 232 and 80 / 208 (3% faster than
-// 56 / 224 on the R = 147 decode and the 8 x 20 prefill), the mixed and paged
-// mixed variants 80 / 208 and 72 / 216; the rest 48 or 56 / 224.
+// 384 x 168 = 64512 in all.  ptxas's spill report moves erratically with the
+// split, so each kernel variant takes the split that measured fastest among
+// those with the fewest spilled bytes: the contiguous ring 64 / 216 (its
+// unrolled MMA loop spilled at 48), the zigzag / striped ring 144 / 176 (5.57
+// against 5.73 ms on the 32K zigzag prefill), the fan-out split and paired
+// variants 40 / 232 and 80 / 208 (3% faster than 56 / 224 on the R = 147
+// decode and the 8 x 20 prefill); the rest by the spill report alone.
 template <int MODE>
 struct RegSplit {
-    static constexpr int dec = MODE == kModeRing           ? 64
-                               : MODE == kModeFanMixed      ? 80
-                               : MODE == kModeFanSplit      ? 40
-                               : MODE == kModeFanPaired     ? 80
-                               : MODE == kModeRingLayout    ? 48
-                               : MODE == kModeFanMixedPaged ? 72
-                                                            : 56;
-    static constexpr int inc = MODE == kModeRing           ? 216
-                               : MODE == kModeFanMixed      ? 208
-                               : MODE == kModeFanSplit      ? 232
-                               : MODE == kModeFanPaired     ? 208
-                               : MODE == kModeFanMixedPaged ? 216
-                                                            : 224;
+    static constexpr int dec = MODE == kModeRing                ? 64
+                               : MODE == kModeFanMixed           ? 80
+                               : MODE == kModeFanSplit           ? 40
+                               : MODE == kModeFanPaired          ? 80
+                               : MODE == kModeRingLayout         ? 144
+                               : MODE == kModeFanMixedPaged      ? 72
+                               : MODE == kModeRingPartials       ? 64
+                               : MODE == kModeRingLayoutPartials ? 48
+                                                                 : 56;
+    static constexpr int inc = MODE == kModeRing                ? 216
+                               : MODE == kModeFanMixed           ? 208
+                               : MODE == kModeFanSplit           ? 232
+                               : MODE == kModeFanPaired          ? 208
+                               : MODE == kModeRingLayout         ? 176
+                               : MODE == kModeFanMixedPaged      ? 216
+                               : MODE == kModeRingPartials       ? 216
+                                                                 : 224;
     static_assert(128 * dec + 256 * inc <= kThreads * kLaunchRegs, "register split exceeds the launch's registers");
 };
 template <int MODE>
@@ -466,10 +475,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_k2,
                    const __grid_constant__ CUtensorMap tm_v2, const TcParams p) {
     using C = Cfg<D>;
-    constexpr bool RING = MODE == kModeRing || MODE == kModeRingLayout;
+    constexpr bool PART = MODE == kModeRingPartials || MODE == kModeRingLayoutPartials;  // one partial per KV shard
+    constexpr bool RING = MODE == kModeRing || MODE == kModeRingLayout || PART;
     constexpr bool FAN = !RING;
-    constexpr bool LAY = MODE == kModeRingLayout;
-    constexpr bool PG = MODE >= kModeFanMixedPaged;              // paged KV pool
+    constexpr bool LAY = MODE == kModeRingLayout || MODE == kModeRingLayoutPartials;
+    constexpr bool PG = MODE >= kModeFanMixedPaged && MODE <= kModeFanPairedPaged;  // paged KV pool
     constexpr int FMODE = PG ? MODE - kModeFanMixedPaged + kModeFanMixed : MODE;  // its unpaged fan-out mode
     const Unit u = decode_unit<FAN, LAY>(p);
     if (!u.valid) return;
@@ -702,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t q0 = q_lo0, q1 = q_lo0 + kStageLo;
                 const uint32_t k_end = k_lo0 + nK * kStageLo, v_end = v_lo0 + nV * kStageLo;
                 uint32_t k_lo = k_lo0, v_lo = v_lo0;
-                const bool track = p.partials && !FAN;
+                const bool track = PART && !FAN;
                 RingIterT<LAY> wp;  // tile i - 1 (shard openings restart O in partials mode)
                 if (track) wp.start(w);
                 // One iteration with runtime stage indices.
@@ -755,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (contiguous ring prefill only: the fan-out and zigzag / striped variants
                 // measured slower with it -- their larger code missed the instruction
                 // cache: 3x the no-instruction stalls of the contiguous mode under ncu)
-                for (; MODE == kModeRing && ok && i + kBlk <= total; i += kBlk) {
+                for (; (MODE == kModeRing || MODE == kModeRingPartials) && ok && i + kBlk <= total; i += kBlk) {
                     const uint32_t kb = k_lo0, vb = v_lo0, qa = q0, qb = q1;
 #pragma unroll
                     for (int pos = 0; pos < kBlk; ++pos) {
@@ -791,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             RingIterT<LAY> wp;  // at iteration i >= 1: tile i-1 (shard openings restart O in partials mode)
             if (!FAN) wp.start(w);
             for (int i = 0; ok && !split && T == 1 && i <= total; ++i) {
-                const bool fresh_prev = (p.partials && !FAN) ? wp.first() : (i == 1);
+                const bool fresh_prev = (PART && !FAN) ? wp.first() : (i == 1);
                 for (int t = 0; t < T && ok; ++t) {
                     const uint32_t tS = tmem_base + t * 256;
                     if (i > 0) {
@@ -931,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!(ok = mbar_wait(s_bar, s_par, abort_flag, status, 0x07000000u | i))) break;
             tc_fence_after();
-            if (p.partials && tile_first && jj > 0) {
+            if (PART && tile_first && jj > 0) {
                 // The previous KV shard of the ring is complete (this tile's S was
                 // committed after its last PV): flush it.
                 flush(nullptr, 0, last_shard);
@@ -999,7 +1009,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mraw = dead_row ? -INFINITY : fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
             const float mx = mraw * p.scale_log2;  // scores in log2 units
-            const bool fresh = (jj == 0) || (p.partials && tile_first);
+            const bool fresh = (jj == 0) || (PART && tile_first);
             float alpha = 1.f;
             bool resc = false;
             if (fresh) {
@@ -1124,7 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     L > 0.f ? (m + log2f(L)) * 0.69314718055994531f : -INFINITY;
         } else if (ok) {
             // the last PV: every MMA of the CTA is complete once `drain` is
-            if (!FAN && p.partials) {
+            if (!FAN && PART) {
                 ok = flush(drain, 0, last_shard);
             } else if (jj > 0) {
                 ok = flush(drain, 0, FAN ? u.slot[t] : 0);
@@ -1133,7 +1143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 out.lse[lse_base + static_cast<long long>(u.slot[t]) * out.lse_part] = -INFINITY;
             }
         }
-        if (ok && !FAN && p.partials) {
+        if (ok && !FAN && PART) {
             // KV shards the causal mask empties for this tile: O = 0, lse = -inf
             for (int t2 = w.n_visited; t2 < p.n_shards; ++t2) {
                 const int j = ring_shard_at(w, t2);
@@ -1215,7 +1225,6 @@ bool make_map(CUtensorMap* m, const void* base, const unsigned long long dims[4]
 cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
     TcParams p{};
     p.fanout = 0;
-    p.partials = a.partials;
     p.causal = a.causal;
     p.layout = a.layout;
     p.B = a.B;
@@ -1240,9 +1249,14 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
     const int grid = p.n_qtiles * a.B * p.n_head_groups;
     // without a causal mask every layout is the same walk
     if (a.causal && a.layout != kLayoutContiguous)
-        return a.D == 128 ? launch<128, kModeRingLayout>(p, grid, tq, tk, tv, tk, tv, stream)
-                          : launch<64, kModeRingLayout>(p, grid, tq, tk, tv, tk, tv, stream);
+        return a.partials ? (a.D == 128 ? launch<128, kModeRingLayoutPartials>(p, grid, tq, tk, tv, tk, tv, stream)
+                                        : launch<64, kModeRingLayoutPartials>(p, grid, tq, tk, tv, tk, tv, stream))
+                          : (a.D == 128 ? launch<128, kModeRingLayout>(p, grid, tq, tk, tv, tk, tv, stream)
+                                        : launch<64, kModeRingLayout>(p, grid, tq, tk, tv, tk, tv, stream));
     p.layout = kLayoutContiguous;
+    if (a.partials)
+        return a.D == 128 ? launch<128, kModeRingPartials>(p, grid, tq, tk, tv, tk, tv, stream)
+                          : launch<64, kModeRingPartials>(p, grid, tq, tk, tv, tk, tv, stream);
     return a.D == 128 ? launch<128, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream)
                       : launch<64, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream);
 }
@@ -1250,7 +1264,6 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
 cudaError_t launch_fanout_tc(const FanoutTcArgs& a, cudaStream_t stream) {
     TcParams p{};
     p.fanout = 1;
-    p.partials = 0;
     p.causal = 0;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
