@@ -69,6 +69,10 @@ struct TcParams {
     int suffix_slot0;   // partial slot of the suffix (suffix units; only without a prefix)
     int fold;           // suffixes folded into prefix units: branch b into chunk b % n_chunks
     int suffix_causal;  // fan-out prefill: a branch's rows are the last tokens of its suffix, causal inside it
+    // ring over a zigzag-stored sequence walked in sequence-position order (0: rows are positions):
+    // position chunk c of zz_half tokens is the first half of shard c (c < zz_n) or the
+    // second half of shard 2 zz_n - 1 - c
+    int zz_n, zz_half;
     // paged KV: the K/V maps address a page pool [n_pages * page_size, Hkv, D];
     // key k of the prefix lives in page prefix_pages[k >> page_shift], key k of
     // branch b's suffix in page suffix_pages[b * n_suffix_pages + (k >> page_shift)]
@@ -119,6 +123,7 @@ struct Unit {
     int suffix;            // fan-out: K/V from the suffix maps
     // ring
     int b, head[2], q_row0;
+    int q_srow0;           // storage row of the query tile (q_row0 unless zigzag in position order)
     // fan-out
     int row0[2], row_hi, kv_lo, kv_hi;
     int split;             // both tiles share Q tile 0 and take alternate KV tiles
@@ -128,6 +133,13 @@ struct Unit {
     int fold_b0;           // fan-out prefix unit: first branch whose suffix is folded in (-1: none)
     int unit_row_lo, unit_row_hi;  // stacked rows the unit's tiles cover
 };
+
+// Storage row of sequence position pos (tile-aligned runs stay inside one chunk).
+__device__ __forceinline__ int zz_row(const TcParams& p, int pos) {
+    if (p.zz_half == 0) return pos;
+    const int c = pos / p.zz_half, o = pos - c * p.zz_half;
+    return (c < p.zz_n ? 2 * c * p.zz_half : (4 * p.zz_n - 1 - 2 * c) * p.zz_half) + o;
+}
 
 template <bool FAN, bool LAY = false>
 __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
@@ -150,11 +162,12 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         u.q_row0 = !p.causal ? qt_rev * kTileM
                    : LAY     ? heavy_tile_row0(p.layout, p.S, p.n_shards, kTileM, qt_rev)
                              : (p.n_qtiles - 1 - qt_rev) * kTileM;
+        u.q_srow0 = LAY ? u.q_row0 : zz_row(p, u.q_row0);
         u.T = p.T2 ? 2 : 1;
         for (int t = 0; t < 2; ++t) {
             u.head[t] = hg * u.T + (t < u.T ? t : 0);
             u.qc1[t] = u.head[t];
-            u.qc2[t] = u.q_row0;
+            u.qc2[t] = u.q_srow0;
             u.qc3[t] = u.b;
         }
         u.kv_head = u.head[0] / (p.Hq / p.Hkv);
@@ -643,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     for (int c = 0; c < C::kChunks; ++c)
                         tma_load_4d(map, &full[cs.s], ring + cs.s * C::kTileBytes + c * 16384, c * 64, u.kv_head,
-                                    wi.key(), z);
+                                    (RING && !LAY) ? zz_row(p, wi.key()) : wi.key(), z);
                 }
                 cs.next(n_stages);
                 ++issued;
@@ -862,9 +875,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             row_ok = row < u.row_hi;
         }
         const OutDesc& out = p.out;
-        const long long o_row_base = static_cast<long long>(u.b) * out.o_b + static_cast<long long>(row) * out.o_row +
+        const int out_row = FAN ? row : u.q_srow0 + lane_row;  // storage row of the output
+        const long long o_row_base = static_cast<long long>(u.b) * out.o_b + static_cast<long long>(out_row) * out.o_row +
                                      static_cast<long long>(head) * out.o_h;
-        const long long lse_base = static_cast<long long>(u.b) * out.lse_b + static_cast<long long>(head) * out.lse_h + row;
+        const long long lse_base = static_cast<long long>(u.b) * out.lse_b + static_cast<long long>(head) * out.lse_h + out_row;
 
         float m_use = -INFINITY, l_sum = 0.f;
         bool ok = true;
@@ -1247,6 +1261,18 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
     if (!make_map(&tq, a.q, qd, qs, box) || !make_map(&tk, a.k, kd, ks, box) || !make_map(&tv, a.v, kd, ks, box))
         return cudaErrorInvalidValue;
     const int grid = p.n_qtiles * a.B * p.n_head_groups;
+    // A causal zigzag sequence with one output is the contiguous causal problem on
+    // its 2N chunks of L/2 tokens, each 128-row tile addressed through the chunk map:
+    // the contiguous ring over the 2N chunks visits the same tiles and masks only
+    // the diagonal one, in the contiguous variant's code (order changes rounding only).
+    if (a.causal && a.layout == kLayoutZigzag && !a.partials) {
+        p.layout = kLayoutContiguous;
+        p.n_shards = 2 * a.n_shards;
+        p.zz_n = a.n_shards;
+        p.zz_half = a.S / (2 * a.n_shards);
+        return a.D == 128 ? launch<128, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream)
+                          : launch<64, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream);
+    }
     // without a causal mask every layout is the same walk
     if (a.causal && a.layout != kLayoutContiguous)
         return a.partials ? (a.D == 128 ? launch<128, kModeRingLayoutPartials>(p, grid, tq, tk, tv, tk, tv, stream)
