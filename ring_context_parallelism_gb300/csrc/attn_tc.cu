@@ -141,7 +141,7 @@ __device__ __forceinline__ int zz_row(const TcParams& p, int pos) {
     return (c < p.zz_n ? 2 * c * p.zz_half : (4 * p.zz_n - 1 - 2 * c) * p.zz_half) + o;
 }
 
-template <bool FAN, bool LAY = false>
+template <bool FAN, bool LAY = false, bool STR = false>
 __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
     Unit u;
     u.valid = 1;
@@ -159,9 +159,10 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p) {
         const int qt_rev = rem / hg_per_kv;
         u.b = g / p.Hkv;
         const int hg = (g - u.b * p.Hkv) * hg_per_kv + (rem - qt_rev * hg_per_kv);
-        u.q_row0 = !p.causal ? qt_rev * kTileM
-                   : LAY     ? heavy_tile_row0(p.layout, p.S, p.n_shards, kTileM, qt_rev)
-                             : (p.n_qtiles - 1 - qt_rev) * kTileM;
+        u.q_row0 = !p.causal             ? qt_rev * kTileM
+                   : LAY                   ? heavy_tile_row0(p.layout, p.S, p.n_shards, kTileM, qt_rev)
+                   : STR                   ? heavy_tile_row0(kLayoutStriped, p.S, p.n_shards, kTileM, qt_rev)
+                                           : (p.n_qtiles - 1 - qt_rev) * kTileM;
         u.q_srow0 = LAY ? u.q_row0 : zz_row(p, u.q_row0);
         u.T = p.T2 ? 2 : 1;
         for (int t = 0; t < 2; ++t) {
@@ -424,7 +425,10 @@ struct StageCtr {
 // their KV tiles over the two tile slots (one row tile), all pair two row
 // tiles, or mix both (suffix units without a prefix).  The uniform fan-out
 // variants compile only their own issue and softmax paths.
-// kModeRingLayout: a causal ring walk over zigzag or striped shards.  The
+// A causal ring over zigzag shards runs the contiguous variant (its tiles
+// addressed through the layout's chunk map), one over striped shards its own
+// variant of the same code (kModeRingStriped); the per-shard partials over
+// either layout walk the layout's ring in kModeRingLayoutPartials.  The
 // fan-out modes over a paged KV pool (kModeFan*Paged) are the same three
 // fan-out variants with the producers' page-table path compiled in.  The ring
 // walks that write one partial per KV shard (kModeRing*Partials) are compiled
@@ -435,39 +439,38 @@ enum KernelMode : int {
     kModeFanMixed = 1,
     kModeFanSplit = 2,
     kModeFanPaired = 3,
-    kModeRingLayout = 4,
     kModeFanMixedPaged = 5,
     kModeFanSplitPaged = 6,
     kModeFanPairedPaged = 7,
     kModeRingPartials = 8,
-    kModeRingLayoutPartials = 9
+    kModeRingLayoutPartials = 9,
+    kModeRingStriped = 10
 };
 
 // Register split per warpgroup: the producer / MMA warpgroup's registers per
 // thread (dec) and the two softmax warpgroups' (inc), at most the launch's
 // 384 x 168 = 64512 in all.  ptxas's spill report moves erratically with the
 // split, so each kernel variant takes the split that measured fastest among
-// those with the fewest spilled bytes: the contiguous ring 64 / 216 (its
-// unrolled MMA loop spilled at 48), the zigzag / striped ring 144 / 176 (5.57
-// against 5.73 ms on the 32K zigzag prefill), the fan-out split and paired
+// those with the fewest spilled bytes: the contiguous and striped rings 64 / 216
+// (the unrolled MMA loop spilled at 48), the fan-out split and paired
 // variants 40 / 232 and 80 / 208 (3% faster than 56 / 224 on the R = 147
 // decode and the 8 x 20 prefill); the rest by the spill report alone.
 template <int MODE>
 struct RegSplit {
     static constexpr int dec = MODE == kModeRing                ? 64
+                               : MODE == kModeRingStriped        ? 64
                                : MODE == kModeFanMixed           ? 80
                                : MODE == kModeFanSplit           ? 40
                                : MODE == kModeFanPaired          ? 80
-                               : MODE == kModeRingLayout         ? 144
                                : MODE == kModeFanMixedPaged      ? 72
                                : MODE == kModeRingPartials       ? 64
                                : MODE == kModeRingLayoutPartials ? 48
                                                                  : 56;
     static constexpr int inc = MODE == kModeRing                ? 216
+                               : MODE == kModeRingStriped        ? 216
                                : MODE == kModeFanMixed           ? 208
                                : MODE == kModeFanSplit           ? 232
                                : MODE == kModeFanPaired          ? 208
-                               : MODE == kModeRingLayout         ? 176
                                : MODE == kModeFanMixedPaged      ? 216
                                : MODE == kModeRingPartials       ? 216
                                                                  : 224;
@@ -489,12 +492,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v2, const TcParams p) {
     using C = Cfg<D>;
     constexpr bool PART = MODE == kModeRingPartials || MODE == kModeRingLayoutPartials;  // one partial per KV shard
-    constexpr bool RING = MODE == kModeRing || MODE == kModeRingLayout || PART;
+    // causal striped shards with one output: the contiguous variant's code with the
+    // striped walk's per-shard tile counts and diagonal masks
+    constexpr bool STR = MODE == kModeRingStriped;
+    constexpr bool RING = MODE == kModeRing || PART || STR;
     constexpr bool FAN = !RING;
-    constexpr bool LAY = MODE == kModeRingLayout || MODE == kModeRingLayoutPartials;
+    constexpr bool LAY = MODE == kModeRingLayoutPartials;
     constexpr bool PG = MODE >= kModeFanMixedPaged && MODE <= kModeFanPairedPaged;  // paged KV pool
     constexpr int FMODE = PG ? MODE - kModeFanMixedPaged + kModeFanMixed : MODE;  // its unpaged fan-out mode
-    const Unit u = decode_unit<FAN, LAY>(p);
+    const Unit u = decode_unit<FAN, LAY, STR>(p);
     if (!u.valid) return;
     const bool split = FMODE == kModeFanSplit ? true : (RING || FMODE == kModeFanPaired) ? false : u.split != 0;
 
@@ -528,6 +534,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int total;
     if (!FAN) {
         w = make_ring_walk(p.S, p.n_shards, kTileN, p.causal, u.q_row0, kTileM, LAY ? p.layout : kLayoutContiguous);
+        if (STR) {
+            // the same walk as the striped layout's: each of the N shards, in ring
+            // order, up to the tile at the query tile's own in-shard index
+            const int n = (u.q_row0 - w.k * w.shard_len) / kTileN + 1;
+            w.first_tiles = w.tiles_per_shard = n;
+            w.n_visited = p.n_shards;
+            w.total = p.n_shards * n;
+        }
         total = w.total;
     } else {
         total = u.total;
@@ -775,10 +789,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr int kBlk = C::kBlk;
                 constexpr int nKc = C::kMaxKV, nVc = C::kNVPair;
                 uint32_t kflip = 0, vflip = 0;
-                // (contiguous ring prefill only: the fan-out and zigzag / striped variants
-                // measured slower with it -- their larger code missed the instruction
-                // cache: 3x the no-instruction stalls of the contiguous mode under ncu)
-                for (; (MODE == kModeRing || MODE == kModeRingPartials) && ok && i + kBlk <= total; i += kBlk) {
+                // (ring prefill variants only: the fan-out variants and the former
+                // layout-walk variant measured slower with it -- their larger code
+                // missed the instruction cache: 3x the no-instruction stalls of the
+                // contiguous mode under ncu)
+                for (; (MODE == kModeRing || MODE == kModeRingPartials || STR) && ok && i + kBlk <= total; i += kBlk) {
                     const uint32_t kb = k_lo0, vb = v_lo0, qa = q0, qb = q1;
 #pragma unroll
                     for (int pos = 0; pos < kBlk; ++pos) {
@@ -889,6 +904,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // sees are seen by every row, so whole tiles of them need no mask
         const int tile_minpos = LAY ? layout_pos(p.layout, shard_len, p.n_shards, FAN ? 0 : u.q_row0) : 0;
         int lay_full = 0;  // leading tiles of the current shard every row sees whole
+        const int shard_len_c = STR ? p.S / p.n_shards : 0;
+        const int q_shard = STR ? u.q_row0 / shard_len_c : 0;
 
         // Normalise the O accumulator and write it as part `part`, once `done`
         // (if given) shows its last PV complete.
@@ -974,8 +991,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (wi.ring.in >= lay_full)
                         lim = min(lim, shard_visible(p.layout, shard_len, p.n_shards, wi.ring.j, row_pos) -
                                            (tile_kb - wi.ring.j * shard_len) - 1);
-                } else if (p.causal)
-                    lim = min(lim, row - tile_kb);
+                } else if (p.causal) {
+                    // striped: key offset <= row offset in the query's shard and the
+                    // shards before it in the sequence, < in the shards after it
+                    lim = min(lim, STR ? row - tile_kb + (wi.ring.j - q_shard) * shard_len_c - (wi.ring.j > q_shard)
+                                       : row - tile_kb);
+                }
             } else {
                 lim = min(lim, wi.key_end - 1 - tile_kb);
                 // rows of another branch (a folded suffix) or past the stacked rows
@@ -1273,12 +1294,18 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
         return a.D == 128 ? launch<128, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream)
                           : launch<64, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream);
     }
+    // A causal striped sequence with one output: the layout's own ring walk, in a
+    // variant compiled from the contiguous one with its per-shard tile counts and
+    // diagonal masks.
+    if (a.causal && a.layout == kLayoutStriped && !a.partials) {
+        p.layout = kLayoutContiguous;
+        return a.D == 128 ? launch<128, kModeRingStriped>(p, grid, tq, tk, tv, tk, tv, stream)
+                          : launch<64, kModeRingStriped>(p, grid, tq, tk, tv, tk, tv, stream);
+    }
     // without a causal mask every layout is the same walk
     if (a.causal && a.layout != kLayoutContiguous)
-        return a.partials ? (a.D == 128 ? launch<128, kModeRingLayoutPartials>(p, grid, tq, tk, tv, tk, tv, stream)
-                                        : launch<64, kModeRingLayoutPartials>(p, grid, tq, tk, tv, tk, tv, stream))
-                          : (a.D == 128 ? launch<128, kModeRingLayout>(p, grid, tq, tk, tv, tk, tv, stream)
-                                        : launch<64, kModeRingLayout>(p, grid, tq, tk, tv, tk, tv, stream));
+        return a.D == 128 ? launch<128, kModeRingLayoutPartials>(p, grid, tq, tk, tv, tk, tv, stream)
+                          : launch<64, kModeRingLayoutPartials>(p, grid, tq, tk, tv, tk, tv, stream);
     p.layout = kLayoutContiguous;
     if (a.partials)
         return a.D == 128 ? launch<128, kModeRingPartials>(p, grid, tq, tk, tv, tk, tv, stream)
