@@ -77,7 +77,11 @@ struct BwdCfg {
 
 struct BwdParams {
     int B, S, Hq, Hkv, n_shards, causal, G, n_tiles;
-    int layout;        // shard layout of the rows (ra_walk.h); the LAY kernels run causal zigzag / striped
+    int layout;        // shard layout of the rows (ra_walk.h); the LAY kernels run causal striped
+    // causal zigzag in the contiguous kernels: the walk runs over sequence positions
+    // (2 zz_n chunks of zz_half tokens as the shards) and every tile's rows are
+    // addressed through the chunk map (zz_half = 0: rows are positions)
+    int zz_n, zz_half;
     float scale_log2;  // log2(e) / sqrt(D)
     float scale;       // 1 / sqrt(D)
     const float* delta;
@@ -255,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const RingWalk w = make_ring_walk(p.S, p.n_shards, kT, p.causal, q0, kT, LAY ? p.layout : kLayoutContiguous);
     const int total = w.total;
+    const int q0s = zigzag_row(p.zz_n, p.zz_half, q0);  // storage row of the query tile
 
     if (threadIdx.x == 0) {
         mbar_init(qd_full, 1);
@@ -298,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&tm_q);
                 tma_prefetch_desc(&tm_do);
                 mbar_arrive_expect_tx(qd_full, 2 * C::kTileBytes);
-                load_tile<D>(&tm_q, qd_full, q_smem, h, q0, b);
-                load_tile<D>(&tm_do, qd_full, do_smem, h, q0, b);
+                load_tile<D>(&tm_q, qd_full, q_smem, h, q0s, b);
+                load_tile<D>(&tm_do, qd_full, do_smem, h, q0s, b);
             }
             RingIterT<LAY> it;
             it.start(w);
@@ -309,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&empty[st.s], st.ph ^ 1, abort_flag, status, 0x11000000u | (2 * i + (is_k ? 0 : 1))))
                     break;
                 mbar_arrive_expect_tx(&full[st.s], C::kTileBytes);
-                load_tile<D>(map, &full[st.s], ring + st.s * C::kTileBytes, hk, it.kb, b);
+                load_tile<D>(map, &full[st.s], ring + st.s * C::kTileBytes, hk, zigzag_row(p.zz_n, p.zz_half, it.kb),
+                             b);
                 st.next(ns);
                 ++issued;
             }
@@ -373,7 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q0 + lane_row;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS0 = tmem_base + lane_off, tS1 = tS0 + 384, tdP = tS0 + 128, tdQ = tS0 + 256;
-        const long long vrow = (static_cast<long long>(b) * p.Hq + h) * p.S + row;
+        const int srow = q0s + lane_row;  // storage row
+        const long long vrow = (static_cast<long long>(b) * p.Hq + h) * p.S + srow;
         const float lse2_r = p.lse2[vrow];
         const float delta_r = p.delta[vrow];
         const float sl2 = p.scale_log2;
@@ -451,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && mbar_wait(dq_done, 0, abort_flag, status, 0x17000000u)) {
             tc_fence_after();
-            const long long off = ((static_cast<long long>(b) * p.S + row) * p.Hq + h) * D + hw * (D / 2);
+            const long long off = ((static_cast<long long>(b) * p.S + srow) * p.Hq + h) * D + hw * (D / 2);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t r[32];
@@ -587,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int k0 = LAY ? heavy_tile_row0(p.layout, p.S, p.n_shards, kT, p.n_tiles - 1 - x) : x * kT;
     const int L = p.S / p.n_shards, tps = L / kT;
     const int j = k0 / L, x_in = (k0 - j * L) / kT;
+    const int k0s = zigzag_row(p.zz_n, p.zz_half, k0);  // storage row of the key tile
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -665,8 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&tm_k);
                 tma_prefetch_desc(&tm_v);
                 mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
-                load_tile<D>(&tm_k, kv_full, k_smem, hk, k0, b);
-                load_tile<D>(&tm_v, kv_full, v_smem, hk, k0, b);
+                load_tile<D>(&tm_k, kv_full, k_smem, hk, k0s, b);
+                load_tile<D>(&tm_v, kv_full, v_smem, hk, k0s, b);
             }
             Walk it = qw;
             Stage st;
@@ -674,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < total; ++u, it.next()) {
                 if (!mbar_wait(&empty[st.s], st.ph ^ 1, abort_flag, status, 0x21000000u | (2 * u + (is_q ? 0 : 1))))
                     break;
-                const int q0 = it.a * L + it.qt * kT, h = hk * p.G + it.g;
+                const int q0 = zigzag_row(p.zz_n, p.zz_half, it.a * L + it.qt * kT), h = hk * p.G + it.g;
                 if constexpr (LAY) {
                     if (is_q) stage_info[st.s] = make_int2(it.col_lo_shard(), it.qt * kT);
                 }
@@ -849,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && mbar_wait(done, 0, abort_flag, status, 0x28000000u)) {
             tc_fence_after();
-            const long long off = ((static_cast<long long>(b) * p.S + key) * p.Hkv + hk) * D + hw * (D / 2);
+            const long long off = ((static_cast<long long>(b) * p.S + k0s + lane_row) * p.Hkv + hk) * D + hw * (D / 2);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t r[32];
@@ -1103,7 +1111,7 @@ __global__ void __launch_bounds__(kSimtRows * (D / 32)) bwd_dkdv_simt_kernel(con
 cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t stream) {
     cudaError_t e = launch_prep<__nv_bfloat16>(a, stream);
     if (e != cudaSuccess) return e;
-    const BwdParams p = make_params(a, 0, kT);
+    BwdParams p = make_params(a, 0, kT);
     const unsigned long long D = a.D, esz = 2;
     const unsigned long long qd[4] = {D, (unsigned long long)a.Hq, (unsigned long long)a.S, (unsigned long long)a.B};
     const unsigned long long qs[3] = {D * esz, D * esz * a.Hq, D * esz * a.Hq * a.S};
@@ -1114,8 +1122,18 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t stream) {
     if (!make_map(&tq, a.q, qd, qs, box) || !make_map(&tdo, a.dout, qd, qs, box) || !make_map(&tk, a.k, kd, ks, box) ||
         !make_map(&tv, a.v, kd, ks, box))
         return cudaErrorInvalidValue;
+    // A causal zigzag sequence is the contiguous causal problem on the 2N chunks of
+    // its cut, each 128-row tile addressed through the chunk map: the contiguous
+    // kernels walk the same tiles (in the ring over the 2N chunks; order changes
+    // rounding only).
+    if (a.causal && a.layout == kLayoutZigzag) {
+        p.layout = kLayoutContiguous;
+        p.n_shards = 2 * a.n_shards;
+        p.zz_n = a.n_shards;
+        p.zz_half = a.S / (2 * a.n_shards);
+    }
     // without a causal mask every layout is the same walk
-    if (a.causal && a.layout != kLayoutContiguous)
+    if (a.causal && p.layout != kLayoutContiguous)
         return a.D == 128 ? launch_tc<128, true>(p, tq, tdo, tk, tv, stream)
                           : launch_tc<64, true>(p, tq, tdo, tk, tv, stream);
     return a.D == 128 ? launch_tc<128, false>(p, tq, tdo, tk, tv, stream)

@@ -135,11 +135,7 @@ struct Unit {
 };
 
 // Storage row of sequence position pos (tile-aligned runs stay inside one chunk).
-__device__ __forceinline__ int zz_row(const TcParams& p, int pos) {
-    if (p.zz_half == 0) return pos;
-    const int c = pos / p.zz_half, o = pos - c * p.zz_half;
-    return (c < p.zz_n ? 2 * c * p.zz_half : (4 * p.zz_n - 1 - 2 * c) * p.zz_half) + o;
-}
+__device__ __forceinline__ int zz_row(const TcParams& p, int pos) { return zigzag_row(p.zz_n, p.zz_half, pos); }
 
 template <bool FAN, bool LAY = false, bool STR = false>
 __device__ __forceinline__ Unit decode_unit(const TcParams& p) {

@@ -59,6 +59,16 @@ RA_HD int shard_visible(int layout, int L, int n_shards, int j, int pos) {
     return clampi(pos + 1 - j * L, 0, L);
 }
 
+// Storage row of sequence position pos in a zigzag-stored sequence of n_shards
+// shards, cut into 2 n_shards chunks of `half` tokens: chunk c is the first half
+// of shard c (c < n_shards) or the second half of shard 2 n_shards - 1 - c.  The
+// inverse of layout_pos for the zigzag layout; half = 0 means rows are positions.
+RA_HD int zigzag_row(int n_shards, int half, int pos) {
+    if (half == 0) return pos;
+    const int c = pos / half, o = pos - c * half;
+    return (c < n_shards ? 2 * c * half : (4 * n_shards - 1 - 2 * c) * half) + o;
+}
+
 struct RingWalk {
     int n_shards;     // N
     int shard_len;    // L = S / N
