@@ -100,10 +100,14 @@ ra_status ra_blockwise_attn_fwd(const void* q, const void* k, const void* v, voi
 /*
  * ra_blockwise_attn_fwd for rows stored in a zigzag or striped shard layout
  * (ra_layout above; same page, section 5).  q/k/v/out/lse are indexed by
- * storage row; the causal mask compares the rows' sequence positions.  Each
- * query tile walks the KV shards in the same ring order, taking from each
- * shard the prefix of its rows that the tile can see (positions increase
- * along a shard's rows in every layout).
+ * storage row; the causal mask compares the rows' sequence positions.
+ * Striped: each query tile walks the KV shards in the same ring order, taking
+ * from each shard the prefix of its rows that the tile can see (positions
+ * increase along a shard's rows in every layout).  Zigzag: the causal walk
+ * runs in sequence-position order over the 2 n_shards chunks of the zigzag
+ * cut (the query's own chunk, then the earlier ones: the contiguous ring over
+ * those chunks), each tile of rows addressed through the layout; it visits the
+ * same keys, and the order changes rounding only.
  *   layout : an ra_layout value.  RA_LAYOUT_ZIGZAG needs an even shard length,
  *            and (S / n_shards / 2) % 128 == 0 on the bf16 path, % 32 == 0 on
  *            the fp32 path.
@@ -178,7 +182,9 @@ ra_status ra_blockwise_attn_bwd(const void* q, const void* k, const void* v, con
  * positions.  The dQ walk takes from each KV shard the prefix of its rows a
  * query tile can see (as the forward); the dK/dV walk takes from each query
  * shard the suffix of its rows that can see a KV tile (positions increase
- * along a shard's rows in every layout).  Other arguments, rules and errors
+ * along a shard's rows in every layout).  A causal zigzag sequence is walked,
+ * as in the forward, over the 2 n_shards chunks of its cut in sequence-position
+ * order (rounding differs only).  Other arguments, rules and errors
  * as ra_blockwise_attn_bwd and ra_blockwise_attn_fwd_layout.
  */
 ra_status ra_blockwise_attn_bwd_layout(const void* q, const void* k, const void* v, const void* out,
@@ -383,7 +389,10 @@ int ra_tile_launch_order(int S, int n_shards, int layout, int tile_rows, int* ro
  * it), KV tiles of `tile` keys.  Writes, for each visited shard in ring order,
  * shard_order[t] and visible_keys[t] (the keys of that shard the tile's last
  * row can see, a prefix of the shard's rows; the shard length when not
- * causal), and *total_tiles = the KV tiles the kernels walk for this tile.
+ * causal), and *total_tiles = the KV tiles the kernels walk for this tile
+ * (the zigzag forward and backward take the same tiles in the order of the
+ * 2 n_shards chunks, i.e. this call with RA_LAYOUT_CONTIGUOUS and
+ * 2 n_shards shards on sequence positions).
  * Shards after the returned count see nothing.  Arrays hold n_shards ints.
  * Returns the number of visited shards, or -1 on invalid arguments.
  */

@@ -104,6 +104,30 @@ def test_walk_visits_the_visible_prefix_of_each_shard(lib, layout, causal):
             assert total == sum(math.ceil(x / tile) for x in keys)
 
 
+@pytest.mark.parametrize("N,S,tile", [(2, 32, 4), (4, 64, 8), (3, 48, 8), (8, 256, 16), (8, 32768, 128)])
+def test_zigzag_position_walk_takes_the_layout_walk_tiles(lib, N, S, tile):
+    """The causal zigzag kernels walk sequence positions over the 2N chunks of the cut
+    (the contiguous ring with 2N shards), addressing each tile through the layout: every
+    storage tile is `tile` consecutive positions, and for every query tile that walk
+    takes as many tiles as the zigzag layout's own ring walk and covers exactly the key
+    positions the tile can see."""
+    pos = ra.layout_positions(S, N, "zigzag")
+    H = S // (2 * N)
+    for r0 in range(0, S, tile):
+        p = pos[r0:r0 + tile]
+        assert p == list(range(p[0], p[0] + tile)) and p[0] % tile == 0
+    for r0 in range(0, S, tile):
+        P0 = pos[r0]
+        order_z, keys_z, total_z = ra.ring_walk(S, N, True, "zigzag", r0, tile, tile)
+        order_c, keys_c, total_c = ra.ring_walk(S, 2 * N, True, "contiguous", P0, tile, tile)
+        assert total_c == total_z
+        assert order_c == [P0 // H - t for t in range(P0 // H + 1)]   # own chunk, then the earlier ones
+        # key positions covered: the query's own chunk up to the tile's last row, the earlier chunks
+        # whole, i.e. exactly the positions 0 .. P0 + tile - 1
+        c0 = P0 // H
+        assert keys_c == [P0 + tile - c0 * H] + [H] * c0
+
+
 def _step_work(S, N, layout):
     """work[a][t]: visible (query, key) pairs between query shard a and the KV
     shard it holds at ring step t, counted from the walk of every single row."""
