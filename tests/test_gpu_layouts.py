@@ -64,6 +64,8 @@ CASES = [
     (1, 4096, 4, 2, 64, 8, 128, True, "zigzag"),      # D = 64, long walks through the unrolled issue block
     (1, 3072, 2, 1, 128, 6, 128, True, "zigzag"),     # 6 shards of 512: one tile per chunk
     (1, 1024, 4, 2, 128, 4, 128, False, "zigzag"),    # no mask: the layout changes nothing
+    (2, 2048, 6, 2, 128, 4, 128, True, "zigzag"),     # two batches, odd GQA group: one head per CTA
+    (2, 2048, 6, 2, 64, 2, 64, True, "striped"),      # the same for striped, D = 64, block 64
 ]
 
 
