@@ -422,9 +422,11 @@ struct StageCtr {
 // tiles, or mix both (suffix units without a prefix).  The uniform fan-out
 // variants compile only their own issue and softmax paths.
 // A causal ring over zigzag shards runs the contiguous variant (its tiles
-// addressed through the layout's chunk map), one over striped shards its own
-// variant of the same code (kModeRingStriped); the per-shard partials over
-// either layout walk the layout's ring in kModeRingLayoutPartials.  The
+// addressed through the layout's chunk map), one over striped shards the
+// contiguous walk over positions with tiles gathered by 5-D boxes
+// (kModeRingStripedPos; N dividing 128) or else the layout's ring
+// (kModeRingStriped); the per-shard partials over either layout walk the
+// layout's ring in kModeRingLayoutPartials.  The
 // fan-out modes over a paged KV pool (kModeFan*Paged) are the same three
 // fan-out variants with the producers' page-table path compiled in.  The ring
 // walks that write one partial per KV shard (kModeRing*Partials) are compiled
@@ -440,7 +442,8 @@ enum KernelMode : int {
     kModeFanPairedPaged = 7,
     kModeRingPartials = 8,
     kModeRingLayoutPartials = 9,
-    kModeRingStriped = 10
+    kModeRingStriped = 10,
+    kModeRingStripedPos = 11
 };
 
 // Register split per warpgroup: the producer / MMA warpgroup's registers per
@@ -455,6 +458,7 @@ template <int MODE>
 struct RegSplit {
     static constexpr int dec = MODE == kModeRing                ? 64
                                : MODE == kModeRingStriped        ? 64
+                               : MODE == kModeRingStripedPos     ? 64
                                : MODE == kModeFanMixed           ? 80
                                : MODE == kModeFanSplit           ? 40
                                : MODE == kModeFanPaired          ? 80
@@ -464,6 +468,7 @@ struct RegSplit {
                                                                  : 56;
     static constexpr int inc = MODE == kModeRing                ? 216
                                : MODE == kModeRingStriped        ? 216
+                               : MODE == kModeRingStripedPos     ? 216
                                : MODE == kModeFanMixed           ? 208
                                : MODE == kModeFanSplit           ? 232
                                : MODE == kModeFanPaired          ? 208
@@ -491,13 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // causal striped shards with one output: the contiguous variant's code with the
     // striped walk's per-shard tile counts and diagonal masks
     constexpr bool STR = MODE == kModeRingStriped;
-    constexpr bool RING = MODE == kModeRing || PART || STR;
+    // causal striped shards with one output, N dividing 128: the contiguous causal walk over
+    // sequence positions, every 128-position tile gathered by one 5-D TMA box per 64
+    // columns (shard index the faster box dimension, so rows land in position order)
+    constexpr bool SPOS = MODE == kModeRingStripedPos;
+    constexpr bool RING = MODE == kModeRing || PART || STR || SPOS;
     constexpr bool FAN = !RING;
     constexpr bool LAY = MODE == kModeRingLayoutPartials;
     // single-output ring variants: the Unit's per-slot arrays indexed with constants
     // only (a runtime index keeps the Unit in local memory; the ring prefill measured
     // 0.6-1.3% faster without, the fan-out variants 2-7% slower, so they keep it)
-    constexpr bool CSEL = MODE == kModeRing || STR;
+    constexpr bool CSEL = MODE == kModeRing || STR || SPOS;
     constexpr bool PG = MODE >= kModeFanMixedPaged && MODE <= kModeFanPairedPaged;  // paged KV pool
     constexpr int FMODE = PG ? MODE - kModeFanMixedPaged + kModeFanMixed : MODE;  // its unpaged fan-out mode
     const Unit u = decode_unit<FAN, LAY, STR>(p);
@@ -609,7 +618,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (is_k && lead) {
                 tma_prefetch_desc(&tm_q);
                 mbar_arrive_expect_tx(q_full, u.n_q * C::kTileBytes);
-                if (CSEL) {
+                if (SPOS) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+                        if (t < u.n_q)
+                            for (int c = 0; c < C::kChunks; ++c)
+                                tma_load_5d(&tm_q, q_full, q_smem + t * C::kTileBytes + c * 16384, c * 64,
+                                            u.qc1[t], 0, u.q_row0 / p.n_shards, u.qc3[t]);
+                } else if (CSEL) {
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
                         if (t < u.n_q)
@@ -676,6 +692,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_4d(map, &full[cs.s], ring + cs.s * C::kTileBytes + c * 16384 + r0 * 128, c * 64,
                                     u.kv_head, row, 0);
                     }
+                } else if (SPOS) {
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_5d(map, &full[cs.s], ring + cs.s * C::kTileBytes + c * 16384, c * 64, u.kv_head, 0,
+                                    wi.key() / p.n_shards, z);
                 } else {
                     for (int c = 0; c < C::kChunks; ++c)
                         tma_load_4d(map, &full[cs.s], ring + cs.s * C::kTileBytes + c * 16384, c * 64, u.kv_head,
@@ -802,7 +822,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // layout-walk variant measured slower with it -- their larger code
                 // missed the instruction cache: 3x the no-instruction stalls of the
                 // contiguous mode under ncu)
-                for (; (MODE == kModeRing || MODE == kModeRingPartials || STR) && ok && i + kBlk <= total; i += kBlk) {
+                for (; (MODE == kModeRing || MODE == kModeRingPartials || STR || SPOS) && ok && i + kBlk <= total;
+                     i += kBlk) {
                     const uint32_t kb = k_lo0, vb = v_lo0, qa = q0, qb = q1;
 #pragma unroll
                     for (int pos = 0; pos < kBlk; ++pos) {
@@ -899,7 +920,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             row_ok = row < u.row_hi;
         }
         const OutDesc& out = p.out;
-        const int out_row = FAN ? row : u.q_srow0 + lane_row;  // storage row of the output
+        // storage row of the output (striped over positions: position i sits in shard i mod N
+        // at row i / N)
+        const int out_row = FAN    ? row
+                            : SPOS ? (row % p.n_shards) * (p.S / p.n_shards) + row / p.n_shards
+                                   : u.q_srow0 + lane_row;
         const long long o_row_base = static_cast<long long>(u.b) * out.o_b + static_cast<long long>(out_row) * out.o_row +
                                      static_cast<long long>(head) * out.o_h;
         const long long lse_base = static_cast<long long>(u.b) * out.lse_b + static_cast<long long>(head) * out.lse_h + out_row;
@@ -1252,19 +1277,30 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// bf16 tensor map of `rank` (4 or 5) dims, innermost first, strides in bytes for
+// dims 1.., box (64, b1, ...), 128-byte swizzle.
+static bool make_map_nd(CUtensorMap* m, const void* base, int rank, const unsigned long long* dims,
+                        const unsigned long long* strides, const unsigned* box) {
+    auto fn = encode_fn();
+    if (!fn || rank < 1 || rank > 5) return false;
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i > 0) gs[i - 1] = strides[i - 1];
+    }
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bx, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 4-D bf16 tensor map, dims innermost first, strides in bytes for dims 1..3,
 // box (64, b1, b2, b3), 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, const unsigned long long dims[4], const unsigned long long strides[3],
               const unsigned box[4]) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
-    cuuint64_t gs[3] = {strides[0], strides[1], strides[2]};
-    cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gd, gs, bx, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return make_map_nd(m, base, 4, dims, strides, box);
 }
 
 cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
@@ -1304,11 +1340,30 @@ cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {
         return a.D == 128 ? launch<128, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream)
                           : launch<64, kModeRing>(p, grid, tq, tk, tv, tk, tv, stream);
     }
-    // A causal striped sequence with one output: the layout's own ring walk, in a
-    // variant compiled from the contiguous one with its per-shard tile counts and
-    // diagonal masks.
+    // A causal striped sequence with one output: over positions (below) when N divides
+    // 128, otherwise the layout's own ring walk, in a variant compiled from the contiguous
+    // one with its per-shard tile counts and diagonal masks.
     if (a.causal && a.layout == kLayoutStriped && !a.partials) {
         p.layout = kLayoutContiguous;
+        if (128 % a.n_shards == 0) {
+            // N dividing 128: a tile of 128 consecutive positions holds 128/N rows of every
+            // shard, one 5-D box [64 cols, 1 head, N shards, 128/N rows, 1 batch] per 64
+            // columns (the shard the faster box dimension: rows land in position order), and
+            // the contiguous causal walk runs over positions (N position-order shards of L
+            // tokens; the same visible keys, one diagonal tile per query tile)
+            const unsigned long long L = a.S / a.n_shards, N = a.n_shards, S = a.S, B = a.B;
+            const unsigned long long qd5[5] = {D, (unsigned long long)a.Hq, N, L, B};
+            const unsigned long long qs5[4] = {D * esz, L * a.Hq * D * esz, a.Hq * D * esz, S * a.Hq * D * esz};
+            const unsigned long long kd5[5] = {D, (unsigned long long)a.Hkv, N, L, B};
+            const unsigned long long ks5[4] = {D * esz, L * a.Hkv * D * esz, a.Hkv * D * esz, S * a.Hkv * D * esz};
+            const unsigned box5[5] = {64, 1, (unsigned)N, (unsigned)(128 / N), 1};
+            CUtensorMap tq5, tk5, tv5;
+            if (!make_map_nd(&tq5, a.q, 5, qd5, qs5, box5) || !make_map_nd(&tk5, a.k, 5, kd5, ks5, box5) ||
+                !make_map_nd(&tv5, a.v, 5, kd5, ks5, box5))
+                return cudaErrorInvalidValue;
+            return a.D == 128 ? launch<128, kModeRingStripedPos>(p, grid, tq5, tk5, tv5, tk5, tv5, stream)
+                              : launch<64, kModeRingStripedPos>(p, grid, tq5, tk5, tv5, tk5, tv5, stream);
+        }
         return a.D == 128 ? launch<128, kModeRingStriped>(p, grid, tq, tk, tv, tk, tv, stream)
                           : launch<64, kModeRingStriped>(p, grid, tq, tk, tv, tk, tv, stream);
     }
