@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, valid only while the kernel source hashes to the recorded value.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the timed 32768-token configuration
-    # (bench.py --profile-case prefill_32k, third launch): 404549632 read + 237947648 written
-    "a30ba7208807bf8b": 642497280,
+    # (bench.py --profile-case prefill_32k, third launch): 403617792 read + 238159872 written
+    "65b249db36d9ca01": 641777664,
 }
 
 
