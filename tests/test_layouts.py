@@ -128,6 +128,22 @@ def test_zigzag_position_walk_takes_the_layout_walk_tiles(lib, N, S, tile):
         assert keys_c == [P0 + tile - c0 * H] + [H] * c0
 
 
+@pytest.mark.parametrize("N,S", [(1, 1024), (2, 1024), (4, 2048), (8, 32768), (16, 4096), (128, 16384)])
+def test_striped_position_tile_is_one_box(lib, N, S):
+    """The causal striped kernel (N dividing 128) reads the 128 consecutive positions
+    [P, P + 128) as one box over (shard j, row t) with rows P/N + t of every shard, the
+    shard the faster dimension: box element t*N + j must be the storage row holding
+    position P + t*N + j, i.e. the box lands the tile in position order, and the output
+    row of position i is (i mod N) * L + i / N."""
+    pos = ra.layout_positions(S, N, "striped")
+    L = S // N
+    for P in range(0, S, 128):
+        rows = [j * L + P // N + t for t in range(128 // N) for j in range(N)]
+        assert [pos[r] for r in rows] == list(range(P, P + 128))
+    inv = {p: r for r, p in enumerate(pos)}
+    assert all(inv[i] == (i % N) * L + i // N for i in range(S))
+
+
 def _step_work(S, N, layout):
     """work[a][t]: visible (query, key) pairs between query shard a and the KV
     shard it holds at ring step t, counted from the walk of every single row."""
