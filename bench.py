@@ -9,7 +9,7 @@ TFLOP/s (4*D FLOPs per unmasked query/key pair), `e2e` the same call with the
 inputs copied from pinned host memory and the results read back every step.
 The same line carries the other rows measured on their own workloads: the
 headline workload in the zigzag and striped shard layouts, its backward pass
-(contiguous and zigzag), shared-prefix fan-out decode (HBM GB/s; contiguous and
+(contiguous, zigzag and striped), shared-prefix fan-out decode (HBM GB/s; contiguous and
 over a paged KV pool), fan-out prefill (8 branches x 20 rows), per-shard
 partials + LSE merge on the Llama-3-70B-shaped layer, and the million-token
 stress case.
@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, valid only while the kernel source hashes to the recorded value.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the timed 32768-token configuration
-    # (bench.py --profile-case prefill_32k, third launch): 403617792 read + 238159872 written
-    "65b249db36d9ca01": 641777664,
+    # (bench.py --profile-case prefill_32k, third launch): 403008512 read + 237972736 written
+    "b5ed574b6f1cc6fc": 640981248,
 }
 
 
@@ -329,14 +329,15 @@ def run_ours(args, rank, world):
                               "flop_convention": "2.5x the forward's causal-adjusted FLOPs (5 GEMMs); the kernels "
                                                  "execute 7 (dQ recomputes S and dP)",
                               "launches_per_call": 3}
-        # the backward over the zigzag layout (same data in storage order, causal on positions)
-        ra.attn(q, k, v, w.n_shards, w.block, w.causal, out=out, lse=lse, layout="zigzag")
-        zms = timed_steps(lambda: ra.attn_bwd(q, k, v, out, lse, dO, w.n_shards, w.block, w.causal, dq, dk, dv, bws,
-                                              layout="zigzag"), min(args.steps, 10), 3, flush)
-        ra.device_status()
-        tz = statistics.median(zms) * 1e-3
-        result["backward"]["zigzag"] = {"ms": tz * 1e3, "TFLOP_per_s": bflops / tz / 1e12,
-                                        "frac_bf16_peak": bflops / tz / 1e12 / pk["bf16_tflops"]}
+        # the backward over the zigzag and striped layouts (same data in storage order, causal on positions)
+        for lay in ("zigzag", "striped"):
+            ra.attn(q, k, v, w.n_shards, w.block, w.causal, out=out, lse=lse, layout=lay)
+            zms = timed_steps(lambda: ra.attn_bwd(q, k, v, out, lse, dO, w.n_shards, w.block, w.causal, dq, dk, dv,
+                                                  bws, layout=lay), min(args.steps, 10), 3, flush)
+            ra.device_status()
+            tz = statistics.median(zms) * 1e-3
+            result["backward"][lay] = {"ms": tz * 1e3, "TFLOP_per_s": bflops / tz / 1e12,
+                                       "frac_bf16_peak": bflops / tz / 1e12 / pk["bf16_tflops"]}
         del dO, dq, dk, dv, bws
 
         # e2e through the public API with host buffers.  Every step copies its inputs from pinned

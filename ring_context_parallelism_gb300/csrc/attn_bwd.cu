@@ -82,6 +82,10 @@ struct BwdParams {
     // (2 zz_n chunks of zz_half tokens as the shards) and every tile's rows are
     // addressed through the chunk map (zz_half = 0: rows are positions)
     int zz_n, zz_half;
+    // causal striped in the SP kernels (N = st_n dividing 128): the contiguous walk over
+    // positions, 128-position tiles gathered by 5-D boxes, lse2 / Delta in position order,
+    // output row of position i at (i mod N) L + i / N
+    int st_n;
     float scale_log2;  // log2(e) / sqrt(D)
     float scale;       // 1 / sqrt(D)
     const float* delta;
@@ -100,7 +104,7 @@ __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float
 // are consecutive.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* out, const T* dout, const float* lse, float* delta,
-                                                      float* lse2, long long rows, int S, int Hq) {
+                                                      float* lse2, long long rows, int S, int Hq, int st_n) {
     const long long w = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= rows) return;
@@ -118,8 +122,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* out, const T* do
 #pragma unroll
     for (int x = 16; x > 0; x >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
     if (lane == 0) {
-        delta[w] = acc;
-        lse2[w] = lse[w] * kLog2e;
+        // striped rows walked over positions: Delta and lse2 stored at the row's position
+        const long long wo = st_n ? w - i + (i % (S / st_n)) * st_n + i / (S / st_n) : w;
+        delta[wo] = acc;
+        lse2[wo] = lse[w] * kLog2e;
     }
 }
 
@@ -166,6 +172,19 @@ __device__ __forceinline__ void load_tile(const CUtensorMap* map, uint64_t* bar,
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) tma_load_4d(map, bar, dst + c * 16384, c * 64, head, row0, b);
 }
+
+// The 128 positions [pos0, pos0 + 128) of a striped sequence of n shards (n
+// dividing 128): rows pos0/n .. pos0/n + 128/n - 1 of every shard, one 5-D box per
+// 64 columns with the shard the faster box dimension, so the rows land in position order.
+template <int D>
+__device__ __forceinline__ void load_tile_pos(const CUtensorMap* map, uint64_t* bar, uint8_t* dst, int head, int pos0,
+                                              int b, int n) {
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) tma_load_5d(map, bar, dst + c * 16384, c * 64, head, 0, pos0 / n, b);
+}
+
+// Storage row of position i in a striped sequence of n shards of len rows.
+__device__ __forceinline__ int striped_row(int i, int n, int len) { return (i % n) * len + i / n; }
 
 struct Stage {
     int s = 0, ph = 0;
@@ -217,7 +236,7 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int issued, int n_sta
 // ---------------------------------------------------------------------------
 // dQ: query-tile outer, KV tiles in ring order
 // ---------------------------------------------------------------------------
-template <int D, bool LAY>
+template <int D, bool LAY, bool SP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -303,8 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&tm_q);
                 tma_prefetch_desc(&tm_do);
                 mbar_arrive_expect_tx(qd_full, 2 * C::kTileBytes);
-                load_tile<D>(&tm_q, qd_full, q_smem, h, q0s, b);
-                load_tile<D>(&tm_do, qd_full, do_smem, h, q0s, b);
+                if (SP) {
+                    load_tile_pos<D>(&tm_q, qd_full, q_smem, h, q0, b, p.st_n);
+                    load_tile_pos<D>(&tm_do, qd_full, do_smem, h, q0, b, p.st_n);
+                } else {
+                    load_tile<D>(&tm_q, qd_full, q_smem, h, q0s, b);
+                    load_tile<D>(&tm_do, qd_full, do_smem, h, q0s, b);
+                }
             }
             RingIterT<LAY> it;
             it.start(w);
@@ -314,8 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&empty[st.s], st.ph ^ 1, abort_flag, status, 0x11000000u | (2 * i + (is_k ? 0 : 1))))
                     break;
                 mbar_arrive_expect_tx(&full[st.s], C::kTileBytes);
-                load_tile<D>(map, &full[st.s], ring + st.s * C::kTileBytes, hk, zigzag_row(p.zz_n, p.zz_half, it.kb),
-                             b);
+                if (SP)
+                    load_tile_pos<D>(map, &full[st.s], ring + st.s * C::kTileBytes, hk, it.kb, b, p.st_n);
+                else
+                    load_tile<D>(map, &full[st.s], ring + st.s * C::kTileBytes, hk,
+                                 zigzag_row(p.zz_n, p.zz_half, it.kb), b);
                 st.next(ns);
                 ++issued;
             }
@@ -379,8 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q0 + lane_row;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS0 = tmem_base + lane_off, tS1 = tS0 + 384, tdP = tS0 + 128, tdQ = tS0 + 256;
-        const int srow = q0s + lane_row;  // storage row
-        const long long vrow = (static_cast<long long>(b) * p.Hq + h) * p.S + srow;
+        const int srow = SP ? striped_row(row, p.st_n, p.S / p.st_n) : q0s + lane_row;  // storage row
+        // lse2 / Delta: by storage row, or by position in the SP kernels
+        const long long vrow = (static_cast<long long>(b) * p.Hq + h) * p.S + (SP ? row : srow);
         const float lse2_r = p.lse2[vrow];
         const float delta_r = p.delta[vrow];
         const float sl2 = p.scale_log2;
@@ -578,7 +606,7 @@ struct QWalkL {
     __device__ __forceinline__ int col_lo_shard() const { return qt >= full ? -1 : a; }
 };
 
-template <int D, bool LAY>
+template <int D, bool LAY, bool SP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -673,8 +701,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&tm_k);
                 tma_prefetch_desc(&tm_v);
                 mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
-                load_tile<D>(&tm_k, kv_full, k_smem, hk, k0s, b);
-                load_tile<D>(&tm_v, kv_full, v_smem, hk, k0s, b);
+                if (SP) {
+                    load_tile_pos<D>(&tm_k, kv_full, k_smem, hk, k0, b, p.st_n);
+                    load_tile_pos<D>(&tm_v, kv_full, v_smem, hk, k0, b, p.st_n);
+                } else {
+                    load_tile<D>(&tm_k, kv_full, k_smem, hk, k0s, b);
+                    load_tile<D>(&tm_v, kv_full, v_smem, hk, k0s, b);
+                }
             }
             Walk it = qw;
             Stage st;
@@ -682,12 +715,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < total; ++u, it.next()) {
                 if (!mbar_wait(&empty[st.s], st.ph ^ 1, abort_flag, status, 0x21000000u | (2 * u + (is_q ? 0 : 1))))
                     break;
-                const int q0 = zigzag_row(p.zz_n, p.zz_half, it.a * L + it.qt * kT), h = hk * p.G + it.g;
+                // first row of the query tile: its storage row, or its position in the SP kernels
+                const int q0 = SP ? it.a * L + it.qt * kT : zigzag_row(p.zz_n, p.zz_half, it.a * L + it.qt * kT);
+                const int h = hk * p.G + it.g;
                 if constexpr (LAY) {
                     if (is_q) stage_info[st.s] = make_int2(it.col_lo_shard(), it.qt * kT);
                 }
                 mbar_arrive_expect_tx(&full[st.s], C::kTileBytes + (is_q ? 1024 : 0));
-                load_tile<D>(map, &full[st.s], ring + st.s * C::kTileBytes, h, q0, b);
+                if (SP)
+                    load_tile_pos<D>(map, &full[st.s], ring + st.s * C::kTileBytes, h, q0, b, p.st_n);
+                else
+                    load_tile<D>(map, &full[st.s], ring + st.s * C::kTileBytes, h, q0, b);
                 if (is_q) {
                     const long long vrow = (static_cast<long long>(b) * p.Hq + h) * p.S + q0;
                     bulk_load(vec + st.s * 256, p.lse2 + vrow, 512, &full[st.s]);
@@ -857,7 +895,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && mbar_wait(done, 0, abort_flag, status, 0x28000000u)) {
             tc_fence_after();
-            const long long off = ((static_cast<long long>(b) * p.S + k0s + lane_row) * p.Hkv + hk) * D + hw * (D / 2);
+            const int krow = SP ? striped_row(key, p.st_n, L) : k0s + lane_row;  // storage row of the key
+            const long long off = ((static_cast<long long>(b) * p.S + krow) * p.Hkv + hk) * D + hw * (D / 2);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t r[32];
@@ -883,18 +922,18 @@ cudaError_t set_smem(K kernel, int bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int D, bool LAY>
+template <int D, bool LAY, bool SP = false>
 cudaError_t launch_tc(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
                       const CUtensorMap& tv, cudaStream_t stream) {
     using C = BwdCfg<D>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = set_smem(bwd_dkdv_kernel<D, LAY>, C::kKvSmem);
-        if (attr_err == cudaSuccess) attr_err = set_smem(bwd_dq_kernel<D, LAY>, C::kDqSmem);
+        attr_err = set_smem(bwd_dkdv_kernel<D, LAY, SP>, C::kKvSmem);
+        if (attr_err == cudaSuccess) attr_err = set_smem(bwd_dq_kernel<D, LAY, SP>, C::kDqSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    bwd_dkdv_kernel<D, LAY><<<p.B * p.Hkv * p.n_tiles, kThreads, C::kKvSmem, stream>>>(tq, tdo, tk, tv, p);
+    bwd_dkdv_kernel<D, LAY, SP><<<p.B * p.Hkv * p.n_tiles, kThreads, C::kKvSmem, stream>>>(tq, tdo, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -907,7 +946,7 @@ cudaError_t launch_tc(const BwdParams& p, const CUtensorMap& tq, const CUtensorM
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D, LAY>, tq, tdo, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, bwd_dq_kernel<D, LAY, SP>, tq, tdo, tk, tv, p);
 }
 
 BwdParams make_params(const BwdArgs& a, int out_f32, int tile) {
@@ -933,15 +972,15 @@ BwdParams make_params(const BwdArgs& a, int out_f32, int tile) {
 }
 
 template <typename T>
-cudaError_t launch_prep(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_prep(const BwdArgs& a, cudaStream_t stream, int st_n = 0) {
     const long long rows = static_cast<long long>(a.B) * a.Hq * a.S;
     const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
     const T* o = static_cast<const T*>(a.out);
     const T* d = static_cast<const T*>(a.dout);
     if (a.D == 128)
-        bwd_prep_kernel<T, 128><<<grid, 256, 0, stream>>>(o, d, a.lse, a.ws_delta, a.ws_lse2, rows, a.S, a.Hq);
+        bwd_prep_kernel<T, 128><<<grid, 256, 0, stream>>>(o, d, a.lse, a.ws_delta, a.ws_lse2, rows, a.S, a.Hq, st_n);
     else
-        bwd_prep_kernel<T, 64><<<grid, 256, 0, stream>>>(o, d, a.lse, a.ws_delta, a.ws_lse2, rows, a.S, a.Hq);
+        bwd_prep_kernel<T, 64><<<grid, 256, 0, stream>>>(o, d, a.lse, a.ws_delta, a.ws_lse2, rows, a.S, a.Hq, st_n);
     return cudaGetLastError();
 }
 
@@ -1109,7 +1148,9 @@ __global__ void __launch_bounds__(kSimtRows * (D / 32)) bwd_dkdv_simt_kernel(con
 }  // namespace
 
 cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t stream) {
-    cudaError_t e = launch_prep<__nv_bfloat16>(a, stream);
+    // causal striped with N dividing 128: the contiguous kernels over positions
+    const int st_n = (a.causal && a.layout == kLayoutStriped && 128 % a.n_shards == 0) ? a.n_shards : 0;
+    cudaError_t e = launch_prep<__nv_bfloat16>(a, stream, st_n);
     if (e != cudaSuccess) return e;
     BwdParams p = make_params(a, 0, kT);
     const unsigned long long D = a.D, esz = 2;
@@ -1131,6 +1172,25 @@ cudaError_t launch_bwd_tc(const BwdArgs& a, cudaStream_t stream) {
         p.n_shards = 2 * a.n_shards;
         p.zz_n = a.n_shards;
         p.zz_half = a.S / (2 * a.n_shards);
+    }
+    if (st_n) {
+        // a tile of 128 consecutive positions holds 128/N rows of every shard: one 5-D box
+        // [64 cols, 1 head, N shards, 128/N rows, 1 batch] per 64 columns lands it in position
+        // order, and the contiguous kernels walk positions (N position-order shards)
+        p.layout = kLayoutContiguous;
+        p.st_n = st_n;
+        const unsigned long long L = a.S / a.n_shards, N = a.n_shards, S = a.S, B = a.B;
+        const unsigned long long qd5[5] = {D, (unsigned long long)a.Hq, N, L, B};
+        const unsigned long long qs5[4] = {D * esz, L * a.Hq * D * esz, a.Hq * D * esz, S * a.Hq * D * esz};
+        const unsigned long long kd5[5] = {D, (unsigned long long)a.Hkv, N, L, B};
+        const unsigned long long ks5[4] = {D * esz, L * a.Hkv * D * esz, a.Hkv * D * esz, S * a.Hkv * D * esz};
+        const unsigned box5[5] = {64, 1, (unsigned)N, (unsigned)(128 / N), 1};
+        CUtensorMap tq5, tdo5, tk5, tv5;
+        if (!make_map_5d(&tq5, a.q, qd5, qs5, box5) || !make_map_5d(&tdo5, a.dout, qd5, qs5, box5) ||
+            !make_map_5d(&tk5, a.k, kd5, ks5, box5) || !make_map_5d(&tv5, a.v, kd5, ks5, box5))
+            return cudaErrorInvalidValue;
+        return a.D == 128 ? launch_tc<128, false, true>(p, tq5, tdo5, tk5, tv5, stream)
+                          : launch_tc<64, false, true>(p, tq5, tdo5, tk5, tv5, stream);
     }
     // without a causal mask every layout is the same walk
     if (a.causal && p.layout != kLayoutContiguous)

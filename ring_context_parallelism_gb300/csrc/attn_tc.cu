@@ -24,8 +24,10 @@
 // for tile 1.  TMEM: tile t uses columns [256t, 256t+128) for S (P~ overwrites
 // its first half as packed bf16) and [256t+128, 256t+128+D) for O.
 //
-// Kernel modes: the ring prefill over contiguous shards, the same walk over
-// causal zigzag / striped shards (ra_walk.h), and the fan-out (stacked branch
+// Kernel modes: the ring prefill over contiguous shards (which also runs causal
+// zigzag shards, through their chunk map, and causal striped shards over
+// positions), the layouts' own rings (ra_walk.h) for striped shard counts that do
+// not divide 128 and for per-shard partials, and the fan-out (stacked branch
 // rows against a prefix chunk plus folded private suffixes; decode, prefill with
 // a causal suffix, or a paged KV pool), whose units split their KV tiles over
 // the two softmax slots (one row tile) or pair two row tiles.
@@ -1301,6 +1303,11 @@ static bool make_map_nd(CUtensorMap* m, const void* base, int rank, const unsign
 bool make_map(CUtensorMap* m, const void* base, const unsigned long long dims[4], const unsigned long long strides[3],
               const unsigned box[4]) {
     return make_map_nd(m, base, 4, dims, strides, box);
+}
+
+bool make_map_5d(CUtensorMap* m, const void* base, const unsigned long long dims[5],
+                 const unsigned long long strides[4], const unsigned box[5]) {
+    return make_map_nd(m, base, 5, dims, strides, box);
 }
 
 cudaError_t launch_ring_tc(const RingTcArgs& a, cudaStream_t stream) {

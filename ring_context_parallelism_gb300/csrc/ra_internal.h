@@ -115,6 +115,9 @@ cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t stream);
 // kernels.  Returns false if the driver entry point or the encode fails.
 bool make_map(CUtensorMap* m, const void* base, const unsigned long long dims[4], const unsigned long long strides[3],
               const unsigned box[4]);
+// The same for 5 dims (strides for dims 1..4, box of 5).
+bool make_map_5d(CUtensorMap* m, const void* base, const unsigned long long dims[5],
+                 const unsigned long long strides[4], const unsigned box[5]);
 
 // Backward pass (dQ, dK, dV) for an upstream gradient dO.  ws_delta / ws_lse2:
 // workspace [B, Hq, S] fp32 each (rowsum(dO * O), lse * log2 e).
