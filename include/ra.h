@@ -103,7 +103,9 @@ ra_status ra_blockwise_attn_fwd(const void* q, const void* k, const void* v, voi
  * storage row; the causal mask compares the rows' sequence positions.
  * Striped: each query tile walks the KV shards in the same ring order, taking
  * from each shard the prefix of its rows that the tile can see (positions
- * increase along a shard's rows in every layout).  Zigzag: the causal walk
+ * increase along a shard's rows in every layout); when n_shards divides 128
+ * the causal walk runs over positions instead (tiles of 128 consecutive
+ * positions, 128 / n_shards rows of every shard).  Zigzag: the causal walk
  * runs in sequence-position order over the 2 n_shards chunks of the zigzag
  * cut (the query's own chunk, then the earlier ones: the contiguous ring over
  * those chunks), each tile of rows addressed through the layout; it visits the
@@ -184,7 +186,9 @@ ra_status ra_blockwise_attn_bwd(const void* q, const void* k, const void* v, con
  * shard the suffix of its rows that can see a KV tile (positions increase
  * along a shard's rows in every layout).  A causal zigzag sequence is walked,
  * as in the forward, over the 2 n_shards chunks of its cut in sequence-position
- * order (rounding differs only).  Other arguments, rules and errors
+ * order, and a causal striped one with n_shards dividing 128 over positions
+ * (tiles of 128 consecutive positions; rounding differs only).  Other
+ * arguments, rules and errors
  * as ra_blockwise_attn_bwd and ra_blockwise_attn_fwd_layout.
  */
 ra_status ra_blockwise_attn_bwd_layout(const void* q, const void* k, const void* v, const void* out,
