@@ -393,10 +393,12 @@ int ra_tile_launch_order(int S, int n_shards, int layout, int tile_rows, int* ro
  * it), KV tiles of `tile` keys.  Writes, for each visited shard in ring order,
  * shard_order[t] and visible_keys[t] (the keys of that shard the tile's last
  * row can see, a prefix of the shard's rows; the shard length when not
- * causal), and *total_tiles = the KV tiles the kernels walk for this tile
- * (the zigzag forward and backward take the same tiles in the order of the
- * 2 n_shards chunks, i.e. this call with RA_LAYOUT_CONTIGUOUS and
- * 2 n_shards shards on sequence positions).
+ * causal), and *total_tiles = the KV tiles the layout's own ring walk takes
+ * for this tile (the per-shard partials, and striped with n_shards not
+ * dividing 128).  The single-output zigzag kernels take the same keys in the
+ * order of the 2 n_shards chunks (this call with RA_LAYOUT_CONTIGUOUS and
+ * 2 n_shards shards on sequence positions); the striped ones with n_shards
+ * dividing 128 walk sequence positions (RA_LAYOUT_CONTIGUOUS, n_shards shards).
  * Shards after the returned count see nothing.  Arrays hold n_shards ints.
  * Returns the number of visited shards, or -1 on invalid arguments.
  */
