@@ -97,35 +97,58 @@ struct BwdParams {
 // ---------------------------------------------------------------------------
 // preparation: Delta = rowsum(dO * O), lse2 = lse * log2(e)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+// E consecutive elements of a row (E = D / 32: one 4-, 8- or 16-byte load per lane).
+template <int E>
+__device__ __forceinline__ void load_row(const float* src, float* v) {
+    if constexpr (E == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+    } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        v[0] = x.x, v[1] = x.y;
+    }
+}
+template <int E>
+__device__ __forceinline__ void load_row(const __nv_bfloat16* src, float* v) {
+    if constexpr (E == 4) {
+        const uint2 x = *reinterpret_cast<const uint2*>(src);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
+        v[0] = a.x, v[1] = a.y, v[2] = b.x, v[3] = b.y;
+    } else {
+        const uint32_t x = *reinterpret_cast<const uint32_t*>(src);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x));
+        v[0] = a.x, v[1] = a.y;
+    }
+}
 
-// One warp per (b, h, i) row; rows ordered (b, h, i) so that a block's results
-// are consecutive.
+// One warp per row, rows in memory order ((b, i, h), h fastest: a block reads 8
+// consecutive rows of [B, S, Hq, D]); lane l holds head dims [l E, l E + E).
+// HBM-bound: reads O and dO once.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* out, const T* dout, const float* lse, float* delta,
                                                       float* lse2, long long rows, int S, int Hq, int st_n) {
+    constexpr int E = D / 32;
     const long long w = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= rows) return;
-    const int i = static_cast<int>(w % S);
-    const long long bh = w / S;
-    const int h = static_cast<int>(bh % Hq);
-    const long long b = bh / Hq;
-    const long long base = ((b * S + i) * Hq + h) * D;
+    float o[E], g[E];
+    load_row<E>(out + w * D + lane * E, o);
+    load_row<E>(dout + w * D + lane * E, g);
     float acc = 0.f;
 #pragma unroll
-    for (int e = 0; e < D / 32; ++e) {
-        const int d = lane + 32 * e;
-        acc = fmaf(to_f(out[base + d]), to_f(dout[base + d]), acc);
-    }
+    for (int e = 0; e < E; ++e) acc = fmaf(o[e], g[e], acc);
 #pragma unroll
     for (int x = 16; x > 0; x >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
     if (lane == 0) {
+        const int h = static_cast<int>(w % Hq);
+        const long long bi = w / Hq;
+        const int i = static_cast<int>(bi % S);
+        const long long bh = (bi / S) * Hq + h;
         // striped rows walked over positions: Delta and lse2 stored at the row's position
-        const long long wo = st_n ? w - i + (i % (S / st_n)) * st_n + i / (S / st_n) : w;
-        delta[wo] = acc;
-        lse2[wo] = lse[w] * kLog2e;
+        const int ip = st_n ? (i % (S / st_n)) * st_n + i / (S / st_n) : i;
+        delta[bh * S + ip] = acc;
+        lse2[bh * S + ip] = lse[bh * S + i] * kLog2e;
     }
 }
 
