@@ -426,6 +426,9 @@ def run_ours(args, rank, world):
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                "h2d_GB_per_s_alone": h2d_gbs, "d2h_GB_per_s_alone": d2h_gbs,
                "bound": "copies" if copy_ms > ms_step else "kernel",
+               # the step against what bounds it: 1.0 when the copies hide fully behind the kernel
+               # (or the kernel behind the copies)
+               "pipeline_efficiency": max(copy_ms, ms_step) / e2e_ms,
                "host_numa_node": numa_node, "pinned_alloc_cpus": numa_cpus}
         del qh, kh, vh, slots, hin, hout
 
